@@ -1,0 +1,189 @@
+"""Exact IO-aware attention on GB300: the Python binding of libfa.so.
+
+Thin argument marshalling over the C ABI declared in ``include/fa.h``: every
+step of the computation runs in the library's CUDA kernels; PyTorch only
+supplies device memory and the current stream. There is no fallback: when
+the library is missing or the device is not a CC 10.3 GPU, the calls raise.
+
+The functions carry the C entry points' names:
+
+    fa_fwd(q, k, v, causal=False, scale=None)        -> (o, lse)
+    fa_bwd(q, k, v, o, lse, do, causal=False, scale=None) -> (dq, dk, dv)
+    fa_bwd_workspace_bytes(B, H, N, d)
+    fa_strerror(code), fa_get_last_device_status(), fa_version()
+
+q, k, v, o, do: bfloat16 CUDA tensors [B, H, N, d], contiguous; lse: float32
+[B, H, N]. ``scale`` defaults to 1/sqrt(d) as in the dense attention block of
+"FlashAttention -- the same attention, made memory-aware", section 00.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+from .accounting import (flops_fwd, flops_bwd, bytes_fwd, bytes_bwd,  # noqa: F401
+                         transfer_ledger)
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libfa.so")
+
+FA_OK = 0
+FA_ERR_INVALID = -1
+FA_ERR_UNSUPPORTED = -2
+FA_ERR_LAUNCH = -3
+FA_ERR_TIMEOUT = -4
+FA_ERR_WORKSPACE = -5
+
+# Every symbol include/fa.h declares, with (restype, argtypes).
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_F = ctypes.c_float
+_S = ctypes.c_size_t
+SIGNATURES = {
+    "fa_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F]),
+    "fa_fwd_stream": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P]),
+    "fa_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F]),
+    "fa_bwd_stream": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P, _S, _P]),
+    "fa_bwd_workspace_bytes": (_S, [_I, _I, _I, _I]),
+    "fa_strerror": (ctypes.c_char_p, [_I]),
+    "fa_get_last_device_status": (_I, []),
+    "fa_version": (_I, []),
+}
+
+
+class FAError(RuntimeError):
+    """A libfa call returned a non-zero code."""
+
+    def __init__(self, code: int, what: str):
+        self.code = code
+        super().__init__(f"{what}: {fa_strerror(code)} (code {code})")
+
+
+_lib = None
+
+
+def load_library(path: str | None = None) -> ctypes.CDLL:
+    """Load libfa.so (once) and declare its signatures. Raises if missing."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise ImportError(
+            f"libfa.so is not built ({p}); run `python -m exact_io_aware_33_gb300.build` "
+            "or __graft_entry__.build() first")
+    lib = ctypes.CDLL(p)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def fa_version() -> int:
+    return load_library().fa_version()
+
+
+def fa_strerror(code: int) -> str:
+    try:
+        return load_library().fa_strerror(int(code)).decode()
+    except ImportError:
+        return f"code {code}"
+
+
+def fa_get_last_device_status() -> int:
+    return load_library().fa_get_last_device_status()
+
+
+def fa_bwd_workspace_bytes(B: int, H: int, N: int, d: int) -> int:
+    return load_library().fa_bwd_workspace_bytes(B, H, N, d)
+
+
+def _check(code: int, what: str):
+    if code != FA_OK:
+        raise FAError(code, what)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None and t.numel() > 0 else ctypes.c_void_p(0)
+
+
+def _stream_handle(stream, device):
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check_tensor(t, name, shape, dtype):
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name} must be a CUDA tensor (no CPU path exists)")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def fa_fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None,
+           stream=None):
+    """Exact attention forward; returns (o bf16 [B,H,N,d], lse fp32 [B,H,N])."""
+    import torch
+    if q.dim() != 4:
+        raise ValueError("q must be [B, H, N, d]")
+    B, H, N, d = q.shape
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _check_tensor(t, name, (B, H, N, d), torch.bfloat16)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    _check_tensor(out, "out", (B, H, N, d), torch.bfloat16)
+    _check_tensor(lse, "lse", (B, H, N), torch.float32)
+    lib = load_library()
+    with torch.cuda.device(q.device):
+        rc = lib.fa_fwd_stream(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, N, d,
+                               int(bool(causal)), float(scale), _stream_handle(stream, q.device))
+    _check(rc, "fa_fwd")
+    return out, lse
+
+
+def fa_bwd(q, k, v, o, lse, do, causal: bool = False, scale: float | None = None, dq=None,
+           dk=None, dv=None, workspace=None, stream=None):
+    """Exact attention backward by recomputation; returns (dq, dk, dv) bf16."""
+    import torch
+    if q.dim() != 4:
+        raise ValueError("q must be [B, H, N, d]")
+    B, H, N, d = q.shape
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("do", do)):
+        _check_tensor(t, name, (B, H, N, d), torch.bfloat16)
+    _check_tensor(lse, "lse", (B, H, N), torch.float32)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
+        _check_tensor(t, name, (B, H, N, d), torch.bfloat16)
+    lib = load_library()
+    need = lib.fa_bwd_workspace_bytes(B, H, N, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    if workspace.numel() < need:
+        raise ValueError(f"workspace needs {need} bytes")
+    with torch.cuda.device(q.device):
+        rc = lib.fa_bwd_stream(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do), _ptr(dq),
+                               _ptr(dk), _ptr(dv), B, H, N, d, int(bool(causal)), float(scale),
+                               _ptr(workspace), ctypes.c_size_t(workspace.numel()),
+                               _stream_handle(stream, q.device))
+    _check(rc, "fa_bwd")
+    return dq, dk, dv

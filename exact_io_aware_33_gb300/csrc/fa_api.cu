@@ -1,0 +1,233 @@
+// C ABI of libfa.so: argument checks, TMA tensor maps, the device status
+// word, and the extern "C" entry points declared in fa.h.
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "fa.h"
+#include "fa_internal.h"
+#include "sm103_ptx.cuh"
+
+namespace fa {
+
+// One status word per device: set by a kernel whose bounded wait ran out.
+__device__ int g_status_word;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int kSmemSlots = 16;
+
+struct DeviceState {
+  bool probed = false;
+  bool supported = false;
+  int* status = nullptr;
+  bool smem_set[kSmemSlots] = {};
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+EncodeTiledFn encode_fn() {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+  }
+  return g_encode;
+}
+
+// Current device, checked once: compute capability 10.3 (GB300).
+int current_device(DeviceState** st) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA_ERR_LAUNCH;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceState& s = g_dev[dev];
+  if (!s.probed) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return FA_ERR_LAUNCH;
+    s.supported = (major == 10 && minor == 3);
+    void* addr = nullptr;
+    if (s.supported) {
+      if (cudaGetSymbolAddress(&addr, g_status_word) != cudaSuccess) return FA_ERR_LAUNCH;
+      s.status = static_cast<int*>(addr);
+    }
+    s.probed = true;
+  }
+  *st = &s;
+  return s.supported ? FA_OK : FA_ERR_UNSUPPORTED;
+}
+
+bool aligned16(const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Common checks of both passes. Returns FA_OK, or an error code; sets
+// *empty when there is nothing to compute.
+int check_problem(int B, int H, int N, int d, float scale, bool* empty) {
+  *empty = false;
+  if (B < 0 || H < 0 || N < 0) return FA_ERR_INVALID;
+  if (!std::isfinite(scale) || scale < 0.f) return FA_ERR_INVALID;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (B == 0 || H == 0 || N == 0) {
+    *empty = true;
+    return FA_OK;
+  }
+  const long long bh = static_cast<long long>(B) * H;
+  if (bh > (1LL << 31) - 1) return FA_ERR_INVALID;
+  // TMA coordinates and tensor extents are 32-bit; keep element offsets in range.
+  if (bh * static_cast<long long>(N) * d > (1LL << 46)) return FA_ERR_INVALID;
+  return FA_OK;
+}
+
+}  // namespace
+
+bool make_map_bhnd(CUtensorMap* map, const void* ptr, int BH, int N, int d) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+                              static_cast<cuuint64_t>(BH)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
+                                 static_cast<cuuint64_t>(N) * static_cast<cuuint64_t>(d) * 2};
+  const cuuint32_t box[3] = {64, 128, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r =
+      enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box,
+          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+int* device_status_word() {
+  DeviceState* st = nullptr;
+  if (current_device(&st) != FA_OK) return nullptr;
+  return st->status;
+}
+
+bool ensure_smem_attr(const void* func, int bytes, int slot) {
+  DeviceState* st = nullptr;
+  if (current_device(&st) != FA_OK || slot < 0 || slot >= kSmemSlots) return false;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!st->smem_set[slot]) {
+    if (cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) !=
+        cudaSuccess)
+      return false;
+    st->smem_set[slot] = true;
+  }
+  return true;
+}
+
+}  // namespace fa
+
+using fa::Problem;
+
+extern "C" {
+
+int fa_version(void) { return 100; }
+
+const char* fa_strerror(int code) {
+  switch (code) {
+    case FA_OK: return "success";
+    case FA_ERR_INVALID: return "invalid argument (pointer, size, alignment or scale)";
+    case FA_ERR_UNSUPPORTED: return "unsupported (head size must be 64 or 128; device must be CC 10.3)";
+    case FA_ERR_LAUNCH: return "a CUDA call failed (launch, attribute or tensor map)";
+    case FA_ERR_TIMEOUT: return "a bounded wait inside a kernel ran out";
+    case FA_ERR_WORKSPACE: return "workspace missing or too small";
+    default: return "unknown error code";
+  }
+}
+
+int fa_fwd_stream(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                  int N, int d, int causal, float scale, void* cuda_stream) {
+  bool empty = false;
+  int rc = fa::check_problem(B, H, N, d, scale, &empty);
+  if (rc != FA_OK || empty) return rc;
+  if (!fa::aligned16(q) || !fa::aligned16(k) || !fa::aligned16(v) || !fa::aligned16(o) ||
+      !fa::aligned16(lse))
+    return FA_ERR_INVALID;
+  fa::DeviceState* st = nullptr;
+  rc = fa::current_device(&st);
+  if (rc != FA_OK) return rc;
+  Problem p{q, k, v, B, H, N, d, causal, scale};
+  return fa::launch_fwd(p, o, lse, static_cast<cudaStream_t>(cuda_stream));
+}
+
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
+           int d, int causal, float scale) {
+  return fa_fwd_stream(q, k, v, o, lse, B, H, N, d, causal, scale, nullptr);
+}
+
+size_t fa_bwd_workspace_bytes(int B, int H, int N, int d) {
+  if (B <= 0 || H <= 0 || N <= 0 || d <= 0) return 0;
+  return fa::bwd_workspace_bytes(B, H, N, d);
+}
+
+int fa_bwd_stream(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                  const void* dO, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+                  int causal, float scale, void* workspace, size_t ws_bytes, void* cuda_stream) {
+  bool empty = false;
+  int rc = fa::check_problem(B, H, N, d, scale, &empty);
+  if (rc != FA_OK || empty) return rc;
+  const void* ptrs[] = {q, k, v, o, lse, dO, dq, dk, dv};
+  for (const void* ptr : ptrs)
+    if (!fa::aligned16(ptr)) return FA_ERR_INVALID;
+  if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
+      ws_bytes < fa::bwd_workspace_bytes(B, H, N, d))
+    return FA_ERR_WORKSPACE;
+  fa::DeviceState* st = nullptr;
+  rc = fa::current_device(&st);
+  if (rc != FA_OK) return rc;
+  Problem p{q, k, v, B, H, N, d, causal, scale};
+  return fa::launch_bwd(p, o, lse, dO, dq, dk, dv, workspace,
+                        static_cast<cudaStream_t>(cuda_stream));
+}
+
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+           const void* dO, void* dq, void* dk, void* dv, int B, int H, int N, int d, int causal,
+           float scale) {
+  bool empty = false;
+  int rc = fa::check_problem(B, H, N, d, scale, &empty);
+  if (rc != FA_OK || empty) return rc;
+  const void* ptrs[] = {q, k, v, o, lse, dO, dq, dk, dv};
+  for (const void* ptr : ptrs)
+    if (!fa::aligned16(ptr)) return FA_ERR_INVALID;
+  fa::DeviceState* st = nullptr;
+  rc = fa::current_device(&st);
+  if (rc != FA_OK) return rc;
+  const size_t bytes = fa::bwd_workspace_bytes(B, H, N, d);
+  void* ws = nullptr;
+  if (cudaMallocAsync(&ws, bytes, nullptr) != cudaSuccess) return FA_ERR_LAUNCH;
+  rc = fa_bwd_stream(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, causal, scale, ws, bytes,
+                     nullptr);
+  if (cudaFreeAsync(ws, nullptr) != cudaSuccess && rc == FA_OK) rc = FA_ERR_LAUNCH;
+  return rc;
+}
+
+int fa_get_last_device_status(void) {
+  fa::DeviceState* st = nullptr;
+  if (fa::current_device(&st) != FA_OK) return FA_ERR_LAUNCH;
+  if (cudaDeviceSynchronize() != cudaSuccess) return FA_ERR_LAUNCH;
+  int word = 0;
+  if (cudaMemcpyFromSymbol(&word, fa::g_status_word, sizeof(int)) != cudaSuccess)
+    return FA_ERR_LAUNCH;
+  const int zero = 0;
+  if (cudaMemcpyToSymbol(fa::g_status_word, &zero, sizeof(int)) != cudaSuccess)
+    return FA_ERR_LAUNCH;
+  return word == fa::kStatusTimeout ? FA_ERR_TIMEOUT : FA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,435 @@
+// Forward pass of exact attention on sm_103a.
+//
+// Method ("Flash Attention: IO-Aware Exact Attention", sections "Online
+// softmax makes tiling exact" and "Loop order changes which data is
+// reloaded"): a block of query rows stays on chip with its row state while
+// every key/value tile streams past; per row the kernel carries a running
+// maximum m, a denominator l and an unnormalised numerator a, rescales the
+// old sums by alpha = exp(m_old - m_new) when the maximum moves, and divides
+// once at the end. Scores S and probabilities P exist only in tensor memory.
+//
+// CTA organisation (320 threads, one CTA per SM):
+//   warps 0-3  softmax warpgroup of query tile 0 (thread = row = TMEM lane)
+//   warps 4-7  softmax warpgroup of query tile 1
+//   warp  8    tcgen05 MMA issue (one thread) and TMEM allocation
+//   warp  9    TMA producer (one thread)
+// Each CTA owns 256 query rows of one (batch, head): two 128-row tiles that
+// ping-pong, so the tensor core works on one tile's QK^T / PV while the
+// other tile's softmax runs.
+//
+// Tensor memory (512 columns x 128 lanes, fp32):
+//   [  0,128)  S of tile 0; its first 64 columns are overwritten by P (bf16
+//              pairs) which the P.V MMA reads straight from TMEM
+//   [128,256)  S / P of tile 1
+//   [256,256+d)      O accumulator of tile 0
+//   [256+d,256+2d)   O accumulator of tile 1
+//
+// Shared memory: Q tiles (2 x 128 x d bf16), and rings of K and V tiles
+// (stages x 128 x d bf16 each), all in the 128-byte-swizzled layout TMA
+// writes and the tensor core reads; d = 128 is stored as two 64-column
+// halves. The online-softmax statistics never leave registers.
+//
+// Exactness note: the reference maximum of a row only moves when a tile's
+// maximum exceeds it by more than 2^8 in the exponent (log2 units); until
+// then exp2(s - m_ref) <= 256 is summed as is. Final division and LSE use
+// the same m_ref, so the result is the same function -- only rounding
+// changes.
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "fa_internal.h"
+#include "sm103_ptx.cuh"
+
+namespace fa {
+namespace {
+
+constexpr int kBlockM = 128;
+constexpr int kBlockN = 128;
+constexpr int kQTiles = 2;
+constexpr int kSoftmaxThreads = 128 * kQTiles;
+constexpr int kMmaWarp = kSoftmaxThreads / 32;
+constexpr int kLoadWarp = kMmaWarp + 1;
+constexpr int kThreads = kSoftmaxThreads + 64;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+constexpr float kLn2 = 0.6931471805599453f;
+
+template <int D>
+struct FwdCfg {
+  static constexpr int kChunks = D / 64;
+  static constexpr int kChunkBytes = kBlockM * 64 * 2;      // 16 KiB
+  static constexpr int kTileBytes = kChunks * kChunkBytes;  // 128 rows x d
+  static constexpr int kStages = (D == 64) ? 4 : 2;
+  static constexpr int kQOff = 0;
+  static constexpr int kKOff = kQOff + kQTiles * kTileBytes;
+  static constexpr int kVOff = kKOff + kStages * kTileBytes;
+  static constexpr int kBarOff = kVOff + kStages * kTileBytes;
+  // barrier indices
+  static constexpr int kBarQFull = 0;
+  static constexpr int kBarKFull = 1;
+  static constexpr int kBarKEmpty = kBarKFull + kStages;
+  static constexpr int kBarVFull = kBarKEmpty + kStages;
+  static constexpr int kBarVEmpty = kBarVFull + kStages;
+  static constexpr int kBarSFull = kBarVEmpty + kStages;
+  static constexpr int kBarPFull = kBarSFull + kQTiles;
+  static constexpr int kBarOFinal = kBarPFull + kQTiles;
+  static constexpr int kBarDrain = kBarOFinal + kQTiles;
+  static constexpr int kNumBars = kBarDrain + 1;
+  static constexpr int kMiscOff = kBarOff + kNumBars * 8;
+  static constexpr int kSmemBytes = kMiscOff + 16 + 1024;  // + slack to align the base
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr uint32_t kColO = 256;
+};
+
+struct FwdArgs {
+  __nv_bfloat16* o;
+  float* lse;
+  int* status;
+  int N;
+  int BH;
+  int causal;
+  int num_pairs;
+  float scale_log2;  // scale * log2(e), > 0
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                  const __grid_constant__ CUtensorMap tmV, const FwdArgs args) {
+  using C = FwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_u32 = smem_u32(smem_raw);
+  const uint32_t base = (raw_u32 + 1023u) & ~1023u;
+  uint8_t* base_ptr = smem_raw + (base - raw_u32);
+  auto bar = [&](int i) -> uint32_t { return base + C::kBarOff + 8u * i; };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base_ptr + C::kMiscOff);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(base_ptr + C::kMiscOff + 4);
+
+  const int N = args.N;
+  const int bh = blockIdx.x % args.BH;
+  const int pair = args.num_pairs - 1 - static_cast<int>(blockIdx.x / args.BH);
+  const int n_kv = (N + kBlockN - 1) / kBlockN;
+  int q_row0[kQTiles], n_t[kQTiles];
+#pragma unroll
+  for (int t = 0; t < kQTiles; ++t) {
+    q_row0[t] = pair * (kBlockM * kQTiles) + t * kBlockM;
+    if (q_row0[t] >= N) n_t[t] = 0;
+    else n_t[t] = args.causal ? (q_row0[t] / kBlockN + 1) : n_kv;
+  }
+  const int n_max = n_t[0] > n_t[1] ? n_t[0] : n_t[1];
+
+  const int warp = warp_id();
+  const int lane = lane_id();
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(C::kBarQFull), 1);
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(bar(C::kBarKFull + s), 1);
+      mbar_init(bar(C::kBarKEmpty + s), 1);
+      mbar_init(bar(C::kBarVFull + s), 1);
+      mbar_init(bar(C::kBarVEmpty + s), 1);
+    }
+    for (int t = 0; t < kQTiles; ++t) {
+      mbar_init(bar(C::kBarSFull + t), 1);
+      mbar_init(bar(C::kBarPFull + t), 128);
+      mbar_init(bar(C::kBarOFinal + t), 1);
+    }
+    mbar_init(bar(C::kBarDrain), 1);
+    *abort_flag = 0;
+    mbar_fence_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == kLoadWarp) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_map(&tmQ);
+      tma_prefetch_map(&tmK);
+      tma_prefetch_map(&tmV);
+      uint32_t q_bytes = 0;
+      for (int t = 0; t < kQTiles; ++t)
+        if (n_t[t] > 0) q_bytes += C::kTileBytes;
+      mbar_arrive_expect_tx(bar(C::kBarQFull), q_bytes);
+      for (int t = 0; t < kQTiles; ++t) {
+        if (n_t[t] == 0) continue;
+        for (int c = 0; c < C::kChunks; ++c)
+          tma_load_3d(base + C::kQOff + t * C::kTileBytes + c * C::kChunkBytes, &tmQ,
+                      bar(C::kBarQFull), c * 64, q_row0[t], bh);
+      }
+      int issued = 0;
+      bool ok = true;
+      for (int j = 0; j < n_max && ok; ++j) {
+        const int s = j % C::kStages;
+        const uint32_t ph = ((j / C::kStages) + 1) & 1;
+        if (j >= C::kStages) ok = mbar_wait(bar(C::kBarKEmpty + s), ph, abort_flag);
+        if (!ok) break;
+        mbar_arrive_expect_tx(bar(C::kBarKFull + s), C::kTileBytes);
+        for (int c = 0; c < C::kChunks; ++c)
+          tma_load_3d(base + C::kKOff + s * C::kTileBytes + c * C::kChunkBytes, &tmK,
+                      bar(C::kBarKFull + s), c * 64, j * kBlockN, bh);
+        if (j >= C::kStages) ok = mbar_wait(bar(C::kBarVEmpty + s), ph, abort_flag);
+        if (!ok) {
+          issued = 2 * j + 1;
+          break;
+        }
+        mbar_arrive_expect_tx(bar(C::kBarVFull + s), C::kTileBytes);
+        for (int c = 0; c < C::kChunks; ++c)
+          tma_load_3d(base + C::kVOff + s * C::kTileBytes + c * C::kChunkBytes, &tmV,
+                      bar(C::kBarVFull + s), c * 64, j * kBlockN, bh);
+        issued = 2 * j + 2;
+      }
+      if (*abort_flag) {
+        // Let every copy this thread started land before the CTA exits.
+        mbar_wait(bar(C::kBarQFull), 0, nullptr);
+        for (int x = issued - 1; x >= 0 && x >= issued - 2 * C::kStages; --x) {
+          const int j = x >> 1;
+          const int s = j % C::kStages;
+          const int b = (x & 1) ? (C::kBarVFull + s) : (C::kBarKFull + s);
+          mbar_wait(bar(b), (j / C::kStages) & 1, nullptr);
+        }
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------ MMA issue
+    if (lane == 0) {
+      constexpr uint32_t kIdS = idesc_bf16_f32(kBlockM, kBlockN, false, false);
+      constexpr uint32_t kIdO = idesc_bf16_f32(kBlockM, D, false, true);
+      bool ok = mbar_wait(bar(C::kBarQFull), 0, abort_flag);
+      tc_fence_after();
+      int k_ready = -1;
+      auto ensure_k = [&](int j) {
+        if (ok && j > k_ready) {
+          ok = mbar_wait(bar(C::kBarKFull + j % C::kStages), (j / C::kStages) & 1, abort_flag);
+          tc_fence_after();
+          k_ready = j;
+        }
+      };
+      auto issue_s = [&](int t, int j) {
+        const uint32_t qb = base + C::kQOff + t * C::kTileBytes;
+        const uint32_t kb = base + C::kKOff + (j % C::kStages) * C::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
+          mma_ss(tmem + t * 128, sdesc_sw128(qb + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024),
+                 kIdS, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(bar(C::kBarSFull + t));
+      };
+      auto issue_pv = [&](int t, int j) {
+        const uint32_t vb = base + C::kVOff + (j % C::kStages) * C::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < kBlockN / 16; ++kk) {
+          mma_ts(tmem + C::kColO + t * D, tmem + t * 128 + kk * 8,
+                 sdesc_sw128(vb + kk * 2048, C::kChunkBytes, 1024), kIdO,
+                 (j > 0 || kk > 0) ? 1u : 0u);
+        }
+      };
+      ensure_k(0);
+      if (ok) {
+        for (int t = 0; t < kQTiles; ++t)
+          if (n_t[t] > 0) issue_s(t, 0);
+        mma_commit(bar(C::kBarKEmpty + 0));
+      }
+      for (int j = 0; j < n_max && ok; ++j) {
+        ok = mbar_wait(bar(C::kBarVFull + j % C::kStages), (j / C::kStages) & 1, abort_flag);
+        tc_fence_after();
+        for (int t = 0; t < kQTiles && ok; ++t) {
+          if (j >= n_t[t]) continue;
+          ok = mbar_wait(bar(C::kBarPFull + t), j & 1, abort_flag);
+          if (!ok) break;
+          tc_fence_after();
+          issue_pv(t, j);
+          if (j + 1 < n_t[t]) {
+            ensure_k(j + 1);
+            if (!ok) break;
+            issue_s(t, j + 1);
+          } else {
+            mma_commit(bar(C::kBarOFinal + t));
+          }
+        }
+        if (!ok) break;
+        mma_commit(bar(C::kBarVEmpty + j % C::kStages));
+        if (j + 1 < n_max) mma_commit(bar(C::kBarKEmpty + (j + 1) % C::kStages));
+      }
+      // Let every MMA this thread issued finish before TMEM is released.
+      mma_commit(bar(C::kBarDrain));
+      mbar_wait(bar(C::kBarDrain), 0, nullptr);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int t = warp / 4;
+    const int row_in_tile = threadIdx.x & 127;
+    const int row = q_row0[t] + row_in_tile;
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + lane_base + t * 128;
+    const uint32_t tO = tmem + lane_base + C::kColO + t * D;
+    const float sl2 = args.scale_log2;
+    const int diag_j = q_row0[t] / kBlockN;
+    const bool ragged = (N % kBlockN) != 0;
+
+    float m_ref = -INFINITY;  // log2-domain reference maximum
+    float l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n_t[t]; ++j) {
+      ok = mbar_wait(bar(C::kBarSFull + t), j & 1, abort_flag);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t sr[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, sr[c]);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld_wait(sr[c]);
+      float x[128];
+#pragma unroll
+      for (int c = 0; c < 128; ++c) x[c] = __uint_as_float(sr[c >> 5][c & 31]);
+
+      const bool need_mask = (args.causal && j == diag_j) || (ragged && j == n_kv - 1);
+      if (need_mask) {
+        int lim = N - j * kBlockN;
+        if (args.causal) lim = min(lim, row - j * kBlockN + 1);
+#pragma unroll
+        for (int c = 0; c < 128; ++c)
+          if (c >= lim) x[c] = -INFINITY;
+      }
+      float mx0 = x[0], mx1 = x[1], mx2 = x[2], mx3 = x[3];
+#pragma unroll
+      for (int c = 4; c < 128; c += 4) {
+        mx0 = fmaxf(mx0, x[c]);
+        mx1 = fmaxf(mx1, x[c + 1]);
+        mx2 = fmaxf(mx2, x[c + 2]);
+        mx3 = fmaxf(mx3, x[c + 3]);
+      }
+      const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+      const bool need = m_tile > m_ref + kRescaleThreshold;
+      const float m_old = m_ref;
+      if (need) m_ref = m_tile;
+      const float alpha = need ? ex2(m_old - m_ref) : 1.0f;
+      const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
+
+      uint32_t pk[2][32];
+      float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+#pragma unroll
+      for (int c = 0; c < 64; c += 2) {
+        const float p0 = ex2(fmaf(x[2 * c], sl2, -m_use));
+        const float p1 = ex2(fmaf(x[2 * c + 1], sl2, -m_use));
+        const float p2 = ex2(fmaf(x[2 * c + 2], sl2, -m_use));
+        const float p3 = ex2(fmaf(x[2 * c + 3], sl2, -m_use));
+        s0 += p0;
+        s1 += p1;
+        s2 += p2;
+        s3 += p3;
+        pk[c >> 5][c & 31] = pack_bf16(p0, p1);
+        pk[(c + 1) >> 5][(c + 1) & 31] = pack_bf16(p2, p3);
+      }
+      l = alpha * l + ((s0 + s1) + (s2 + s3));
+      tmem_st32(tS, pk[0]);
+      tmem_st32(tS + 32, pk[1]);
+
+      // Rescale the accumulator when this warp's maximum moved. The S MMA of
+      // this tile was committed after the previous P.V, so O is settled.
+      if (j > 0 && __any_sync(0xffffffffu, need)) {
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tO + c * 32, o);
+          tmem_ld_wait(o);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+          tmem_st32(tO + c * 32, o);
+        }
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bar(C::kBarPFull + t));
+    }
+    if (ok && n_t[t] > 0) {
+      ok = mbar_wait(bar(C::kBarOFinal + t), 0, abort_flag);
+      ok = __all_sync(0xffffffffu, ok);
+      if (ok) {
+        tc_fence_after();
+        const float inv_l = l > 0.f ? 1.0f / l : 0.f;
+        const bool live = row < N;
+        __nv_bfloat16* orow = args.o + (static_cast<size_t>(bh) * N + row) * D;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tO + c * 32, o);
+          tmem_ld_wait(o);
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            pk[e] = pack_bf16(__uint_as_float(o[2 * e]) * inv_l, __uint_as_float(o[2 * e + 1]) * inv_l);
+          if (live) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              dst[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+          }
+        }
+        if (live) {
+          const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
+          args.lse[static_cast<size_t>(bh) * N + row] =
+              l > 0.f ? (m_use + log2f(l)) * kLn2 : -INFINITY;
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+  if (threadIdx.x == 0 && *abort_flag) atomicExch(args.status, kStatusTimeout);
+}
+
+template <int D>
+int launch_fwd_d(const Problem& p, void* o, float* lse, cudaStream_t stream) {
+  using C = FwdCfg<D>;
+  const int BH = p.B * p.H;
+  CUtensorMap mq, mk, mv;
+  if (!make_map_bhnd(&mq, p.q, BH, p.N, D) || !make_map_bhnd(&mk, p.k, BH, p.N, D) ||
+      !make_map_bhnd(&mv, p.v, BH, p.N, D))
+    return -3;
+  int* status = device_status_word();
+  if (!status) return -3;
+  auto kern = fa_fwd_kernel<D>;
+  if (!ensure_smem_attr(reinterpret_cast<const void*>(kern), C::kSmemBytes, D == 64 ? 0 : 1))
+    return -3;
+  FwdArgs a;
+  a.o = static_cast<__nv_bfloat16*>(o);
+  a.lse = lse;
+  a.status = status;
+  a.N = p.N;
+  a.BH = BH;
+  a.causal = p.causal ? 1 : 0;
+  a.num_pairs = (p.N + kBlockM * kQTiles - 1) / (kBlockM * kQTiles);
+  // scale 0 (uniform weights) runs as a tiny positive scale: exp2 of a
+  // |value| below 2^-25 rounds to exactly 1 in fp32.
+  const float sl2 = p.scale * 1.4426950408889634f;
+  a.scale_log2 = sl2 > 1e-30f ? sl2 : 1e-30f;
+  const long long grid = static_cast<long long>(a.num_pairs) * BH;
+  if (grid > 0x7fffffffLL) return -1;
+  fa_fwd_kernel<D><<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, a);
+  return cudaGetLastError() == cudaSuccess ? 0 : -3;
+}
+
+}  // namespace
+
+int launch_fwd(const Problem& p, void* o, float* lse, cudaStream_t stream) {
+  if (p.d == 64) return launch_fwd_d<64>(p, o, lse, stream);
+  if (p.d == 128) return launch_fwd_d<128>(p, o, lse, stream);
+  return -2;
+}
+
+}  // namespace fa

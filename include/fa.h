@@ -1,0 +1,134 @@
+/*
+ * fa.h -- C ABI of the exact IO-aware attention library (libfa.so).
+ *
+ * The library computes exact scaled-dot-product attention
+ *
+ *     O = softmax(scale * Q K^T  [+ causal mask]) V
+ *
+ * on one GB300 GPU (sm_103a) without ever writing the N x N scores S or the
+ * probabilities P to device memory: query tiles stay on chip while key/value
+ * tiles stream past, and an online softmax carries a running maximum m, a
+ * denominator l and an unnormalised numerator per query row. Sources:
+ *   "Flash Attention: IO-Aware Exact Attention", sections "Why intermediate
+ *   matrices cost memory traffic" (the problem: Q, K, V in, O out),
+ *   "Online softmax makes tiling exact" (the recurrence) and "Loop order
+ *   changes which data is reloaded" (queries resident, keys/values
+ *   streamed); "FlashAttention -- the same attention, made memory-aware",
+ *   section 00 (scale 1/sqrt(d), causal mask, [B, heads, T, head size]
+ *   layout); "FlashAttention" (Road to Intelligence), section "The
+ *   solution" (the backward recomputes scores instead of storing them).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - All tensor arguments are DEVICE pointers owned by the caller. The
+ *    library keeps no allocation of its own between calls.
+ *  - q, k, v, o, dO, dq, dk, dv: bfloat16, shape [B, H, N, d], contiguous
+ *    row-major (d fastest). lse and the backward's D: float32 [B, H, N].
+ *  - d must be 64 or 128. N may be any length (ragged tail tiles are
+ *    masked); keys and queries have the same length N.
+ *  - causal != 0 masks key j for query i when j > i (the diagonal is
+ *    visible). scale multiplies Q K^T before masking and softmax; it must be
+ *    finite and >= 0 (0 gives uniform weights over the visible keys).
+ *  - lse[b,h,i] = m_i + ln(l_i): the natural-log log-sum-exp of row i of the
+ *    scaled, masked scores (the normalisation statistic the backward needs).
+ *  - B, H or N equal to 0 is an empty problem: the call returns FA_OK and
+ *    touches nothing (pointers may then be NULL). Negative sizes, NULL
+ *    pointers or pointers that are not 16-byte aligned return
+ *    FA_ERR_INVALID before anything is launched.
+ *  - Calls are asynchronous on the given stream (stream 0 for the forms
+ *    without a stream argument); argument checks are synchronous. Outputs
+ *    must not alias inputs.
+ *  - Each wait inside the kernels is bounded (about one second). A wait that
+ *    runs out makes the kernel wind down and raise a device status word that
+ *    fa_get_last_device_status() reads (FA_ERR_TIMEOUT); no kernel traps.
+ *  - Thread safety: calls from several host threads are safe; the device
+ *    status word is shared by all calls on a device.
+ */
+#ifndef FA_H_
+#define FA_H_
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Return codes. */
+#define FA_OK 0
+#define FA_ERR_INVALID -1      /* bad pointer, size, alignment or scale      */
+#define FA_ERR_UNSUPPORTED -2  /* d not in {64,128}, or not a CC 10.3 device */
+#define FA_ERR_LAUNCH -3       /* a CUDA call failed (launch, attribute, map) */
+#define FA_ERR_TIMEOUT -4      /* a bounded wait in a kernel ran out          */
+#define FA_ERR_WORKSPACE -5    /* workspace missing or too small              */
+
+/*
+ * Forward pass.
+ *   q, k, v : in,  bf16 [B,H,N,d]
+ *   o       : out, bf16 [B,H,N,d]   O = softmax(scale*QK^T [+mask]) V
+ *   lse     : out, fp32 [B,H,N]     per-row log-sum-exp (natural log)
+ * Sources: "Flash Attention: IO-Aware Exact Attention", sections "Online
+ * softmax makes tiling exact" and "Check the recurrence on CPU" (the
+ * recurrence and its final division, one per row); "Storage, arithmetic and
+ * IO are separate quantities" (only the output and per-row statistics are
+ * kept for the backward).
+ * Runs on stream 0.
+ */
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+           int N, int d, int causal, float scale);
+
+/* fa_fwd on `cuda_stream` (a cudaStream_t; NULL is the legacy stream). */
+int fa_fwd_stream(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                  int H, int N, int d, int causal, float scale, void* cuda_stream);
+
+/*
+ * Backward pass by recomputation.
+ *   q, k, v, o : in,  bf16 [B,H,N,d]  (o: the forward's output)
+ *   lse        : in,  fp32 [B,H,N]    (the forward's log-sum-exp)
+ *   dO         : in,  bf16 [B,H,N,d]  gradient of the loss w.r.t. O
+ *   dq, dk, dv : out, bf16 [B,H,N,d]  gradients w.r.t. Q, K, V
+ * Computes, with P = exp(scale*QK^T [masked] - lse) recomputed tile by tile:
+ *   dV = P^T dO, dP = dO V^T, D = rowsum(dO * O), dS = P * (dP - D),
+ *   dQ = scale * dS K, dK = scale * dS^T Q.
+ * Source: "FlashAttention" (Road to Intelligence), sections "The solution"
+ * and "What to remember" (scores recomputed from Q, K, V rather than
+ * stored); the gradient formulas follow from the forward's definition.
+ * This form allocates its float32 workspace (fa_bwd_workspace_bytes) with
+ * cudaMallocAsync on stream 0 and frees it stream-ordered after the call.
+ */
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+           const void* dO, void* dq, void* dk, void* dv, int B, int H, int N, int d, int causal,
+           float scale);
+
+/*
+ * fa_bwd on `cuda_stream` with a caller-provided device workspace of at
+ * least fa_bwd_workspace_bytes(B,H,N,d) bytes, 256-byte aligned. The
+ * workspace holds D (fp32 [B,H,N]) and the fp32 dQ accumulator
+ * ([B,H,N,d]); its contents on entry do not matter and on return are
+ * unspecified. Two calls in flight at once need two workspaces.
+ */
+int fa_bwd_stream(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                  const void* dO, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+                  int causal, float scale, void* workspace, size_t ws_bytes, void* cuda_stream);
+
+/* Workspace bytes fa_bwd_stream needs for these sizes (0 when empty). */
+size_t fa_bwd_workspace_bytes(int B, int H, int N, int d);
+
+/* Static description of a return code. Never NULL. */
+const char* fa_strerror(int code);
+
+/*
+ * Device status word of the current device: FA_OK, or FA_ERR_TIMEOUT when a
+ * kernel launched since the last read gave up on a bounded wait. Reading
+ * synchronises the device and clears the word. Returns FA_ERR_LAUNCH if the
+ * word cannot be read.
+ */
+int fa_get_last_device_status(void);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int fa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_H_ */
