@@ -49,9 +49,12 @@ def test_strerror_and_version(lib):
 def test_workspace_bytes(lib):
     assert lib.fa_bwd_workspace_bytes(0, 1, 1, 64) == 0
     assert lib.fa_bwd_workspace_bytes(-1, 1, 1, 64) == 0
+    # D and the log2-domain LSE, each fp32 over N rounded up to 128, then the
+    # fp32 dQ accumulator
     B, H, N, d = 2, 3, 100, 64
-    want_d = ((B * H * N * 4 + 255) // 256) * 256
-    assert lib.fa_bwd_workspace_bytes(B, H, N, d) == want_d + B * H * N * d * 4
+    n_pad = 128
+    assert lib.fa_bwd_workspace_bytes(B, H, N, d) == 2 * B * H * n_pad * 4 + B * H * N * d * 4
+    assert lib.fa_bwd_workspace_bytes(1, 1, 256, 128) == 2 * 256 * 4 + 256 * 128 * 4
 
 
 NULL = ctypes.c_void_p(0)
