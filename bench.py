@@ -1,0 +1,457 @@
+"""Throughput of exact attention (forward + backward) on GB300.
+
+One step is one pass of the whole hot path over one batch: the forward
+(fa_fwd) and the three backward stages (fa_bwd preprocess, main, finish) on
+the causal forward+backward workload B=8, H=12, N=2048, d=64 with iid N(0,1)
+bf16 inputs. The metric is TFLOP/s with the method's algorithmic count,
+4 B H N^2 d for the forward (halved when causal) and 2.5x that for the
+backward, and its fraction of the measured dense BF16 tensor peak.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Timing: W untimed warm-up steps, then K steps between a barrier and a device
+synchronisation on both sides, each step bracketed by CUDA events on the
+stream the kernels run on; L2 is flushed (a 256 MiB write) between steps,
+outside the events. Under torchrun every rank runs its own batch (weak
+scaling; no collective in the data path) and rank 0 prints one JSON line
+with the slowest rank's time.
+
+``--impl reference`` times the float64 CPU oracle instead, on a bounded
+sample of the same workload per step (rank 0 only).
+"""
+
+from __future__ import annotations
+
+import argparse
+import ctypes
+import json
+import math
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synthetic_inputs as si  # noqa: E402
+
+METRIC = "attention fwd/bwd TFLOP/s on 1 GB300 and % of dense BF16 tensor peak"
+UNIT = "TFLOP/s"
+FALLBACK_PEAK_TFLOPS = 1900.0
+L2_FLUSH_BYTES = 256 << 20
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=si.WORKLOADS[4].name)
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the end-to-end, CPU-baseline and long-forward legs")
+    return ap.parse_args()
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["bf16_tflops"]), float(p.get("bf16_tflops_sustained", 0.0)), "measured"
+    except Exception:
+        return FALLBACK_PEAK_TFLOPS, 1700.0, "fallback"
+
+
+def step_flops(w):
+    import exact_io_aware_33_gb300 as fa
+    f = fa.flops_fwd(w.B, w.H, w.N, w.d, w.causal)
+    return f, (fa.flops_bwd(w.B, w.H, w.N, w.d, w.causal) if w.backward else 0.0)
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons, every 200 ms."""
+
+    FIELDS = ("index,pci.bus_id,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, bus_id):
+        self.bus_id = (bus_id or "").lower()
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=self.out, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.out.close()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            if self.bus_id and parts[1].lower() != self.bus_id:
+                continue
+            rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return float("nan")
+        sm = [num(r[2]) for r in rows]
+        busy = [s for s in sm if s > 0]
+        sm_max = max(num(r[3]) for r in rows)
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[6 + i].lower() == "active"})
+        busy.sort()
+        return {"sm_mhz": busy[len(busy) // 2] if busy else None, "sm_max_mhz": sm_max,
+                "reasons": reasons, "samples": len(rows),
+                "power_w_max": max(num(r[4]) for r in rows)}
+
+
+# ------------------------------------------------------------------ GPU arm
+class Runner:
+    """Buffers and C-ABI calls of one forward+backward step."""
+
+    def __init__(self, w, device, seed_offset=0):
+        import torch
+        import exact_io_aware_33_gb300 as fa
+        self.torch, self.fa, self.w, self.dev = torch, fa, w, device
+        self.lib = fa.load_library()
+        x = si.make_small(w.B, w.H, w.N, w.d, seed=w.seed + seed_offset, k_mult=w.k_mult,
+                          with_grad=w.backward)
+        self.host = x
+        self.x = {k: t.to(device) for k, t in x.items()}
+        self.o = torch.empty_like(self.x["q"])
+        self.lse = torch.empty(w.B, w.H, w.N, dtype=torch.float32, device=device)
+        if w.backward:
+            self.dq = torch.empty_like(self.x["q"])
+            self.dk = torch.empty_like(self.x["q"])
+            self.dv = torch.empty_like(self.x["q"])
+            self.ws_bytes = self.lib.fa_bwd_workspace_bytes(w.B, w.H, w.N, w.d)
+            self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=device)
+        self.flush_buf = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+        self.launches_per_step = 4 if w.backward else 1
+
+    def _p(self, t):
+        return ctypes.c_void_p(t.data_ptr())
+
+    def step(self, stream, ev=None):
+        """Launch one step on `stream`; ev = dict of event pairs to record."""
+        w, lib, p, x = self.w, self.lib, self._p, self.x
+        sh = ctypes.c_void_p(stream.cuda_stream)
+        c = 1 if w.causal else 0
+        if ev:
+            ev["fwd"][0].record(stream)
+        rc = lib.fa_fwd_stream(p(x["q"]), p(x["k"]), p(x["v"]), p(self.o), p(self.lse),
+                               w.B, w.H, w.N, w.d, c, w.scale, sh)
+        if ev:
+            ev["fwd"][1].record(stream)
+        if rc != 0:
+            raise RuntimeError(f"fa_fwd_stream: {rc}")
+        if not w.backward:
+            return
+        wsb = ctypes.c_size_t(self.ws_bytes)
+        rc = lib.fa_bwd_preprocess_stream(p(self.o), p(self.lse), p(x["do"]), w.B, w.H, w.N, w.d,
+                                          p(self.ws), wsb, sh)
+        if ev:
+            ev["bwd_main"][0].record(stream)
+        rc = rc or lib.fa_bwd_main_stream(p(x["q"]), p(x["k"]), p(x["v"]), p(x["do"]), p(self.dk),
+                                          p(self.dv), w.B, w.H, w.N, w.d, c, w.scale, p(self.ws),
+                                          wsb, sh)
+        if ev:
+            ev["bwd_main"][1].record(stream)
+        rc = rc or lib.fa_bwd_finish_stream(p(self.dq), w.B, w.H, w.N, w.d, p(self.ws), wsb, sh)
+        if rc != 0:
+            raise RuntimeError(f"fa_bwd stages: {rc}")
+
+    def flush_l2(self):
+        self.flush_buf.zero_()
+
+
+def timed_loop(runner, steps, warmup, barrier, stream):
+    torch = runner.torch
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            runner.flush_l2()
+            runner.step(stream)
+    torch.cuda.synchronize()
+    mk = lambda: torch.cuda.Event(enable_timing=True)
+    evs = [{"step": (mk(), mk()), "fwd": (mk(), mk()), "bwd_main": (mk(), mk())}
+           for _ in range(steps)]
+    barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for e in evs:
+            runner.flush_l2()
+            e["step"][0].record(stream)
+            runner.step(stream, e)
+            e["step"][1].record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    wall = time.perf_counter() - t0
+    keys = ("step", "fwd", "bwd_main") if runner.w.backward else ("step", "fwd")
+    t = {k: [e[k][0].elapsed_time(e[k][1]) for e in evs] for k in keys}
+    return t, wall
+
+
+def e2e_loop(runner, steps, warmup, stream):
+    """Same step through host buffers: H2D of the inputs, D2H of every output."""
+    torch = runner.torch
+    names_in = ["q", "k", "v"] + (["do"] if runner.w.backward else [])
+    h_in = {n: runner.host[n].pin_memory() for n in names_in}
+    outs = [runner.o, runner.lse] + ([runner.dq, runner.dk, runner.dv] if runner.w.backward else [])
+    h_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
+    h2d = sum(t.numel() * t.element_size() for t in h_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in h_out)
+
+    def one():
+        for n in names_in:
+            runner.x[n].copy_(h_in[n], non_blocking=True)
+        runner.step(stream)
+        for d, h in zip(outs, h_out):
+            h.copy_(d, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            one()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(steps):
+            one()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / steps, h2d, d2h
+
+
+def traffic_from_profiles(kernel):
+    """DRAM bytes per launch recorded by ncu for `kernel`, if the kernel's
+    source is unchanged since the capture (profiles/traffic.txt)."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(path):
+        return None
+    src = {"fa_fwd_kernel": "fa_fwd.cu", "fa_bwd_main": "fa_bwd.cu"}.get(kernel)
+    if src is None:
+        return None
+    h = hashlib.sha256()
+    for f in (src, "sm103_ptx.cuh"):
+        h.update(open(os.path.join(ROOT, "exact_io_aware_33_gb300", "csrc", f), "rb").read())
+    digest = h.hexdigest()[:16]
+    for line in open(path):
+        parts = line.split()
+        if len(parts) >= 4 and parts[0] == kernel and parts[1] == digest:
+            return float(parts[2])
+    return None
+
+
+def cpu_baseline(w, budget_s=12.0):
+    """The float64 oracle on a bounded sample of the workload's heads."""
+    import numpy as np  # noqa: F401
+    from oracle import dense
+    x = si.make_inputs(w)
+    heads = [(b, h) for b in range(w.B) for h in range(w.H)]
+    done, t0 = 0, time.perf_counter()
+    for b, h in heads:
+        o, lse = dense.forward_head(x["q"][b, h], x["k"][b, h], x["v"][b, h], w.causal, w.scale)
+        if w.backward:
+            dense.backward_head(x["q"][b, h], x["k"][b, h], x["v"][b, h], o, lse, x["do"][b, h],
+                                w.causal, w.scale)
+        done += 1
+        if time.perf_counter() - t0 > budget_s and done >= 2:
+            break
+    dt = time.perf_counter() - t0
+    f_fwd, f_bwd = step_flops(w)
+    flops = (f_fwd + f_bwd) * done / w.heads
+    return {"value": flops / dt / 1e12, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
+            "sample": f"{done} of {w.heads} heads of {w.name} (dense float64 numpy "
+                      f"{'forward+backward' if w.backward else 'forward'}), {dt:.1f} s"}
+
+
+def blas_threads():
+    try:
+        import threadpoolctl
+        import numpy  # noqa: F401
+        for info in threadpoolctl.threadpool_info():
+            if info.get("user_api") == "blas":
+                return int(info["num_threads"])
+    except Exception:
+        pass
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
+        if os.environ.get(var):
+            return int(os.environ[var])
+    return os.cpu_count()
+
+
+def run_ours(args):
+    import torch
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        barrier = lambda: dist.barrier()
+    else:
+        torch.cuda.set_device(0)
+        barrier = lambda: None
+    dev = torch.device("cuda", torch.cuda.current_device())
+    w = si.workload(args.workload)
+    runner = Runner(w, dev, seed_offset=rank)
+    stream = torch.cuda.Stream(dev)
+    props = torch.cuda.get_device_properties(dev)
+    bus = ""
+    if hasattr(props, "pci_bus_id"):
+        bus = "%08X:%02X:%02X.0" % (getattr(props, "pci_domain_id", 0), props.pci_bus_id,
+                                     getattr(props, "pci_device_id", 0))
+    sampler = ClockSampler(bus)
+    sampler.start()
+    times, wall = timed_loop(runner, args.steps, max(args.warmup, 3), barrier, stream)
+    clocks = sampler.stop()
+    ms = sum(times["step"]) / len(times["step"])
+    ms_fwd = sum(times["fwd"]) / len(times["fwd"])
+    ms_bwd = sum(times["bwd_main"]) / len(times["bwd_main"]) if w.backward else 0.0
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms, ms_fwd, ms_bwd], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms, ms_fwd, ms_bwd = (float(v) for v in t.tolist())
+    f_fwd, f_bwd = step_flops(w)
+    value = world * (f_fwd + f_bwd) / (ms * 1e-3) / 1e12
+    peak, peak_sus, peak_src = measured_peaks()
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
+    kernels = {"fa_fwd_kernel": (f_fwd, ms_fwd)}
+    if w.backward:
+        kernels["fa_bwd_main"] = (f_bwd, ms_bwd)
+    dom = max(kernels, key=lambda k: kernels[k][1])
+    fl, kms = kernels[dom]
+    achieved = fl / (kms * 1e-3) / 1e12
+    roofline = {"bound": "tensor", "kernel": dom, "achieved": round(achieved, 1), "peak": peak,
+                "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                "traffic": traffic_from_profiles(dom),
+                "peak_source": f"{peak_src} bf16 dense burst (MEASURED_PEAKS.json)"
+                if peak_src == "measured" else "fallback 1.9 PFLOP/s"}
+    out = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": round(ms, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded iid N(0,1) bf16 q, k, v, dO)",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d,
+                   "causal": w.causal, "pass": "forward+backward" if w.backward else "forward",
+                   "l2": "flushed between steps (256 MiB write, outside the events)",
+                   "parallelism": f"replicas x{world} (independent batches)"},
+        "pct_of_peak": round(100.0 * value / (world * peak), 2),
+        "kernels_ms": {"fa_fwd_kernel": round(ms_fwd, 4),
+                       **({"fa_bwd_main": round(ms_bwd, 4)} if w.backward else {})},
+        "kernels_tflops": {k: round(v[0] / (v[1] * 1e-3) / 1e12, 1) for k, v in kernels.items()},
+        "roofline": roofline,
+        "gpu_launches": runner.launches_per_step * args.steps,
+        "clocks": clocks,
+        "wall_s": round(wall, 3),
+    }
+    if not args.no_extras:
+        e_ms, h2d, d2h = e2e_loop(runner, max(3, args.steps // 2), 2, stream)
+        out["e2e"] = {"value": round(world * (f_fwd + f_bwd) / (e_ms * 1e-3) / 1e12, 2),
+                      "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                      "ms_per_step": round(e_ms, 4)}
+        # the long causal forward (B=1, H=16, N=8192, d=128), the head-size-128 target shape
+        wl = si.WORKLOADS[3]
+        rl = Runner(wl, dev)
+        tl, _ = timed_loop(rl, max(5, args.steps // 2), 3, barrier, stream)
+        ms_l = sum(tl["fwd"]) / len(tl["fwd"])
+        tf_l = step_flops(wl)[0] / (ms_l * 1e-3) / 1e12
+        out["fwd_long"] = {"workload": wl.name, "ms": round(ms_l, 4), "tflops": round(tf_l, 1),
+                           "frac": round(tf_l / peak, 4)}
+        del rl
+        if world == 1:
+            out["cpu_baseline"] = cpu_baseline(w)
+    print(json.dumps(out), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def run_reference(args):
+    """The oracle, as it stands, on the host cores: one head per step."""
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    from oracle import dense
+    w = si.workload(args.workload)
+    x = si.make_inputs(w)
+    heads = [(b, h) for b in range(w.B) for h in range(w.H)]
+
+    def one(i):
+        b, h = heads[i % len(heads)]
+        o, lse = dense.forward_head(x["q"][b, h], x["k"][b, h], x["v"][b, h], w.causal, w.scale)
+        if w.backward:
+            dense.backward_head(x["q"][b, h], x["k"][b, h], x["v"][b, h], o, lse, x["do"][b, h],
+                                w.causal, w.scale)
+
+    for i in range(max(args.warmup, 3)):
+        one(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        one(i)
+    dt = (time.perf_counter() - t0) / args.steps
+    f_fwd, f_bwd = step_flops(w)
+    value = (f_fwd + f_bwd) / w.heads / dt / 1e12
+    cores = blas_threads()
+    sample = f"one head of {w.name} per step (dense float64 numpy oracle)"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": round(dt * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded iid N(0,1) bf16 q, k, v, dO upcast to float64)",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d,
+                   "causal": w.causal, "sample": "one (batch, head) per step"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

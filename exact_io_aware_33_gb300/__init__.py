@@ -46,6 +46,9 @@ SIGNATURES = {
     "fa_fwd_stream": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P]),
     "fa_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F]),
     "fa_bwd_stream": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P, _S, _P]),
+    "fa_bwd_preprocess_stream": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _S, _P]),
+    "fa_bwd_main_stream": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P, _S, _P]),
+    "fa_bwd_finish_stream": (_I, [_P, _I, _I, _I, _I, _P, _S, _P]),
     "fa_bwd_workspace_bytes": (_S, [_I, _I, _I, _I]),
     "fa_strerror": (ctypes.c_char_p, [_I]),
     "fa_get_last_device_status": (_I, []),

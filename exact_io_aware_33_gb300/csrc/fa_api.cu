@@ -6,6 +6,7 @@
 
 #include <cmath>
 #include <cstdint>
+#include <initializer_list>
 #include <mutex>
 
 #include "fa.h"
@@ -176,24 +177,66 @@ size_t fa_bwd_workspace_bytes(int B, int H, int N, int d) {
   return fa::bwd_workspace_bytes(B, H, N, d);
 }
 
-int fa_bwd_stream(const void* q, const void* k, const void* v, const void* o, const float* lse,
-                  const void* dO, void* dq, void* dk, void* dv, int B, int H, int N, int d,
-                  int causal, float scale, void* workspace, size_t ws_bytes, void* cuda_stream) {
-  bool empty = false;
-  int rc = fa::check_problem(B, H, N, d, scale, &empty);
-  if (rc != FA_OK || empty) return rc;
-  const void* ptrs[] = {q, k, v, o, lse, dO, dq, dk, dv};
+namespace {
+
+// Checks shared by the backward entry points. `ptrs` must all be non-NULL
+// and 16-byte aligned; the workspace 256-byte aligned and large enough.
+int check_bwd(int B, int H, int N, int d, float scale, std::initializer_list<const void*> ptrs,
+              const void* workspace, size_t ws_bytes, bool* empty) {
+  int rc = fa::check_problem(B, H, N, d, scale, empty);
+  if (rc != FA_OK || *empty) return rc;
   for (const void* ptr : ptrs)
     if (!fa::aligned16(ptr)) return FA_ERR_INVALID;
   if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
       ws_bytes < fa::bwd_workspace_bytes(B, H, N, d))
     return FA_ERR_WORKSPACE;
   fa::DeviceState* st = nullptr;
-  rc = fa::current_device(&st);
-  if (rc != FA_OK) return rc;
+  return fa::current_device(&st);
+}
+
+}  // namespace
+
+int fa_bwd_preprocess_stream(const void* o, const float* lse, const void* dO, int B, int H,
+                             int N, int d, void* workspace, size_t ws_bytes, void* cuda_stream) {
+  bool empty = false;
+  int rc = check_bwd(B, H, N, d, 1.f, {o, lse, dO}, workspace, ws_bytes, &empty);
+  if (rc != FA_OK || empty) return rc;
+  Problem p{nullptr, nullptr, nullptr, B, H, N, d, 0, 1.f};
+  return fa::launch_bwd_pre(p, o, lse, dO, workspace, static_cast<cudaStream_t>(cuda_stream));
+}
+
+int fa_bwd_main_stream(const void* q, const void* k, const void* v, const void* dO, void* dk,
+                       void* dv, int B, int H, int N, int d, int causal, float scale,
+                       void* workspace, size_t ws_bytes, void* cuda_stream) {
+  bool empty = false;
+  int rc = check_bwd(B, H, N, d, scale, {q, k, v, dO, dk, dv}, workspace, ws_bytes, &empty);
+  if (rc != FA_OK || empty) return rc;
   Problem p{q, k, v, B, H, N, d, causal, scale};
-  return fa::launch_bwd(p, o, lse, dO, dq, dk, dv, workspace,
-                        static_cast<cudaStream_t>(cuda_stream));
+  return fa::launch_bwd_main(p, dO, dk, dv, workspace, static_cast<cudaStream_t>(cuda_stream));
+}
+
+int fa_bwd_finish_stream(void* dq, int B, int H, int N, int d, const void* workspace,
+                         size_t ws_bytes, void* cuda_stream) {
+  bool empty = false;
+  int rc = check_bwd(B, H, N, d, 1.f, {dq}, workspace, ws_bytes, &empty);
+  if (rc != FA_OK || empty) return rc;
+  Problem p{nullptr, nullptr, nullptr, B, H, N, d, 0, 1.f};
+  return fa::launch_bwd_post(p, dq, workspace, static_cast<cudaStream_t>(cuda_stream));
+}
+
+int fa_bwd_stream(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                  const void* dO, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+                  int causal, float scale, void* workspace, size_t ws_bytes, void* cuda_stream) {
+  bool empty = false;
+  int rc = check_bwd(B, H, N, d, scale, {q, k, v, o, lse, dO, dq, dk, dv}, workspace, ws_bytes,
+                     &empty);
+  if (rc != FA_OK || empty) return rc;
+  const cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+  Problem p{q, k, v, B, H, N, d, causal, scale};
+  rc = fa::launch_bwd_pre(p, o, lse, dO, workspace, st);
+  if (rc == FA_OK) rc = fa::launch_bwd_main(p, dO, dk, dv, workspace, st);
+  if (rc == FA_OK) rc = fa::launch_bwd_post(p, dq, workspace, st);
+  return rc;
 }
 
 int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,

@@ -462,20 +462,49 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0 && *abort_flag) atomicExch(args.status, kStatusTimeout);
 }
 
+// Workspace sections: D and lse2 (fp32 [BH, Npad] each), then the fp32 dQ
+// accumulator [BH, N, d]. Npad * 4 bytes is a multiple of 512, so every
+// section and every query block's vector slice is 512-byte aligned.
+struct Workspace {
+  float* Dvec;
+  float* lse2;
+  float* acc;
+  int n_pad;
+  long long pad_rows;
+};
+
+Workspace carve(const Problem& p, void* workspace) {
+  Workspace w;
+  w.n_pad = (p.N + kBlk - 1) / kBlk * kBlk;
+  w.pad_rows = static_cast<long long>(p.B) * p.H * w.n_pad;
+  w.Dvec = static_cast<float*>(workspace);
+  w.lse2 = w.Dvec + w.pad_rows;
+  w.acc = w.lse2 + w.pad_rows;
+  return w;
+}
+
 template <int D>
-int launch_bwd_d(const Problem& p, const void* o, const float* lse, const void* dO, void* dq,
-                 void* dk, void* dv, void* workspace, cudaStream_t stream) {
+int launch_pre_d(const Problem& p, const void* o, const float* lse, const void* dO,
+                 void* workspace, cudaStream_t stream) {
+  const Workspace w = carve(p, workspace);
+  const long long acc_vec4 = static_cast<long long>(p.B) * p.H * p.N * D / 4;
+  const long long work = w.pad_rows * (D / 8) > acc_vec4 ? w.pad_rows * (D / 8) : acc_vec4;
+  long long blocks = (work + 255) / 256;
+  if (blocks > 65536) blocks = 65536;
+  fa_bwd_pre<D><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+      static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dO), lse, w.Dvec,
+      w.lse2, p.N, w.n_pad, w.pad_rows, reinterpret_cast<float4*>(w.acc), acc_vec4);
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
+template <int D>
+int launch_main_d(const Problem& p, const void* dO, void* dk, void* dv, void* workspace,
+                  cudaStream_t stream) {
   using C = BwdCfg<D>;
+  const Workspace w = carve(p, workspace);
   const int BH = p.B * p.H;
-  const int n_blocks = (p.N + kBlk - 1) / kBlk;
-  const int n_pad = n_blocks * kBlk;
-  const long long pad_rows = static_cast<long long>(BH) * n_pad;
-  float* Dvec = static_cast<float*>(workspace);
-  float* lse2 = Dvec + pad_rows;
-  float* acc = lse2 + pad_rows;  // pad_rows * 4 bytes is a multiple of 512
   int* status = device_status_word();
   if (!status) return FA_ERR_LAUNCH;
-
   CUtensorMap mq, mk, mv, mdo;
   if (!make_map_bhnd(&mq, p.q, BH, p.N, D) || !make_map_bhnd(&mk, p.k, BH, p.N, D) ||
       !make_map_bhnd(&mv, p.v, BH, p.N, D) || !make_map_bhnd(&mdo, dO, BH, p.N, D))
@@ -483,59 +512,55 @@ int launch_bwd_d(const Problem& p, const void* o, const float* lse, const void* 
   auto kern = fa_bwd_main<D>;
   if (!ensure_smem_attr(reinterpret_cast<const void*>(kern), C::kSmemBytes, D == 64 ? 2 : 3))
     return FA_ERR_LAUNCH;
-
-  const long long acc_vec4 = static_cast<long long>(BH) * p.N * D / 4;
-  {
-    const long long work = pad_rows * (D / 8) > acc_vec4 ? pad_rows * (D / 8) : acc_vec4;
-    long long blocks = (work + 255) / 256;
-    if (blocks > 65536) blocks = 65536;
-    fa_bwd_pre<D><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-        static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dO), lse, Dvec,
-        lse2, p.N, n_pad, pad_rows, reinterpret_cast<float4*>(acc), acc_vec4);
-    if (cudaGetLastError() != cudaSuccess) return FA_ERR_LAUNCH;
-  }
   BwdArgs a;
-  a.lse2 = lse2;
-  a.Dvec = Dvec;
-  a.dq_acc = acc;
+  a.lse2 = w.lse2;
+  a.Dvec = w.Dvec;
+  a.dq_acc = w.acc;
   a.dk = static_cast<__nv_bfloat16*>(dk);
   a.dv = static_cast<__nv_bfloat16*>(dv);
   a.status = status;
   a.N = p.N;
-  a.n_pad = n_pad;
+  a.n_pad = w.n_pad;
   a.BH = BH;
   a.causal = p.causal ? 1 : 0;
-  a.n_blocks = n_blocks;
+  a.n_blocks = w.n_pad / kBlk;
   a.scale = p.scale;
   a.scale_log2 = p.scale * kLog2e;
-  const long long grid = static_cast<long long>(n_blocks) * BH;
+  const long long grid = static_cast<long long>(a.n_blocks) * BH;
   if (grid > 0x7fffffffLL) return FA_ERR_INVALID;
   fa_bwd_main<D><<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, mdo, a);
-  if (cudaGetLastError() != cudaSuccess) return FA_ERR_LAUNCH;
-  {
-    long long blocks = (acc_vec4 + 255) / 256;
-    if (blocks > 65536) blocks = 65536;
-    fa_bwd_post<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-        reinterpret_cast<const float4*>(acc), static_cast<uint2*>(dq), acc_vec4);
-    if (cudaGetLastError() != cudaSuccess) return FA_ERR_LAUNCH;
-  }
-  return FA_OK;
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
 }  // namespace
 
 size_t bwd_workspace_bytes(long long B, long long H, long long N, long long d) {
-  // D and lse2 (fp32 [B,H,Npad], Npad = N rounded up to 128), then the fp32
-  // dQ accumulator [B,H,N,d].
   const long long n_pad = (N + kBlk - 1) / kBlk * kBlk;
   return static_cast<size_t>(2 * B * H * n_pad) * 4 + static_cast<size_t>(B * H * N * d) * 4;
 }
 
-int launch_bwd(const Problem& p, const void* o, const float* lse, const void* dO, void* dq,
-               void* dk, void* dv, void* workspace, cudaStream_t stream) {
-  if (p.d == 64) return launch_bwd_d<64>(p, o, lse, dO, dq, dk, dv, workspace, stream);
-  if (p.d == 128) return launch_bwd_d<128>(p, o, lse, dO, dq, dk, dv, workspace, stream);
+int launch_bwd_pre(const Problem& p, const void* o, const float* lse, const void* dO,
+                   void* workspace, cudaStream_t stream) {
+  if (p.d == 64) return launch_pre_d<64>(p, o, lse, dO, workspace, stream);
+  if (p.d == 128) return launch_pre_d<128>(p, o, lse, dO, workspace, stream);
   return FA_ERR_UNSUPPORTED;
+}
+
+int launch_bwd_main(const Problem& p, const void* dO, void* dk, void* dv, void* workspace,
+                    cudaStream_t stream) {
+  if (p.d == 64) return launch_main_d<64>(p, dO, dk, dv, workspace, stream);
+  if (p.d == 128) return launch_main_d<128>(p, dO, dk, dv, workspace, stream);
+  return FA_ERR_UNSUPPORTED;
+}
+
+int launch_bwd_post(const Problem& p, void* dq, const void* workspace, cudaStream_t stream) {
+  const Workspace w = carve(p, const_cast<void*>(workspace));
+  const long long acc_vec4 = static_cast<long long>(p.B) * p.H * p.N * p.d / 4;
+  long long blocks = (acc_vec4 + 255) / 256;
+  if (blocks > 65536) blocks = 65536;
+  fa_bwd_post<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+      reinterpret_cast<const float4*>(w.acc), static_cast<uint2*>(dq), acc_vec4);
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
 }  // namespace fa

@@ -29,8 +29,11 @@ int* device_status_word();
 bool ensure_smem_attr(const void* func, int bytes, int slot);
 
 int launch_fwd(const Problem& p, void* o, float* lse, cudaStream_t stream);
-int launch_bwd(const Problem& p, const void* o, const float* lse, const void* dO, void* dq,
-               void* dk, void* dv, void* workspace, cudaStream_t stream);
+int launch_bwd_pre(const Problem& p, const void* o, const float* lse, const void* dO,
+                   void* workspace, cudaStream_t stream);
+int launch_bwd_main(const Problem& p, const void* dO, void* dk, void* dv, void* workspace,
+                    cudaStream_t stream);
+int launch_bwd_post(const Problem& p, void* dq, const void* workspace, cudaStream_t stream);
 
 size_t bwd_workspace_bytes(long long B, long long H, long long N, long long d);
 

@@ -102,13 +102,33 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
 /*
  * fa_bwd on `cuda_stream` with a caller-provided device workspace of at
  * least fa_bwd_workspace_bytes(B,H,N,d) bytes, 256-byte aligned. The
- * workspace holds D (fp32 [B,H,N]) and the fp32 dQ accumulator
+ * workspace holds D = rowsum(dO * O) and the LSE in log2 units (fp32, each
+ * over N rounded up to 128 per head) and the fp32 dQ accumulator
  * ([B,H,N,d]); its contents on entry do not matter and on return are
  * unspecified. Two calls in flight at once need two workspaces.
  */
 int fa_bwd_stream(const void* q, const void* k, const void* v, const void* o, const float* lse,
                   const void* dO, void* dq, void* dk, void* dv, int B, int H, int N, int d,
                   int causal, float scale, void* workspace, size_t ws_bytes, void* cuda_stream);
+
+/*
+ * The backward's three stages, for callers that schedule or time them one
+ * by one. fa_bwd_stream is exactly these three calls, in this order, on one
+ * stream with one workspace; each checks its arguments like fa_bwd_stream.
+ *   preprocess: D = rowsum(dO * O) and LSE in log2 units into the
+ *               workspace; zeroes the workspace's fp32 dQ accumulator.
+ *   main:       per block of 128 keys, recomputes the score and probability
+ *               tiles of every query block and accumulates dK, dV (written
+ *               to dk, dv) and dQ (added into the workspace).
+ *   finish:     dq = bf16(workspace dQ accumulator).
+ */
+int fa_bwd_preprocess_stream(const void* o, const float* lse, const void* dO, int B, int H,
+                             int N, int d, void* workspace, size_t ws_bytes, void* cuda_stream);
+int fa_bwd_main_stream(const void* q, const void* k, const void* v, const void* dO, void* dk,
+                       void* dv, int B, int H, int N, int d, int causal, float scale,
+                       void* workspace, size_t ws_bytes, void* cuda_stream);
+int fa_bwd_finish_stream(void* dq, int B, int H, int N, int d, const void* workspace,
+                         size_t ws_bytes, void* cuda_stream);
 
 /* Workspace bytes fa_bwd_stream needs for these sizes (0 when empty). */
 size_t fa_bwd_workspace_bytes(int B, int H, int N, int d);
