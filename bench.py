@@ -72,6 +72,27 @@ def measured_peaks():
         return FALLBACK_PEAK_TFLOPS, 1700.0, "fallback"
 
 
+def max_over_ranks(values, device, world):
+    """Element-wise maximum of per-rank floats (the slowest rank's times)."""
+    if world <= 1:
+        return list(values)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor(list(values), dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def whole_job_tflops(world, flops_per_rank_step, ms_per_step):
+    """Weak scaling: every rank processes its own batch in the slowest rank's time."""
+    return world * flops_per_rank_step / (ms_per_step * 1e-3) / 1e12
+
+
+def rank_seed_offset(rank):
+    """Each rank draws its own batch: the workload's seed plus the rank."""
+    return rank
+
+
 def step_flops(w):
     import exact_io_aware_33_gb300 as fa
     f = fa.flops_fwd(w.B, w.H, w.N, w.d, w.causal)
@@ -328,7 +349,7 @@ def run_ours(args):
         barrier = lambda: None
     dev = torch.device("cuda", torch.cuda.current_device())
     w = si.workload(args.workload)
-    runner = Runner(w, dev, seed_offset=rank)
+    runner = Runner(w, dev, seed_offset=rank_seed_offset(rank))
     stream = torch.cuda.Stream(dev)
     props = torch.cuda.get_device_properties(dev)
     bus = ""
@@ -342,13 +363,9 @@ def run_ours(args):
     ms = sum(times["step"]) / len(times["step"])
     ms_fwd = sum(times["fwd"]) / len(times["fwd"])
     ms_bwd = sum(times["bwd_main"]) / len(times["bwd_main"]) if w.backward else 0.0
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms, ms_fwd, ms_bwd], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, ms_fwd, ms_bwd = (float(v) for v in t.tolist())
+    ms, ms_fwd, ms_bwd = max_over_ranks([ms, ms_fwd, ms_bwd], dev, world)
     f_fwd, f_bwd = step_flops(w)
-    value = world * (f_fwd + f_bwd) / (ms * 1e-3) / 1e12
+    value = whole_job_tflops(world, f_fwd + f_bwd, ms)
     peak, peak_sus, peak_src = measured_peaks()
     if rank != 0:
         if world > 1:
