@@ -1,7 +1,9 @@
 """Backward pass on the GPU against the float64 CPU oracle.
 
 Gate per tensor X in {dQ, dK, dV}: max|dX - dX_ref| / max|dX_ref| <= 5e-2
-(the max-norm reading of "max relative-to-norm error"). The GPU backward
+(the max-norm reading of "max relative-to-norm error"). The norm is floored
+at 1e-3: with a single key dQ is exactly zero (dS = P (dP - D) vanishes when
+P = 1), and fp32 rounding leaves ~1e-8 there. The GPU backward
 consumes the GPU forward's own O and LSE, as a training step would; the
 oracle uses its own float64 forward. Small problems are compared in full;
 the forward+backward workload runs at full size and is compared on a
@@ -27,7 +29,7 @@ REL_MAX = 5e-2
 
 
 def _rel(got, ref):
-    return float(np.abs(got - ref).max() / max(np.abs(ref).max(), 1e-30))
+    return float(np.abs(got - ref).max() / max(np.abs(ref).max(), 1e-3))
 
 
 def _run(x, causal, scale):
