@@ -59,6 +59,9 @@ struct BwdCfg {
   static constexpr int kVecBytes = 2 * kBlk * 4;  // lse2[128], D[128] of one query block
   static constexpr int kStages = (D == 64) ? 3 : 2;
   static constexpr bool kDqAliasDp = (D == 128);
+  // Every kEmuEvery-th pair of probabilities off the causal diagonal uses
+  // the polynomial exp2 on the FMA pipe instead of MUFU ex2 (0: never).
+  static constexpr int kEmuEvery = 0;
   static constexpr int kKOff = 0;
   static constexpr int kVOff = kKOff + kTileBytes;
   static constexpr int kDSOff = kVOff + kTileBytes;             // 2 x 16 KiB
@@ -91,8 +94,8 @@ struct BwdCfg {
 };
 
 struct BwdArgs {
-  const float* lse2;   // [BH, Npad] log2-domain LSE, +inf past N
-  const float* Dvec;   // [BH, Npad] rowsum(dO * O), 0 past N
+  const float* lse2;   // [BH, Npad] -LSE * log2(e), -inf past N
+  const float* Dvec;   // [BH, Npad] -rowsum(dO * O), 0 past N
   float* dq_acc;
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
@@ -107,10 +110,11 @@ struct BwdArgs {
 };
 
 // ---------------------------------------------------------------- B0
-// For every row of the padded [BH, Npad] grid: D = sum_c dO[c] * O[c] and
-// lse2 = LSE * log2(e) (rows past N get D = 0, lse2 = +inf, so that their
-// recomputed probabilities are exactly 0). One group of D/8 lanes per row,
-// each lane reading 8 bf16 (16 bytes) of both tensors. Also zeroes dq_acc.
+// For every row of the padded [BH, Npad] grid: -D = -sum_c dO[c] * O[c] and
+// -LSE * log2(e) (rows past N get 0 and -inf, so that their recomputed
+// probabilities are exactly 0). Stored negated so the main kernel's packed
+// FMAs take them as addends. One group of D/8 lanes per row, each lane
+// reading 8 bf16 (16 bytes) of both tensors. Also zeroes dq_acc.
 template <int D>
 __global__ void __launch_bounds__(256) fa_bwd_pre(const __nv_bfloat16* __restrict__ o,
                                                   const __nv_bfloat16* __restrict__ dO,
@@ -147,8 +151,8 @@ __global__ void __launch_bounds__(256) fa_bwd_pre(const __nv_bfloat16* __restric
 #pragma unroll
     for (int off = kTpr / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
     if (prow < pad_rows && sub == 0) {
-      Dvec[prow] = acc;
-      lse2[prow] = live ? lse[bh * N + n] * kLog2e : INFINITY;
+      Dvec[prow] = -acc;
+      lse2[prow] = live ? -lse[bh * N + n] * kLog2e : -INFINITY;
     }
   }
   for (long long i = tid0; i < acc_vec4; i += stride) dq_acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -166,7 +170,7 @@ __global__ void __launch_bounds__(256) fa_bwd_post(const float4* __restrict__ ac
 }
 
 // ---------------------------------------------------------------- B1
-template <int D>
+template <int D, int EMU>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_bwd_main(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
@@ -334,10 +338,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int key_sw = key_row & 7;
     bool ok = true;
     for (int it = 0; it < n_steps; ++it) {
-      const float* lse2_s =
+      const float* nlse2_s =
           reinterpret_cast<const float*>(base_ptr + C::kStageOff + (it % C::kStages) * C::kStageBytes +
                                          2 * C::kTileBytes);
-      const float* dvec_s = lse2_s + kBlk;
+      const float* nd_s = nlse2_s + kBlk;
       // the stage's vectors arrive with its Q/dO tiles; S^T, dP^T with the MMA commit
       ok = mbar_wait(bar(C::kBarQFull + it % C::kStages), (it / C::kStages) & 1, abort_flag);
       if (ok) ok = mbar_wait(bar(C::kBarSFull), it & 1, abort_flag);
@@ -345,6 +349,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       tc_fence_after();
       const bool diag = args.causal && it == 0;
+      const bool emu = EMU > 0 && !diag;
+      const float2 sl2x2 = make_float2(sl2, sl2);
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t sr[32], dr[32];
@@ -352,28 +358,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld32(tDP + c * 32, dr);
         tmem_ld_wait(sr);
         tmem_ld_wait(dr);
-        float l2v[32], dvv[32];
-#pragma unroll
-        for (int e = 0; e < 32; e += 4) {
-          const float4 a4 = *reinterpret_cast<const float4*>(lse2_s + c * 32 + e);
-          const float4 b4 = *reinterpret_cast<const float4*>(dvec_s + c * 32 + e);
-          l2v[e] = a4.x; l2v[e + 1] = a4.y; l2v[e + 2] = a4.z; l2v[e + 3] = a4.w;
-          dvv[e] = b4.x; dvv[e + 1] = b4.y; dvv[e + 2] = b4.z; dvv[e + 3] = b4.w;
-        }
         uint32_t pp[16], dd[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
-          float p[2], g[2];
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int qc = c * 32 + e + u;  // query column within the block
-            float pe = ex2(fmaf(__uint_as_float(sr[e + u]), sl2, -l2v[e + u]));
-            if (diag && qc < key_row) pe = 0.f;
-            p[u] = pe;
-            g[u] = pe * (__uint_as_float(dr[e + u]) - dvv[e + u]);
+          const int qc = c * 32 + e;  // query column within the block
+          const float2 nl = *reinterpret_cast<const float2*>(nlse2_s + qc);
+          const float2 nd = *reinterpret_cast<const float2*>(nd_s + qc);
+          const float2 a = __ffma2_rn(make_float2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])),
+                                      sl2x2, nl);
+          float2 p;
+          if (EMU > 0 && emu && ((qc >> 1) % (EMU > 0 ? EMU : 1)) == (EMU > 0 ? EMU - 1 : 0)) {
+            p = exp2_poly2(a);
+          } else {
+            p.x = ex2(a.x);
+            p.y = ex2(a.y);
           }
-          pp[e >> 1] = pack_bf16(p[0], p[1]);
-          dd[e >> 1] = pack_bf16(g[0], g[1]);
+          if (diag) {  // causal diagonal block: query before key is masked
+            if (qc < key_row) p.x = 0.f;
+            if (qc + 1 < key_row) p.y = 0.f;
+          }
+          const float2 g = __fmul2_rn(
+              p, __fadd2_rn(make_float2(__uint_as_float(dr[e]), __uint_as_float(dr[e + 1])), nd));
+          pp[e >> 1] = pack_bf16(p.x, p.y);
+          dd[e >> 1] = pack_bf16(g.x, g.y);
         }
         tmem_st16(tS + c * 16, pp);
         // dS^T row of this key: queries c*32 .. c*32+31 -> four 16-byte chunks
@@ -411,9 +418,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (q < N) {
 #pragma unroll
           for (int e = 0; e < 32; e += 4)
-            atomicAdd(reinterpret_cast<float4*>(dst + c * 32 + e),
-                      make_float4(__uint_as_float(g[e]) * scale, __uint_as_float(g[e + 1]) * scale,
-                                  __uint_as_float(g[e + 2]) * scale, __uint_as_float(g[e + 3]) * scale));
+            red_add_v4(dst + c * 32 + e, __uint_as_float(g[e]) * scale,
+                       __uint_as_float(g[e + 1]) * scale, __uint_as_float(g[e + 2]) * scale,
+                       __uint_as_float(g[e + 3]) * scale);
         }
       }
       tc_fence_before();
@@ -509,7 +516,7 @@ int launch_main_d(const Problem& p, const void* dO, void* dk, void* dv, void* wo
   if (!make_map_bhnd(&mq, p.q, BH, p.N, D) || !make_map_bhnd(&mk, p.k, BH, p.N, D) ||
       !make_map_bhnd(&mv, p.v, BH, p.N, D) || !make_map_bhnd(&mdo, dO, BH, p.N, D))
     return FA_ERR_LAUNCH;
-  auto kern = fa_bwd_main<D>;
+  auto kern = fa_bwd_main<D, C::kEmuEvery>;
   if (!ensure_smem_attr(reinterpret_cast<const void*>(kern), C::kSmemBytes, D == 64 ? 2 : 3))
     return FA_ERR_LAUNCH;
   BwdArgs a;
@@ -528,7 +535,7 @@ int launch_main_d(const Problem& p, const void* dO, void* dk, void* dv, void* wo
   a.scale_log2 = p.scale * kLog2e;
   const long long grid = static_cast<long long>(a.n_blocks) * BH;
   if (grid > 0x7fffffffLL) return FA_ERR_INVALID;
-  fa_bwd_main<D><<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, mdo, a);
+  kern<<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, mdo, a);
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 

@@ -8,11 +8,13 @@
 // old sums by alpha = exp(m_old - m_new) when the maximum moves, and divides
 // once at the end. Scores S and probabilities P exist only in tensor memory.
 //
-// CTA organisation (320 threads, one CTA per SM):
+// CTA organisation (384 threads, one CTA per SM):
 //   warps 0-3  softmax warpgroup of query tile 0 (thread = row = TMEM lane)
 //   warps 4-7  softmax warpgroup of query tile 1
 //   warp  8    tcgen05 MMA issue (one thread) and TMEM allocation
-//   warp  9    TMA producer (one thread)
+//   warp  9    TMA producer (one thread); warps 10-11 idle
+// The softmax warpgroups take 216 registers per thread, the third
+// warpgroup gives its registers back down to 56.
 // Each CTA owns 256 query rows of one (batch, head): two 128-row tiles that
 // ping-pong, so the tensor core works on one tile's QK^T / PV while the
 // other tile's softmax runs.
@@ -50,7 +52,12 @@ constexpr int kQTiles = 2;
 constexpr int kSoftmaxThreads = 128 * kQTiles;
 constexpr int kMmaWarp = kSoftmaxThreads / 32;
 constexpr int kLoadWarp = kMmaWarp + 1;
-constexpr int kThreads = kSoftmaxThreads + 64;
+constexpr int kThreads = kSoftmaxThreads + 128;  // + one warpgroup: MMA, TMA, two idle warps
+// Register budgets after the split (launch: 168 per thread x 384 threads).
+constexpr uint32_t kRegsSoftmax = 216;
+constexpr uint32_t kRegsOther = 56;
+static_assert(kRegsSoftmax * kSoftmaxThreads + kRegsOther * 128 <= 168 * kThreads,
+              "register split exceeds the launch allocation");
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr float kLn2 = 0.6931471805599453f;
 
@@ -60,6 +67,9 @@ struct FwdCfg {
   static constexpr int kChunkBytes = kBlockM * 64 * 2;      // 16 KiB
   static constexpr int kTileBytes = kChunks * kChunkBytes;  // 128 rows x d
   static constexpr int kStages = (D == 64) ? 4 : 2;
+  // Every kEmuEvery-th pair of probabilities on an unmasked tile uses the
+  // polynomial exp2 on the FMA pipe instead of MUFU ex2 (0: never).
+  static constexpr int kEmuEvery = (D == 64) ? 3 : 0;
   static constexpr int kQOff = 0;
   static constexpr int kKOff = kQOff + kQTiles * kTileBytes;
   static constexpr int kVOff = kKOff + kStages * kTileBytes;
@@ -92,7 +102,7 @@ struct FwdArgs {
   float scale_log2;  // scale * log2(e), > 0
 };
 
-template <int D>
+template <int D, int EMU>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const FwdArgs args) {
@@ -146,6 +156,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  if (warp >= kMmaWarp) regs_decrease<kRegsOther>();
 
   if (warp == kLoadWarp) {
     // ------------------------------------------------------------ producer
@@ -154,9 +165,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_map(&tmK);
       tma_prefetch_map(&tmV);
       uint32_t q_bytes = 0;
+#pragma unroll
       for (int t = 0; t < kQTiles; ++t)
         if (n_t[t] > 0) q_bytes += C::kTileBytes;
       mbar_arrive_expect_tx(bar(C::kBarQFull), q_bytes);
+#pragma unroll
       for (int t = 0; t < kQTiles; ++t) {
         if (n_t[t] == 0) continue;
         for (int c = 0; c < C::kChunks; ++c)
@@ -233,6 +246,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       ensure_k(0);
       if (ok) {
+#pragma unroll
         for (int t = 0; t < kQTiles; ++t)
           if (n_t[t] > 0) issue_s(t, 0);
         mma_commit(bar(C::kBarKEmpty + 0));
@@ -240,8 +254,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < n_max && ok; ++j) {
         ok = mbar_wait(bar(C::kBarVFull + j % C::kStages), (j / C::kStages) & 1, abort_flag);
         tc_fence_after();
-        for (int t = 0; t < kQTiles && ok; ++t) {
-          if (j >= n_t[t]) continue;
+#pragma unroll
+        for (int t = 0; t < kQTiles; ++t) {
+          if (!ok || j >= n_t[t]) continue;
           ok = mbar_wait(bar(C::kBarPFull + t), j & 1, abort_flag);
           if (!ok) break;
           tc_fence_after();
@@ -262,22 +277,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_commit(bar(C::kBarDrain));
       mbar_wait(bar(C::kBarDrain), 0, nullptr);
     }
-  } else {
+  } else if (warp < kMmaWarp) {
     // ------------------------------------------------------------ softmax
+    regs_increase<kRegsSoftmax>();
     const int t = warp / 4;
+    const int tile_row0 = pair * (kBlockM * kQTiles) + t * kBlockM;
+    const int n_mine = tile_row0 >= N ? 0 : (args.causal ? tile_row0 / kBlockN + 1 : n_kv);
     const int row_in_tile = threadIdx.x & 127;
-    const int row = q_row0[t] + row_in_tile;
+    const int row = tile_row0 + row_in_tile;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + lane_base + t * 128;
     const uint32_t tO = tmem + lane_base + C::kColO + t * D;
     const float sl2 = args.scale_log2;
-    const int diag_j = q_row0[t] / kBlockN;
+    const int diag_j = tile_row0 / kBlockN;
     const bool ragged = (N % kBlockN) != 0;
 
     float m_ref = -INFINITY;  // log2-domain reference maximum
     float l = 0.f;
     bool ok = true;
-    for (int j = 0; j < n_t[t]; ++j) {
+    for (int j = 0; j < n_mine; ++j) {
       ok = mbar_wait(bar(C::kBarSFull + t), j & 1, abort_flag);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
@@ -299,39 +317,41 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < 128; ++c)
           if (c >= lim) x[c] = -INFINITY;
       }
-      float mx0 = x[0], mx1 = x[1], mx2 = x[2], mx3 = x[3];
-#pragma unroll
-      for (int c = 4; c < 128; c += 4) {
-        mx0 = fmaxf(mx0, x[c]);
-        mx1 = fmaxf(mx1, x[c + 1]);
-        mx2 = fmaxf(mx2, x[c + 2]);
-        mx3 = fmaxf(mx3, x[c + 3]);
-      }
-      const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+      const float m_tile =
+          max3(fmaxf(max32(x), max32(x + 32)), max32(x + 64), max32(x + 96)) * sl2;
       const bool need = m_tile > m_ref + kRescaleThreshold;
       const float m_old = m_ref;
       if (need) m_ref = m_tile;
       const float alpha = need ? ex2(m_old - m_ref) : 1.0f;
       const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
 
-      uint32_t pk[2][32];
-      float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+      // p = exp2(s * scale * log2(e) - m_ref), packed two at a time; on
+      // unmasked tiles every kEmuEvery-th pair takes the polynomial exp2
+      const float2 sl2x2 = make_float2(sl2, sl2);
+      const float2 negm = make_float2(-m_use, -m_use);
+      float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+      const bool emu = EMU > 0 && !need_mask;
 #pragma unroll
-      for (int c = 0; c < 64; c += 2) {
-        const float p0 = ex2(fmaf(x[2 * c], sl2, -m_use));
-        const float p1 = ex2(fmaf(x[2 * c + 1], sl2, -m_use));
-        const float p2 = ex2(fmaf(x[2 * c + 2], sl2, -m_use));
-        const float p3 = ex2(fmaf(x[2 * c + 3], sl2, -m_use));
-        s0 += p0;
-        s1 += p1;
-        s2 += p2;
-        s3 += p3;
-        pk[c >> 5][c & 31] = pack_bf16(p0, p1);
-        pk[(c + 1) >> 5][(c + 1) & 31] = pack_bf16(p2, p3);
+      for (int h = 0; h < 2; ++h) {  // P columns [32h, 32h+32) hold scores [64h, 64h+64)
+        uint32_t pk[32];
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          const int e = 64 * h + 2 * c;
+          const float2 a = __ffma2_rn(make_float2(x[e], x[e + 1]), sl2x2, negm);
+          float2 pr;
+          if (EMU > 0 && emu && ((32 * h + c) % (EMU > 0 ? EMU : 1)) == (EMU > 0 ? EMU - 1 : 0)) {
+            pr = exp2_poly2(a);
+          } else {
+            pr.x = ex2(a.x);
+            pr.y = ex2(a.y);
+          }
+          if (c & 1) acc1 = __fadd2_rn(acc1, pr);
+          else acc0 = __fadd2_rn(acc0, pr);
+          pk[c] = pack_bf16(pr.x, pr.y);
+        }
+        tmem_st32(tS + 32 * h, pk);
       }
-      l = alpha * l + ((s0 + s1) + (s2 + s3));
-      tmem_st32(tS, pk[0]);
-      tmem_st32(tS + 32, pk[1]);
+      l = alpha * l + ((acc0.x + acc0.y) + (acc1.x + acc1.y));
 
       // Rescale the accumulator when this warp's maximum moved. The S MMA of
       // this tile was committed after the previous P.V, so O is settled.
@@ -341,8 +361,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t o[32];
           tmem_ld32(tO + c * 32, o);
           tmem_ld_wait(o);
+          const float2 al2 = make_float2(alpha, alpha);
 #pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+          for (int e = 0; e < 32; e += 2) {
+            const float2 v = __fmul2_rn(make_float2(__uint_as_float(o[e]), __uint_as_float(o[e + 1])), al2);
+            o[e] = __float_as_uint(v.x);
+            o[e + 1] = __float_as_uint(v.y);
+          }
           tmem_st32(tO + c * 32, o);
         }
       }
@@ -350,7 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       mbar_arrive(bar(C::kBarPFull + t));
     }
-    if (ok && n_t[t] > 0) {
+    if (ok && n_mine > 0) {
       ok = mbar_wait(bar(C::kBarOFinal + t), 0, abort_flag);
       ok = __all_sync(0xffffffffu, ok);
       if (ok) {
@@ -364,9 +389,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld32(tO + c * 32, o);
           tmem_ld_wait(o);
           uint32_t pk[16];
+          const float2 il2 = make_float2(inv_l, inv_l);
 #pragma unroll
-          for (int e = 0; e < 16; ++e)
-            pk[e] = pack_bf16(__uint_as_float(o[2 * e]) * inv_l, __uint_as_float(o[2 * e + 1]) * inv_l);
+          for (int e = 0; e < 16; ++e) {
+            const float2 v =
+                __fmul2_rn(make_float2(__uint_as_float(o[2 * e]), __uint_as_float(o[2 * e + 1])), il2);
+            pk[e] = pack_bf16(v.x, v.y);
+          }
           if (live) {
             uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
 #pragma unroll
@@ -403,7 +432,8 @@ int launch_fwd_d(const Problem& p, void* o, float* lse, cudaStream_t stream) {
     return -3;
   int* status = device_status_word();
   if (!status) return -3;
-  auto kern = fa_fwd_kernel<D>;
+  constexpr int kEmu = FwdCfg<D>::kEmuEvery;
+  auto kern = fa_fwd_kernel<D, kEmu>;
   if (!ensure_smem_attr(reinterpret_cast<const void*>(kern), C::kSmemBytes, D == 64 ? 0 : 1))
     return -3;
   FwdArgs a;
@@ -420,7 +450,7 @@ int launch_fwd_d(const Problem& p, void* o, float* lse, cudaStream_t stream) {
   a.scale_log2 = sl2 > 1e-30f ? sl2 : 1e-30f;
   const long long grid = static_cast<long long>(a.num_pairs) * BH;
   if (grid > 0x7fffffffLL) return -1;
-  fa_fwd_kernel<D><<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, a);
+  kern<<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, a);
   return cudaGetLastError() == cudaSuccess ? 0 : -3;
 }
 

@@ -10,6 +10,7 @@
 
 #include <cstdint>
 #include <cuda.h>
+#include <cuda_runtime.h>
 
 namespace fa {
 
@@ -111,6 +112,13 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
       : "memory");
 }
 
+// Fire-and-forget 16-byte add into global memory (no value returned).
+__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b),
+               "f"(c), "f"(d)
+               : "memory");
+}
+
 // ---------------------------------------------------------------- fences
 __device__ __forceinline__ void fence_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -123,6 +131,20 @@ __device__ __forceinline__ void tc_fence_after() {
 }
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// ---------------------------------------------------------------- registers
+// Per-warpgroup register budget (all four warps of the warpgroup execute
+// it). The increases of a CTA are served from what its decreases free, so
+// the new budgets, summed over warpgroups, must fit in the registers the
+// CTA was launched with.
+template <uint32_t R>
+__device__ __forceinline__ void regs_increase() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(R));
+}
+template <uint32_t R>
+__device__ __forceinline__ void regs_decrease() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(R));
 }
 
 // ---------------------------------------------------------------- TMEM
@@ -268,6 +290,45 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
 }
 
 // ---------------------------------------------------------------- math
+// 3-input maximum (one instruction on sm_100 and later).
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// Maximum of 32 consecutive values.
+__device__ __forceinline__ float max32(const float* x) {
+  float m = x[0];
+#pragma unroll
+  for (int i = 1; i < 31; i += 2) m = max3(m, x[i], x[i + 1]);
+  return fmaxf(m, x[31]);
+}
+
+// 2^x for two lanes on the FMA pipe, for x <= 8 (x below -125 is clamped,
+// giving about 2e-38 instead of 0). Range reduction 2^x = 2^n * 2^f with
+// n = round(x) via the 1.5 * 2^23 rounding constant, f = x - n in
+// [-1/2, 1/2]; 2^f from a degree-3 minimax polynomial (coefficients and
+// their derivation: fit_exp2_poly.py; max relative error 7.5e-5), and 2^n
+// added into the exponent field. Used for part of the probabilities so the
+// MUFU ex2 unit is not the only exp2 pipe.
+__device__ __forceinline__ float2 exp2_poly2(float2 x) {
+  constexpr float kRound = 12582912.0f;  // 1.5 * 2^23
+  x.x = fmaxf(x.x, -125.0f);
+  x.y = fmaxf(x.y, -125.0f);
+  const float2 t = __fadd2_rn(x, make_float2(kRound, kRound));
+  const float2 n = __fadd2_rn(t, make_float2(-kRound, -kRound));
+  const float2 f = __ffma2_rn(n, make_float2(-1.0f, -1.0f), x);
+  float2 p = __ffma2_rn(f, make_float2(5.517166853e-02f, 5.517166853e-02f),
+                        make_float2(2.426111251e-01f, 2.426111251e-01f));
+  p = __ffma2_rn(p, f, make_float2(6.932609677e-01f, 6.932609677e-01f));
+  p = __ffma2_rn(p, f, make_float2(9.999280572e-01f, 9.999280572e-01f));
+  // the low bits of t hold n (two's complement); shifted into the exponent
+  const int ex = __float_as_int(p.x) + (__float_as_int(t.x) << 23);
+  const int ey = __float_as_int(p.y) + (__float_as_int(t.y) << 23);
+  return make_float2(__int_as_float(ex), __int_as_float(ey));
+}
+
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
