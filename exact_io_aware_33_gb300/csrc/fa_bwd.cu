@@ -24,12 +24,15 @@
 //                dQ_i is added into the fp32 accumulator in global memory.
 //   fa_bwd_post  dQ = bf16(accumulator)
 //
-// CTA of fa_bwd_main (320 threads):
-//   warps 0-3  "softmax" warpgroup: thread = key row = TMEM lane
-//   warps 4-7  dQ warpgroup: reads dQ_i (thread = query row) and adds it
+// CTA of fa_bwd_main (512 threads):
+//   warps 0-7  two P/dS warpgroups: thread = key row = TMEM lane; warpgroup
+//              w handles query columns [64w, 64w+64) of each step, and the
+//              S^T / dP^T MMAs run one query half at a time, so the first
+//              half's P/dS work overlaps the second half's MMAs
+//   warps 8-11 dQ warpgroup: reads dQ_i (thread = query row) and adds it
 //              into global memory; writes dK, dV at the end (thread = key)
-//   warp  8    tcgen05 MMA issue and TMEM allocation
-//   warp  9    TMA producer
+//   warp  12   tcgen05 MMA issue and TMEM allocation
+//   warp  13   TMA producer; warps 14-15 idle
 //
 // TMEM columns: S^T/P^T [0,128), dP^T [128,256); for d = 64 dQ [256,320),
 // dK [320,384), dV [384,448); for d = 128 dQ reuses the dP^T columns (the
@@ -46,9 +49,11 @@ namespace fa {
 namespace {
 
 constexpr int kBlk = 128;  // keys per CTA block and queries per step
-constexpr int kThreads = 320;
-constexpr int kMmaWarp = 8;
-constexpr int kLoadWarp = 9;
+constexpr int kHalf = 64;  // query columns per P/dS warpgroup
+constexpr int kThreads = 512;
+constexpr int kDqWarp0 = 8;
+constexpr int kMmaWarp = 12;
+constexpr int kLoadWarp = 13;
 constexpr float kLog2e = 1.4426950408889634f;
 
 template <int D>
@@ -59,9 +64,6 @@ struct BwdCfg {
   static constexpr int kVecBytes = 2 * kBlk * 4;  // lse2[128], D[128] of one query block
   static constexpr int kStages = (D == 64) ? 3 : 2;
   static constexpr bool kDqAliasDp = (D == 128);
-  // Every kEmuEvery-th pair of probabilities off the causal diagonal uses
-  // the polynomial exp2 on the FMA pipe instead of MUFU ex2 (0: never).
-  static constexpr int kEmuEvery = 0;
   static constexpr int kKOff = 0;
   static constexpr int kVOff = kKOff + kTileBytes;
   static constexpr int kDSOff = kVOff + kTileBytes;             // 2 x 16 KiB
@@ -71,9 +73,9 @@ struct BwdCfg {
   static constexpr int kBarKV = 0;
   static constexpr int kBarQFull = 1;
   static constexpr int kBarQEmpty = kBarQFull + kStages;
-  static constexpr int kBarSFull = kBarQEmpty + kStages;
-  static constexpr int kBarDSFull = kBarSFull + 1;
-  static constexpr int kBarDQFull = kBarDSFull + 1;
+  static constexpr int kBarSFull = kBarQEmpty + kStages;    // one per query half
+  static constexpr int kBarDSFull = kBarSFull + 2;           // one per query half
+  static constexpr int kBarDQFull = kBarDSFull + 2;
   static constexpr int kBarDQEmpty = kBarDQFull + 1;
   static constexpr int kBarDKDV = kBarDQEmpty + 1;
   static constexpr int kBarDrain = kBarDKDV + 1;
@@ -170,7 +172,7 @@ __global__ void __launch_bounds__(256) fa_bwd_post(const float4* __restrict__ ac
 }
 
 // ---------------------------------------------------------------- B1
-template <int D, int EMU>
+template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_bwd_main(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
@@ -203,8 +205,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(C::kBarQFull + s), 1);
       mbar_init(bar(C::kBarQEmpty + s), 1);
     }
-    mbar_init(bar(C::kBarSFull), 1);
-    mbar_init(bar(C::kBarDSFull), 128);
+    for (int h = 0; h < 2; ++h) {
+      mbar_init(bar(C::kBarSFull + h), 1);
+      mbar_init(bar(C::kBarDSFull + h), 128);
+    }
     mbar_init(bar(C::kBarDQFull), 1);
     mbar_init(bar(C::kBarDQEmpty), 128);
     mbar_init(bar(C::kBarDKDV), 1);
@@ -262,7 +266,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issue
     if (lane == 0) {
-      constexpr uint32_t kIdT = idesc_bf16_f32(kBlk, kBlk, false, false);  // S^T, dP^T
+      constexpr uint32_t kIdT = idesc_bf16_f32(kBlk, kHalf, false, false); // S^T, dP^T halves
       constexpr uint32_t kIdKV = idesc_bf16_f32(kBlk, D, false, true);     // dV, dK
       constexpr uint32_t kIdQ = idesc_bf16_f32(kBlk, D, true, true);       // dQ
       const uint32_t kb = base + C::kKOff, vb = base + C::kVOff, dsb = base + C::kDSOff;
@@ -275,41 +279,49 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint32_t qb = base + C::kStageOff + s * C::kStageBytes;
         const uint32_t dob = qb + C::kTileBytes;
-        // S^T = K Q^T
+        // S^T and dP^T one query half (64 columns) at a time, so the first
+        // half's P/dS work overlaps the second half's MMAs
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
-          mma_ss(tmem + C::kColS, sdesc_sw128(kb + off, 16, 1024), sdesc_sw128(qb + off, 16, 1024),
-                 kIdT, kk > 0 ? 1u : 0u);
+        for (int h = 0; h < 2; ++h) {
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {  // S^T_h = K Q_h^T
+            const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
+            mma_ss(tmem + C::kColS + kHalf * h, sdesc_sw128(kb + off, 16, 1024),
+                   sdesc_sw128(qb + off + h * 8192, 16, 1024), kIdT, kk > 0 ? 1u : 0u);
+          }
+          if (C::kDqAliasDp && h == 0 && it > 0) {  // dQ of the last step shares dP's columns
+            ok = mbar_wait(bar(C::kBarDQEmpty), (it - 1) & 1, abort_flag);
+            if (!ok) break;
+            tc_fence_after();
+          }
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {  // dP^T_h = V dO_h^T
+            const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
+            mma_ss(tmem + C::kColDP + kHalf * h, sdesc_sw128(vb + off, 16, 1024),
+                   sdesc_sw128(dob + off + h * 8192, 16, 1024), kIdT, kk > 0 ? 1u : 0u);
+          }
+          mma_commit(bar(C::kBarSFull + h));
         }
-        if (C::kDqAliasDp && it > 0) {
-          ok = mbar_wait(bar(C::kBarDQEmpty), (it - 1) & 1, abort_flag);
+        if (!ok) break;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          ok = mbar_wait(bar(C::kBarDSFull + h), it & 1, abort_flag);
           if (!ok) break;
           tc_fence_after();
-        }
-        // dP^T = V dO^T
+          // dV += P_h^T dO_h   (A = P^T in TMEM, B = dO rows of half h, MN-major)
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
-          mma_ss(tmem + C::kColDP, sdesc_sw128(vb + off, 16, 1024),
-                 sdesc_sw128(dob + off, 16, 1024), kIdT, kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < kHalf / 16; ++kk)
+            mma_ts(tmem + C::kColDV, tmem + C::kColS + kHalf * h + kk * 8,
+                   sdesc_sw128(dob + (4 * h + kk) * 2048, C::kChunkBytes, 1024), kIdKV,
+                   (it > 0 || h > 0 || kk > 0) ? 1u : 0u);
+          // dK += dS_h^T Q_h   (A = dS^T K-major in smem region h, B = Q MN-major)
+#pragma unroll
+          for (int kk = 0; kk < kHalf / 16; ++kk)
+            mma_ss(tmem + C::kColDK, sdesc_sw128(dsb + h * C::kChunkBytes + kk * 32, 16, 1024),
+                   sdesc_sw128(qb + (4 * h + kk) * 2048, C::kChunkBytes, 1024), kIdKV,
+                   (it > 0 || h > 0 || kk > 0) ? 1u : 0u);
         }
-        mma_commit(bar(C::kBarSFull));
-        ok = mbar_wait(bar(C::kBarDSFull), it & 1, abort_flag);
         if (!ok) break;
-        tc_fence_after();
-        // dV += P^T dO      (A = P^T in TMEM, B = dO MN-major)
-#pragma unroll
-        for (int kk = 0; kk < kBlk / 16; ++kk)
-          mma_ts(tmem + C::kColDV, tmem + C::kColS + kk * 8,
-                 sdesc_sw128(dob + kk * 2048, C::kChunkBytes, 1024), kIdKV,
-                 (it > 0 || kk > 0) ? 1u : 0u);
-        // dK += dS^T Q      (A = dS^T K-major in smem, B = Q MN-major)
-#pragma unroll
-        for (int kk = 0; kk < kBlk / 16; ++kk)
-          mma_ss(tmem + C::kColDK, sdesc_sw128(dsb + (kk >> 2) * C::kChunkBytes + (kk & 3) * 32, 16, 1024),
-                 sdesc_sw128(qb + kk * 2048, C::kChunkBytes, 1024), kIdKV,
-                 (it > 0 || kk > 0) ? 1u : 0u);
         if (!C::kDqAliasDp && it > 0) {
           ok = mbar_wait(bar(C::kBarDQEmpty), (it - 1) & 1, abort_flag);
           if (!ok) break;
@@ -327,32 +339,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_commit(bar(C::kBarDrain));
       mbar_wait(bar(C::kBarDrain), 0, nullptr);
     }
-  } else if (warp < 4) {
+  } else if (warp < kDqWarp0) {
     // ------------------------------------------------------------ P and dS
-    const int key_row = threadIdx.x;  // 0..127
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-    const uint32_t tS = tmem + lane_base + C::kColS;
-    const uint32_t tDP = tmem + lane_base + C::kColDP;
+    // warpgroup w owns query columns [64w, 64w+64) of every step
+    const int w = warp >> 2;
+    const int key_row = threadIdx.x & 127;
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + lane_base + C::kColS + kHalf * w;
+    const uint32_t tDP = tmem + lane_base + C::kColDP + kHalf * w;
     const float sl2 = args.scale_log2;
-    uint8_t* ds_base = base_ptr + C::kDSOff + key_row * 128;
+    uint8_t* ds_base = base_ptr + C::kDSOff + w * C::kChunkBytes + key_row * 128;
     const int key_sw = key_row & 7;
+    const float2 sl2x2 = make_float2(sl2, sl2);
     bool ok = true;
     for (int it = 0; it < n_steps; ++it) {
       const float* nlse2_s =
           reinterpret_cast<const float*>(base_ptr + C::kStageOff + (it % C::kStages) * C::kStageBytes +
-                                         2 * C::kTileBytes);
+                                         2 * C::kTileBytes) + kHalf * w;
       const float* nd_s = nlse2_s + kBlk;
       // the stage's vectors arrive with its Q/dO tiles; S^T, dP^T with the MMA commit
       ok = mbar_wait(bar(C::kBarQFull + it % C::kStages), (it / C::kStages) & 1, abort_flag);
-      if (ok) ok = mbar_wait(bar(C::kBarSFull), it & 1, abort_flag);
+      if (ok) ok = mbar_wait(bar(C::kBarSFull + w), it & 1, abort_flag);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
       const bool diag = args.causal && it == 0;
-      const bool emu = EMU > 0 && !diag;
-      const float2 sl2x2 = make_float2(sl2, sl2);
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 2; ++c) {
         uint32_t sr[32], dr[32];
         tmem_ld32(tS + c * 32, sr);
         tmem_ld32(tDP + c * 32, dr);
@@ -361,18 +374,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t pp[16], dd[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
-          const int qc = c * 32 + e;  // query column within the block
-          const float2 nl = *reinterpret_cast<const float2*>(nlse2_s + qc);
-          const float2 nd = *reinterpret_cast<const float2*>(nd_s + qc);
+          const int ql = c * 32 + e;            // query column within this half
+          const int qc = kHalf * w + ql;        // ... within the block
+          const float2 nl = *reinterpret_cast<const float2*>(nlse2_s + ql);
+          const float2 nd = *reinterpret_cast<const float2*>(nd_s + ql);
           const float2 a = __ffma2_rn(make_float2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])),
                                       sl2x2, nl);
-          float2 p;
-          if (EMU > 0 && emu && ((qc >> 1) % (EMU > 0 ? EMU : 1)) == (EMU > 0 ? EMU - 1 : 0)) {
-            p = exp2_poly2(a);
-          } else {
-            p.x = ex2(a.x);
-            p.y = ex2(a.y);
-          }
+          float2 p = make_float2(ex2(a.x), ex2(a.y));
           if (diag) {  // causal diagonal block: query before key is masked
             if (qc < key_row) p.x = 0.f;
             if (qc + 1 < key_row) p.y = 0.f;
@@ -383,23 +391,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           dd[e >> 1] = pack_bf16(g.x, g.y);
         }
         tmem_st16(tS + c * 16, pp);
-        // dS^T row of this key: queries c*32 .. c*32+31 -> four 16-byte chunks
-        uint8_t* region = ds_base + (c >> 1) * C::kChunkBytes;
+        // dS^T row of this key: 32 queries -> four swizzled 16-byte chunks
 #pragma unroll
         for (int v = 0; v < 4; ++v) {
-          const int chunk = ((c & 1) * 4 + v) ^ key_sw;
-          *reinterpret_cast<uint4*>(region + chunk * 16) =
+          const int chunk = (c * 4 + v) ^ key_sw;
+          *reinterpret_cast<uint4*>(ds_base + chunk * 16) =
               make_uint4(dd[4 * v], dd[4 * v + 1], dd[4 * v + 2], dd[4 * v + 3]);
         }
       }
       tmem_st_wait();
       tc_fence_before();
       fence_async_smem();
-      mbar_arrive(bar(C::kBarDSFull));
+      mbar_arrive(bar(C::kBarDSFull + w));
     }
-  } else {
+  } else if (warp < kMmaWarp) {
     // ------------------------------------------------------------ dQ, dK, dV out
-    const int r = threadIdx.x - 128;  // TMEM lane: query row of dQ, key row of dK/dV
+    const int r = threadIdx.x - 32 * kDqWarp0;  // TMEM lane: query row of dQ, key row of dK/dV
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const float scale = args.scale;
     bool ok = true;
@@ -516,7 +523,7 @@ int launch_main_d(const Problem& p, const void* dO, void* dk, void* dv, void* wo
   if (!make_map_bhnd(&mq, p.q, BH, p.N, D) || !make_map_bhnd(&mk, p.k, BH, p.N, D) ||
       !make_map_bhnd(&mv, p.v, BH, p.N, D) || !make_map_bhnd(&mdo, dO, BH, p.N, D))
     return FA_ERR_LAUNCH;
-  auto kern = fa_bwd_main<D, C::kEmuEvery>;
+  auto kern = fa_bwd_main<D>;
   if (!ensure_smem_attr(reinterpret_cast<const void*>(kern), C::kSmemBytes, D == 64 ? 2 : 3))
     return FA_ERR_LAUNCH;
   BwdArgs a;

@@ -67,9 +67,6 @@ struct FwdCfg {
   static constexpr int kChunkBytes = kBlockM * 64 * 2;      // 16 KiB
   static constexpr int kTileBytes = kChunks * kChunkBytes;  // 128 rows x d
   static constexpr int kStages = (D == 64) ? 4 : 2;
-  // Every kEmuEvery-th pair of probabilities on an unmasked tile uses the
-  // polynomial exp2 on the FMA pipe instead of MUFU ex2 (0: never).
-  static constexpr int kEmuEvery = (D == 64) ? 3 : 0;
   static constexpr int kQOff = 0;
   static constexpr int kKOff = kQOff + kQTiles * kTileBytes;
   static constexpr int kVOff = kKOff + kStages * kTileBytes;
@@ -102,7 +99,7 @@ struct FwdArgs {
   float scale_log2;  // scale * log2(e), > 0
 };
 
-template <int D, int EMU>
+template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const FwdArgs args) {
@@ -325,12 +322,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float alpha = need ? ex2(m_old - m_ref) : 1.0f;
       const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
 
-      // p = exp2(s * scale * log2(e) - m_ref), packed two at a time; on
-      // unmasked tiles every kEmuEvery-th pair takes the polynomial exp2
+      // p = exp2(s * scale * log2(e) - m_ref), packed two at a time
       const float2 sl2x2 = make_float2(sl2, sl2);
       const float2 negm = make_float2(-m_use, -m_use);
       float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
-      const bool emu = EMU > 0 && !need_mask;
 #pragma unroll
       for (int h = 0; h < 2; ++h) {  // P columns [32h, 32h+32) hold scores [64h, 64h+64)
         uint32_t pk[32];
@@ -338,13 +333,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < 32; ++c) {
           const int e = 64 * h + 2 * c;
           const float2 a = __ffma2_rn(make_float2(x[e], x[e + 1]), sl2x2, negm);
-          float2 pr;
-          if (EMU > 0 && emu && ((32 * h + c) % (EMU > 0 ? EMU : 1)) == (EMU > 0 ? EMU - 1 : 0)) {
-            pr = exp2_poly2(a);
-          } else {
-            pr.x = ex2(a.x);
-            pr.y = ex2(a.y);
-          }
+          const float2 pr = make_float2(ex2(a.x), ex2(a.y));
           if (c & 1) acc1 = __fadd2_rn(acc1, pr);
           else acc0 = __fadd2_rn(acc0, pr);
           pk[c] = pack_bf16(pr.x, pr.y);
@@ -432,8 +421,7 @@ int launch_fwd_d(const Problem& p, void* o, float* lse, cudaStream_t stream) {
     return -3;
   int* status = device_status_word();
   if (!status) return -3;
-  constexpr int kEmu = FwdCfg<D>::kEmuEvery;
-  auto kern = fa_fwd_kernel<D, kEmu>;
+  auto kern = fa_fwd_kernel<D>;
   if (!ensure_smem_attr(reinterpret_cast<const void*>(kern), C::kSmemBytes, D == 64 ? 0 : 1))
     return -3;
   FwdArgs a;

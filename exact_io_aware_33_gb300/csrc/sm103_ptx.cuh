@@ -305,30 +305,6 @@ __device__ __forceinline__ float max32(const float* x) {
   return fmaxf(m, x[31]);
 }
 
-// 2^x for two lanes on the FMA pipe, for x <= 8 (x below -125 is clamped,
-// giving about 2e-38 instead of 0). Range reduction 2^x = 2^n * 2^f with
-// n = round(x) via the 1.5 * 2^23 rounding constant, f = x - n in
-// [-1/2, 1/2]; 2^f from a degree-3 minimax polynomial (coefficients and
-// their derivation: fit_exp2_poly.py; max relative error 7.5e-5), and 2^n
-// added into the exponent field. Used for part of the probabilities so the
-// MUFU ex2 unit is not the only exp2 pipe.
-__device__ __forceinline__ float2 exp2_poly2(float2 x) {
-  constexpr float kRound = 12582912.0f;  // 1.5 * 2^23
-  x.x = fmaxf(x.x, -125.0f);
-  x.y = fmaxf(x.y, -125.0f);
-  const float2 t = __fadd2_rn(x, make_float2(kRound, kRound));
-  const float2 n = __fadd2_rn(t, make_float2(-kRound, -kRound));
-  const float2 f = __ffma2_rn(n, make_float2(-1.0f, -1.0f), x);
-  float2 p = __ffma2_rn(f, make_float2(5.517166853e-02f, 5.517166853e-02f),
-                        make_float2(2.426111251e-01f, 2.426111251e-01f));
-  p = __ffma2_rn(p, f, make_float2(6.932609677e-01f, 6.932609677e-01f));
-  p = __ffma2_rn(p, f, make_float2(9.999280572e-01f, 9.999280572e-01f));
-  // the low bits of t hold n (two's complement); shifted into the exponent
-  const int ex = __float_as_int(p.x) + (__float_as_int(t.x) << 23);
-  const int ey = __float_as_int(p.y) + (__float_as_int(t.y) << 23);
-  return make_float2(__int_as_float(ex), __int_as_float(ey));
-}
-
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
