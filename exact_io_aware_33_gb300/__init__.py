@@ -49,6 +49,7 @@ SIGNATURES = {
     "fa_bwd_preprocess_stream": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _S, _P]),
     "fa_bwd_main_stream": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P, _S, _P]),
     "fa_bwd_finish_stream": (_I, [_P, _I, _I, _I, _I, _P, _S, _P]),
+    "fa_bwd_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P]),
     "fa_bwd_workspace_bytes": (_S, [_I, _I, _I, _I]),
     "fa_strerror": (ctypes.c_char_p, [_I]),
     "fa_get_last_device_status": (_I, []),
@@ -189,4 +190,41 @@ def fa_bwd(q, k, v, o, lse, do, causal: bool = False, scale: float | None = None
                                _ptr(workspace), ctypes.c_size_t(workspace.numel()),
                                _stream_handle(stream, q.device))
     _check(rc, "fa_bwd")
+    return dq, dk, dv
+
+
+# Size of the scratch array built into the library for fa_bwd_noalloc.
+FA_BWD_NOALLOC_MAX_SCRATCH_BYTES = 64 << 20
+
+
+def fa_bwd_noalloc(q, k, v, o, lse, do, causal: bool = False, scale: float | None = None,
+                   dq=None, dk=None, dv=None, stream=None):
+    """fa_bwd using the library's built-in scratch array instead of a workspace.
+
+    For callers that may not allocate device memory on this path (the C entry
+    point allocates nothing; passing dq/dk/dv keeps this wrapper allocation
+    free too). Problems needing more than FA_BWD_NOALLOC_MAX_SCRATCH_BYTES of
+    workspace raise FAError(FA_ERR_WORKSPACE). Calls that overlap on the GPU
+    share the scratch and race: keep them on one stream.
+    """
+    import torch
+    if q.dim() != 4:
+        raise ValueError("q must be [B, H, N, d]")
+    B, H, N, d = q.shape
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("do", do)):
+        _check_tensor(t, name, (B, H, N, d), torch.bfloat16)
+    _check_tensor(lse, "lse", (B, H, N), torch.float32)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
+        _check_tensor(t, name, (B, H, N, d), torch.bfloat16)
+    lib = load_library()
+    with torch.cuda.device(q.device):
+        rc = lib.fa_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do), _ptr(dq),
+                                _ptr(dk), _ptr(dv), B, H, N, d, int(bool(causal)), float(scale),
+                                _stream_handle(stream, q.device))
+    _check(rc, "fa_bwd_noalloc")
     return dq, dk, dv

@@ -113,6 +113,11 @@ bool make_map_bhnd(CUtensorMap* map, const void* ptr, int BH, int N, int d) {
   return r == CUDA_SUCCESS;
 }
 
+int current_device_status() {
+  DeviceState* st = nullptr;
+  return current_device(&st);
+}
+
 int* device_status_word() {
   DeviceState* st = nullptr;
   if (current_device(&st) != FA_OK) return nullptr;

@@ -22,6 +22,9 @@ struct Problem {
 // 128 rows x 64 columns and 128-byte swizzle. Returns false on failure.
 bool make_map_bhnd(CUtensorMap* map, const void* ptr, int BH, int N, int d);
 
+// FA_OK when the current device is a CC 10.3 GPU, else the error code.
+int current_device_status();
+
 // Device pointer of the status word of the current device (nullptr on error).
 int* device_status_word();
 

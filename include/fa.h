@@ -130,6 +130,29 @@ int fa_bwd_main_stream(const void* q, const void* k, const void* v, const void* 
 int fa_bwd_finish_stream(void* dq, int B, int H, int N, int d, const void* workspace,
                          size_t ws_bytes, void* cuda_stream);
 
+/*
+ * fa_bwd_noalloc: fa_bwd_stream without a caller workspace and without
+ * allocating anything. The pages have no counterpart to this entry point; it
+ * exists for callers that cannot allocate device memory: a host framework
+ * that owns every device allocation and forbids libraries to allocate, or a
+ * serving loop with a fixed memory budget that must not call cudaMalloc on
+ * its hot path (the call can synchronise the device and can fail once memory
+ * is fragmented).
+ * The workspace is a file-scope device array of
+ * FA_BWD_NOALLOC_MAX_SCRATCH_BYTES bytes inside the library, held by every
+ * GPU that loads the library until the process exits. Problems whose
+ * fa_bwd_workspace_bytes exceed it return FA_ERR_WORKSPACE and launch
+ * nothing. The first call on a device looks up the array's device address
+ * (no allocation); make that first call before any stream capture. All calls
+ * share the array: calls whose kernels overlap on the GPU (other streams,
+ * other host threads) race and corrupt each other's results, so serialise
+ * them on one stream. Arguments and results are those of fa_bwd_stream.
+ */
+#define FA_BWD_NOALLOC_MAX_SCRATCH_BYTES ((size_t)64 << 20)
+int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                   const void* dO, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+                   int causal, float scale, void* cuda_stream);
+
 /* Workspace bytes fa_bwd_stream needs for these sizes (0 when empty). */
 size_t fa_bwd_workspace_bytes(int B, int H, int N, int d);
 
