@@ -22,21 +22,16 @@
 //                  dK  += dS^T Q_i          (dS^T read from shared memory)
 //                  dQ_i = dS K_j            (same shared bytes, MN-major)
 //                dQ_i is added into the fp32 accumulator in global memory.
+//                Two variants: fa_bwd_main_d64 (pipelined across query
+//                blocks, dQ added by bulk reductions) and fa_bwd_main_d128
+//                (tensor memory too small to pipeline; see each kernel).
 //   fa_bwd_post  dQ = bf16(accumulator)
 //
-// CTA of fa_bwd_main (512 threads):
-//   warps 0-7  two P/dS warpgroups: thread = key row = TMEM lane; warpgroup
-//              w handles query columns [64w, 64w+64) of each step, and the
-//              S^T / dP^T MMAs run one query half at a time, so the first
-//              half's P/dS work overlaps the second half's MMAs
-//   warps 8-11 dQ warpgroup: reads dQ_i (thread = query row) and adds it
-//              into global memory; writes dK, dV at the end (thread = key)
-//   warp  12   tcgen05 MMA issue and TMEM allocation
-//   warp  13   TMA producer; warps 14-15 idle
-//
-// TMEM columns: S^T/P^T [0,128), dP^T [128,256); for d = 64 dQ [256,320),
-// dK [320,384), dV [384,448); for d = 128 dQ reuses the dP^T columns (the
-// next dP^T waits until dQ has been read), dK [256,384), dV [384,512).
+// The dQ accumulator is fp32 [BH, Npad, d] in a blocked layout: each group
+// of 32 rows is stored as d/32 blocks of 32 rows x 32 columns (4 KiB,
+// contiguous), and inside a block the eight 16-byte chunks of a row are
+// rotated by XOR with (row mod 8). A block is then one contiguous bulk
+// reduction from a bank-conflict-free shared staging tile.
 
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -49,56 +44,12 @@ namespace fa {
 namespace {
 
 constexpr int kBlk = 128;  // keys per CTA block and queries per step
-constexpr int kHalf = 64;  // query columns per P/dS warpgroup
-constexpr int kThreads = 512;
-constexpr int kDqWarp0 = 8;
-constexpr int kMmaWarp = 12;
-constexpr int kLoadWarp = 13;
 constexpr float kLog2e = 1.4426950408889634f;
-
-template <int D>
-struct BwdCfg {
-  static constexpr int kChunks = D / 64;
-  static constexpr int kChunkBytes = kBlk * 64 * 2;
-  static constexpr int kTileBytes = kChunks * kChunkBytes;
-  static constexpr int kVecBytes = 2 * kBlk * 4;  // lse2[128], D[128] of one query block
-  static constexpr int kStages = (D == 64) ? 3 : 2;
-  static constexpr bool kDqAliasDp = (D == 128);
-  static constexpr int kKOff = 0;
-  static constexpr int kVOff = kKOff + kTileBytes;
-  static constexpr int kDSOff = kVOff + kTileBytes;             // 2 x 16 KiB
-  static constexpr int kStageOff = kDSOff + 2 * kChunkBytes;
-  static constexpr int kStageBytes = 2 * kTileBytes + kVecBytes;  // Q, dO, vectors
-  static constexpr int kBarOff = kStageOff + kStages * kStageBytes;
-  static constexpr int kBarKV = 0;
-  static constexpr int kBarQFull = 1;
-  static constexpr int kBarQEmpty = kBarQFull + kStages;
-  static constexpr int kBarSFull = kBarQEmpty + kStages;    // one per query half
-  static constexpr int kBarDSFull = kBarSFull + 2;           // one per query half
-  static constexpr int kBarDQFull = kBarDSFull + 2;
-  static constexpr int kBarDQEmpty = kBarDQFull + 1;
-  static constexpr int kBarDKDV = kBarDQEmpty + 1;
-  static constexpr int kBarDrain = kBarDKDV + 1;
-  static constexpr int kNumBars = kBarDrain + 1;
-  static constexpr int kMiscOff = kBarOff + kNumBars * 8;
-  static constexpr int kLayoutBytes = kMiscOff + 16;
-  // Slack for aligning the base to 1024 bytes, within the 227 KiB limit.
-  static constexpr int kSmemLimit = 232448;
-  static constexpr int kSmemBytes =
-      kLayoutBytes + 1024 <= kSmemLimit ? kLayoutBytes + 1024 : kSmemLimit;
-  static_assert(kLayoutBytes <= kSmemLimit, "backward tiles exceed shared memory");
-  static constexpr uint32_t kTmemCols = 512;
-  static constexpr uint32_t kColS = 0;
-  static constexpr uint32_t kColDP = 128;
-  static constexpr uint32_t kColDQ = kDqAliasDp ? 128 : 256;
-  static constexpr uint32_t kColDK = kDqAliasDp ? 256 : 320;
-  static constexpr uint32_t kColDV = kColDK + D;
-};
 
 struct BwdArgs {
   const float* lse2;   // [BH, Npad] -LSE * log2(e), -inf past N
   const float* Dvec;   // [BH, Npad] -rowsum(dO * O), 0 past N
-  float* dq_acc;
+  float* dq_acc;       // [BH, Npad, d] blocked layout (acc_index)
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
   int* status;
@@ -110,6 +61,14 @@ struct BwdArgs {
   float scale;
   float scale_log2;
 };
+
+// Index (in floats) of dQ accumulator element (bh, row n, column c); c is
+// a multiple of 4 when the caller accesses 16 bytes.
+template <int D>
+__host__ __device__ __forceinline__ size_t acc_index(long long bh, int n, int c, int n_pad) {
+  return (static_cast<size_t>(bh) * n_pad + (n & ~31)) * D + static_cast<size_t>(c >> 5) * 1024 +
+         (n & 31) * 32 + (((((c & 31) >> 2) ^ (n & 7))) << 2) + (c & 3);
+}
 
 // ---------------------------------------------------------------- B0
 // For every row of the padded [BH, Npad] grid: -D = -sum_c dO[c] * O[c] and
@@ -161,20 +120,91 @@ __global__ void __launch_bounds__(256) fa_bwd_pre(const __nv_bfloat16* __restric
 }
 
 // ---------------------------------------------------------------- B2
-__global__ void __launch_bounds__(256) fa_bwd_post(const float4* __restrict__ acc,
-                                                   uint2* __restrict__ dq, long long n_vec4) {
+// dQ = bf16(accumulator), reading the blocked accumulator layout and
+// writing [BH, N, d] row-major; one thread per 4 columns of a row.
+template <int D>
+__global__ void __launch_bounds__(256) fa_bwd_post(const float* __restrict__ acc,
+                                                   uint2* __restrict__ dq, int N, int n_pad,
+                                                   long long n_vec4) {
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
   for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n_vec4;
        i += stride) {
-    const float4 a = acc[i];
+    const long long e = i * 4;
+    const int c = static_cast<int>(e % D);
+    const long long row = e / D;
+    const long long bh = row / N;
+    const int n = static_cast<int>(row - bh * N);
+    const float4 a = *reinterpret_cast<const float4*>(acc + acc_index<D>(bh, n, c, n_pad));
     dq[i] = make_uint2(pack_bf16(a.x, a.y), pack_bf16(a.z, a.w));
   }
 }
+// ---------------------------------------------------------------- B1, d = 128
+// With d = 128 the five accumulators (S^T, dP^T, dQ, dK, dV) need 640
+// tensor-memory columns of the 512, so dQ shares the dP^T columns and each
+// query step runs in sequence: S^T / dP^T (one query half at a time), P/dS,
+// dV / dK, then dQ, whose read-out must finish before the next dP^T.
+//
+// CTA (512 threads):
+//   warps 0-7  two P/dS warpgroups: thread = key row = TMEM lane; warpgroup
+//              w handles query columns [64w, 64w+64) of each step, and the
+//              S^T / dP^T MMAs run one query half at a time, so the first
+//              half's P/dS work overlaps the second half's MMAs
+//   warps 8-11 dQ warpgroup: reads dQ_i (thread = query row) and adds it
+//              into global memory; writes dK, dV at the end (thread = key)
+//   warp  12   tcgen05 MMA issue and TMEM allocation
+//   warp  13   TMA producer; warps 14-15 idle
+// TMEM columns: S^T/P^T [0,128), dP^T and dQ [128,256), dK [256,384),
+// dV [384,512).
+namespace wide {
 
-// ---------------------------------------------------------------- B1
+constexpr int kHalf = 64;  // query columns per P/dS warpgroup
+constexpr int kThreads = 512;
+constexpr int kDqWarp0 = 8;
+constexpr int kMmaWarp = 12;
+constexpr int kLoadWarp = 13;
+
+template <int D>
+struct BwdCfg {
+  static constexpr int kChunks = D / 64;
+  static constexpr int kChunkBytes = kBlk * 64 * 2;
+  static constexpr int kTileBytes = kChunks * kChunkBytes;
+  static constexpr int kVecBytes = 2 * kBlk * 4;  // lse2[128], D[128] of one query block
+  static constexpr int kStages = (D == 64) ? 3 : 2;
+  static constexpr bool kDqAliasDp = (D == 128);
+  static constexpr int kKOff = 0;
+  static constexpr int kVOff = kKOff + kTileBytes;
+  static constexpr int kDSOff = kVOff + kTileBytes;             // 2 x 16 KiB
+  static constexpr int kStageOff = kDSOff + 2 * kChunkBytes;
+  static constexpr int kStageBytes = 2 * kTileBytes + kVecBytes;  // Q, dO, vectors
+  static constexpr int kBarOff = kStageOff + kStages * kStageBytes;
+  static constexpr int kBarKV = 0;
+  static constexpr int kBarQFull = 1;
+  static constexpr int kBarQEmpty = kBarQFull + kStages;
+  static constexpr int kBarSFull = kBarQEmpty + kStages;    // one per query half
+  static constexpr int kBarDSFull = kBarSFull + 2;           // one per query half
+  static constexpr int kBarDQFull = kBarDSFull + 2;
+  static constexpr int kBarDQEmpty = kBarDQFull + 1;
+  static constexpr int kBarDKDV = kBarDQEmpty + 1;
+  static constexpr int kBarDrain = kBarDKDV + 1;
+  static constexpr int kNumBars = kBarDrain + 1;
+  static constexpr int kMiscOff = kBarOff + kNumBars * 8;
+  static constexpr int kLayoutBytes = kMiscOff + 16;
+  // Slack for aligning the base to 1024 bytes, within the 227 KiB limit.
+  static constexpr int kSmemLimit = 232448;
+  static constexpr int kSmemBytes =
+      kLayoutBytes + 1024 <= kSmemLimit ? kLayoutBytes + 1024 : kSmemLimit;
+  static_assert(kLayoutBytes <= kSmemLimit, "backward tiles exceed shared memory");
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr uint32_t kColS = 0;
+  static constexpr uint32_t kColDP = 128;
+  static constexpr uint32_t kColDQ = kDqAliasDp ? 128 : 256;
+  static constexpr uint32_t kColDK = kDqAliasDp ? 256 : 320;
+  static constexpr uint32_t kColDV = kColDK + D;
+};
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
-    fa_bwd_main(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+    fa_bwd_main_d128(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                 const BwdArgs args) {
   using C = BwdCfg<D>;
@@ -416,7 +446,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       tc_fence_after();
       const int q = (i0 + it) * kBlk + r;
-      float* dst = args.dq_acc + (static_cast<size_t>(bh) * N + q) * D;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t g[32];
@@ -425,7 +454,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (q < N) {
 #pragma unroll
           for (int e = 0; e < 32; e += 4)
-            red_add_v4(dst + c * 32 + e, __uint_as_float(g[e]) * scale,
+            red_add_v4(args.dq_acc + acc_index<D>(bh, q, c * 32 + e, args.n_pad),
+                       __uint_as_float(g[e]) * scale,
                        __uint_as_float(g[e + 1]) * scale, __uint_as_float(g[e + 2]) * scale,
                        __uint_as_float(g[e + 3]) * scale);
         }
@@ -476,9 +506,424 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0 && *abort_flag) atomicExch(args.status, kStatusTimeout);
 }
 
+}  // namespace wide
+
+// ---------------------------------------------------------------- B1, d = 64
+// Pipelined across query blocks. The P/dS warpgroups copy S^T_i and dP^T_i
+// from tensor memory into registers and release them at once, so the tensor
+// core computes S^T_{i+1} and dP^T_{i+1} while P_i and dS_i are formed; P^T
+// has tensor-memory columns of its own and dS two shared-memory buffers.
+// Per query block the MMA warp issues, in this order:
+//   S^T_{i+1}, dP^T_{i+1}        (once the warpgroups hold S^T_i, dP^T_i)
+//   dV += P^T_i dO_i, dK += dS^T_i Q_i   (once P_i and dS_i are written)
+//   dQ_i = dS_i K                (once dQ_{i-1} has been read out)
+// dQ_i is added to the fp32 accumulator by the dQ warpgroup through
+// per-warp 4 KiB shared staging tiles and bulk reductions (full 128-byte
+// lines, no per-thread atomics).
+//
+// CTA (512 threads):
+//   warps 0-7  two P/dS warpgroups: thread = key row = TMEM lane; warpgroup
+//              w handles query columns [64w, 64w+64) of every step
+//   warps 8-11 dQ warpgroup: thread = query row of dQ_i; at the end writes
+//              dK and dV (thread = key row)
+//   warp  12   tcgen05 MMA issue and TMEM allocation
+//   warp  13   TMA producer; warps 14-15 idle
+// TMEM columns: S^T [0,128), dP^T [128,256), P^T (bf16 pairs) [256,320),
+// dQ [320,384), dK [384,448), dV [448,512).
+namespace pipe {
+
+constexpr int kD = 64;
+constexpr int kThreads = 512;
+constexpr int kPdsThreads = 256;
+constexpr int kDqWarp0 = 8;
+constexpr int kMmaWarp = 12;
+constexpr int kLoadWarp = 13;
+// Register budgets after the split (launch: 128 per thread x 512 threads).
+constexpr uint32_t kRegsPds = 192;
+constexpr uint32_t kRegsOther = 64;
+static_assert(kRegsPds * kPdsThreads + kRegsOther * (kThreads - kPdsThreads) <= 128 * kThreads,
+              "register split exceeds the launch allocation");
+
+constexpr int kTileBytes = kBlk * kD * 2;           // 16 KiB, one 128B-swizzled chunk
+constexpr int kVecBytes = 2 * kBlk * 4;             // -lse2[128], -D[128] of a query block
+constexpr int kStages = 3;
+constexpr int kKOff = 0;
+constexpr int kVOff = kKOff + kTileBytes;
+constexpr int kDSOff = kVOff + kTileBytes;          // 2 buffers x (2 query halves x 16 KiB)
+constexpr int kDSBytes = 2 * kTileBytes;
+constexpr int kStageOff = kDSOff + 2 * kDSBytes;
+constexpr int kStageBytes = 2 * kTileBytes + kVecBytes;  // Q, dO, vectors
+constexpr int kDqStageOff = kStageOff + kStages * kStageBytes;
+constexpr int kDqStageBytes = 32 * 32 * 4;          // one 32 x 32 fp32 block per dQ warp
+constexpr int kBarOff = kDqStageOff + 4 * kDqStageBytes;
+enum : int {
+  kBarKV = 0,
+  kBarQFull = 1,
+  kBarQEmpty = kBarQFull + kStages,
+  kBarSFull = kBarQEmpty + kStages,
+  kBarSFree,
+  kBarPFree,
+  kBarDSFull,
+  kBarDSFree,  // two, one per dS buffer
+  kBarDQFull = kBarDSFree + 2,
+  kBarDQEmpty,
+  kBarDKDV,
+  kBarDrain,
+  kNumBars
+};
+constexpr int kMiscOff = kBarOff + kNumBars * 8;
+constexpr int kLayoutBytes = kMiscOff + 16;
+constexpr int kSmemBytes = kLayoutBytes + 1024;  // + slack to align the base to 1024
+static_assert(kSmemBytes <= 232448, "backward tiles exceed shared memory");
+static_assert(kStageBytes % 1024 == 0 && kDqStageOff % 1024 == 0, "swizzle atoms need 1 KiB alignment");
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColS = 0, kColDP = 128, kColP = 256, kColDQ = 320, kColDK = 384, kColDV = 448;
+
+__global__ void __launch_bounds__(kThreads, 1)
+    fa_bwd_main_d64(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
+                    const BwdArgs args) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_u32 = smem_u32(smem_raw);
+  const uint32_t base = (raw_u32 + 1023u) & ~1023u;
+  uint8_t* base_ptr = smem_raw + (base - raw_u32);
+  auto bar = [&](int i) -> uint32_t { return base + kBarOff + 8u * i; };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base_ptr + kMiscOff);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(base_ptr + kMiscOff + 4);
+
+  const int bh = blockIdx.x % args.BH;
+  const int jb = static_cast<int>(blockIdx.x / args.BH);  // key block (heaviest first)
+  const int i0 = args.causal ? jb : 0;
+  const int n_steps = args.n_blocks - i0;
+  const int warp = warp_id();
+  const int lane = lane_id();
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(kBarKV), 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(bar(kBarQFull + s), 1);
+      mbar_init(bar(kBarQEmpty + s), 1);
+    }
+    mbar_init(bar(kBarSFull), 1);
+    mbar_init(bar(kBarSFree), kPdsThreads);
+    mbar_init(bar(kBarPFree), 1);
+    mbar_init(bar(kBarDSFull), kPdsThreads);
+    mbar_init(bar(kBarDSFree + 0), 1);
+    mbar_init(bar(kBarDSFree + 1), 1);
+    mbar_init(bar(kBarDQFull), 1);
+    mbar_init(bar(kBarDQEmpty), 128);
+    mbar_init(bar(kBarDKDV), 1);
+    mbar_init(bar(kBarDrain), 1);
+    *abort_flag = 0;
+    mbar_fence_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  if (warp >= kDqWarp0) regs_decrease<kRegsOther>();
+
+  if (warp == kLoadWarp) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_map(&tmQ);
+      tma_prefetch_map(&tmK);
+      tma_prefetch_map(&tmV);
+      tma_prefetch_map(&tmDO);
+      mbar_arrive_expect_tx(bar(kBarKV), 2 * kTileBytes);
+      tma_load_3d(base + kKOff, &tmK, bar(kBarKV), 0, jb * kBlk, bh);
+      tma_load_3d(base + kVOff, &tmV, bar(kBarKV), 0, jb * kBlk, bh);
+      int issued = 0;
+      bool ok = true;
+      for (int it = 0; it < n_steps; ++it) {
+        const int s = it % kStages;
+        if (it >= kStages)
+          ok = mbar_wait(bar(kBarQEmpty + s), ((it / kStages) + 1) & 1, abort_flag);
+        if (!ok) break;
+        const int row0 = (i0 + it) * kBlk;
+        const uint32_t st = base + kStageOff + s * kStageBytes;
+        const uint32_t fb = bar(kBarQFull + s);
+        mbar_arrive_expect_tx(fb, kStageBytes);
+        tma_load_3d(st, &tmQ, fb, 0, row0, bh);
+        tma_load_3d(st + kTileBytes, &tmDO, fb, 0, row0, bh);
+        const size_t voff = static_cast<size_t>(bh) * args.n_pad + row0;
+        bulk_load(st + 2 * kTileBytes, args.lse2 + voff, kBlk * 4, fb);
+        bulk_load(st + 2 * kTileBytes + kBlk * 4, args.Dvec + voff, kBlk * 4, fb);
+        issued = it + 1;
+      }
+      if (*abort_flag) {
+        mbar_wait(bar(kBarKV), 0, nullptr);
+        for (int it = issued - 1; it >= 0 && it >= issued - kStages; --it)
+          mbar_wait(bar(kBarQFull + it % kStages), (it / kStages) & 1, nullptr);
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------ MMA issue
+    if (lane == 0) {
+      constexpr uint32_t kIdS = idesc_bf16_f32(kBlk, kBlk, false, false);  // S^T, dP^T
+      constexpr uint32_t kIdKV = idesc_bf16_f32(kBlk, kD, false, true);     // dV, dK
+      constexpr uint32_t kIdQ = idesc_bf16_f32(kBlk, kD, true, true);       // dQ
+      // Shared-memory descriptors, built once. Advancing an operand by b
+      // bytes adds b / 16 to the descriptor's start-address field, which
+      // cannot carry out of its 14 bits below 256 KiB.
+      const uint64_t kK = sdesc_sw128(base + kKOff, 16, 1024);          // K, K-major
+      const uint64_t kV = sdesc_sw128(base + kVOff, 16, 1024);          // V, K-major
+      const uint64_t kKmn = sdesc_sw128(base + kKOff, kTileBytes, 1024);  // K as MN-major B
+      const uint64_t kQ0 = sdesc_sw128(base + kStageOff, 16, 1024);     // stage 0 Q, K-major
+      const uint64_t kQmn0 = sdesc_sw128(base + kStageOff, kTileBytes, 1024);
+      const uint64_t kDS0 = sdesc_sw128(base + kDSOff, 16, 1024);       // dS buffer 0, K-major
+      const uint64_t kDSmn0 = sdesc_sw128(base + kDSOff, kTileBytes, 1024);
+      constexpr uint64_t kStageStep = kStageBytes >> 4, kTileStep = kTileBytes >> 4;
+      constexpr uint64_t kDSStep = kDSBytes >> 4;
+      // S^T = K Q^T and dP^T = V dO^T of query block `it` (both K-major)
+      auto issue_sdp = [&](int it) {
+        const uint64_t q = kQ0 + (it % kStages) * kStageStep, o = q + kTileStep;
+#pragma unroll
+        for (int kk = 0; kk < kD / 16; ++kk)
+          mma_ss(tmem + kColS, kK + 2 * kk, q + 2 * kk, kIdS, kk > 0 ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < kD / 16; ++kk)
+          mma_ss(tmem + kColDP, kV + 2 * kk, o + 2 * kk, kIdS, kk > 0 ? 1u : 0u);
+        mma_commit(bar(kBarSFull));
+      };
+      bool ok = mbar_wait(bar(kBarKV), 0, abort_flag);
+      if (ok) ok = mbar_wait(bar(kBarQFull), 0, abort_flag);
+      tc_fence_after();
+      if (ok) issue_sdp(0);
+      for (int it = 0; it < n_steps && ok; ++it) {
+        if (it + 1 < n_steps) {
+          ok = mbar_wait(bar(kBarSFree), it & 1, abort_flag);
+          if (ok) ok = mbar_wait(bar(kBarQFull + (it + 1) % kStages), ((it + 1) / kStages) & 1, abort_flag);
+          if (!ok) break;
+          tc_fence_after();
+          issue_sdp(it + 1);
+        }
+        ok = mbar_wait(bar(kBarDSFull), it & 1, abort_flag);
+        if (!ok) break;
+        tc_fence_after();
+        const uint64_t qmn = kQmn0 + (it % kStages) * kStageStep, omn = qmn + kTileStep;
+        const uint64_t dsk = kDS0 + (it & 1) * kDSStep, dsmn = kDSmn0 + (it & 1) * kDSStep;
+        // dV += P^T dO   (A = P^T bf16 pairs in TMEM, B = dO MN-major, 16 rows per step)
+#pragma unroll
+        for (int kk = 0; kk < kBlk / 16; ++kk)
+          mma_ts(tmem + kColDV, tmem + kColP + kk * 8, omn + 128 * kk, kIdKV, (it > 0 || kk > 0) ? 1u : 0u);
+        // dK += dS^T Q   (A = dS^T K-major, query halves in two 16 KiB regions; B = Q MN-major)
+#pragma unroll
+        for (int kk = 0; kk < kBlk / 16; ++kk)
+          mma_ss(tmem + kColDK, dsk + (kk >> 2) * kTileStep + (kk & 3) * 2, qmn + 128 * kk, kIdKV,
+                 (it > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(bar(kBarPFree));
+        if (it > 0) {
+          ok = mbar_wait(bar(kBarDQEmpty), (it - 1) & 1, abort_flag);
+          if (!ok) break;
+          tc_fence_after();
+        }
+        // dQ = dS K      (A = dS MN-major: the same bytes, B = K MN-major)
+#pragma unroll
+        for (int kk = 0; kk < kBlk / 16; ++kk)
+          mma_ss(tmem + kColDQ, dsmn + 128 * kk, kKmn + 128 * kk, kIdQ, kk > 0 ? 1u : 0u);
+        mma_commit(bar(kBarDQFull));
+        mma_commit(bar(kBarQEmpty + it % kStages));
+        mma_commit(bar(kBarDSFree + (it & 1)));
+      }
+      if (ok) mma_commit(bar(kBarDKDV));
+      mma_commit(bar(kBarDrain));
+      mbar_wait(bar(kBarDrain), 0, nullptr);
+    }
+  } else if (warp < kDqWarp0) {
+    // ------------------------------------------------------------ P and dS
+    regs_increase<kRegsPds>();
+    const int w = warp >> 2;  // query columns [64w, 64w+64) of every step
+    const int key_row = threadIdx.x & 127;
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + lane_base + kColS + 64 * w;
+    const uint32_t tDP = tmem + lane_base + kColDP + 64 * w;
+    const uint32_t tP = tmem + lane_base + kColP + 32 * w;
+    const float sl2 = args.scale_log2;
+    const float2 sl2x2 = make_float2(sl2, sl2);
+    const int key_sw = key_row & 7;
+    bool ok = true;
+    for (int it = 0; it < n_steps; ++it) {
+      const int s = it % kStages;
+      const float* nlse2_s =
+          reinterpret_cast<const float*>(base_ptr + kStageOff + s * kStageBytes + 2 * kTileBytes) + 64 * w;
+      const float* nd_s = nlse2_s + kBlk;
+      // the stage's vectors arrive with its Q/dO tiles; S^T, dP^T with the MMA commit
+      ok = mbar_wait(bar(kBarQFull + s), (it / kStages) & 1, abort_flag);
+      if (ok) ok = mbar_wait(bar(kBarSFull), it & 1, abort_flag);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t s0[32], s1[32], d0[32], d1[32];
+      tmem_ld32(tS, s0);
+      tmem_ld32(tS + 32, s1);
+      tmem_ld32(tDP, d0);
+      tmem_ld32(tDP + 32, d1);
+      tmem_ld_wait(s0);
+      tmem_ld_wait(s1);
+      tmem_ld_wait(d0);
+      tmem_ld_wait(d1);
+      // S^T and dP^T of this step are in registers: the next step's MMAs may
+      // overwrite their columns.
+      tc_fence_before();
+      mbar_arrive(bar(kBarSFree));
+
+      const bool diag = args.causal && it == 0;
+      uint32_t pp[32], dd[32];
+      auto half = [&](const uint32_t (&sr)[32], const uint32_t (&dr)[32], int c) {
+#pragma unroll
+        for (int e = 0; e < 32; e += 4) {
+          const int ql = c * 32 + e;     // query column within this warpgroup's half
+          const int qc = 64 * w + ql;    // ... within the query block
+          const float4 nl = *reinterpret_cast<const float4*>(nlse2_s + ql);
+          const float4 nd = *reinterpret_cast<const float4*>(nd_s + ql);
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const float2 nl2 = u ? make_float2(nl.z, nl.w) : make_float2(nl.x, nl.y);
+            const float2 nd2 = u ? make_float2(nd.z, nd.w) : make_float2(nd.x, nd.y);
+            const int x = e + 2 * u;
+            const float2 a = __ffma2_rn(make_float2(__uint_as_float(sr[x]), __uint_as_float(sr[x + 1])),
+                                        sl2x2, nl2);
+            float2 p = make_float2(ex2(a.x), ex2(a.y));
+            if (diag) {  // causal diagonal block: a query before the key is masked
+              if (qc + 2 * u < key_row) p.x = 0.f;
+              if (qc + 2 * u + 1 < key_row) p.y = 0.f;
+            }
+            const float2 g = __fmul2_rn(
+                p, __fadd2_rn(make_float2(__uint_as_float(dr[x]), __uint_as_float(dr[x + 1])), nd2));
+            pp[(ql >> 1) + u] = pack_bf16(p.x, p.y);
+            dd[(ql >> 1) + u] = pack_bf16(g.x, g.y);
+          }
+        }
+      };
+      half(s0, d0, 0);
+      half(s1, d1, 1);
+
+      // P^T into its own columns once the previous step's dV MMA has read them
+      if (it > 0) {
+        ok = mbar_wait(bar(kBarPFree), (it - 1) & 1, abort_flag);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc_fence_after();
+      }
+      tmem_st32(tP, pp);
+      // dS^T row of this key into dS buffer (it & 1), once step it-2's dK and
+      // dQ MMAs have read that buffer: 64 queries -> eight swizzled 16-byte chunks
+      if (it >= 2) {
+        ok = mbar_wait(bar(kBarDSFree + (it & 1)), ((it >> 1) - 1) & 1, abort_flag);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+      }
+      uint8_t* ds_row = base_ptr + kDSOff + (it & 1) * kDSBytes + w * kTileBytes + key_row * 128;
+#pragma unroll
+      for (int v = 0; v < 8; ++v)
+        *reinterpret_cast<uint4*>(ds_row + ((v ^ key_sw) * 16)) =
+            make_uint4(dd[4 * v], dd[4 * v + 1], dd[4 * v + 2], dd[4 * v + 3]);
+      tmem_st_wait();
+      tc_fence_before();
+      fence_async_smem();
+      mbar_arrive(bar(kBarDSFull));
+    }
+  } else if (warp < kMmaWarp) {
+    // ------------------------------------------------------------ dQ, dK, dV out
+    const int qw = warp - kDqWarp0;  // TMEM lanes [32 qw, 32 qw + 32)
+    const uint32_t lane_base = static_cast<uint32_t>(qw * 32) << 16;
+    const uint32_t stage = base + kDqStageOff + qw * kDqStageBytes;
+    uint8_t* stage_row = base_ptr + kDqStageOff + qw * kDqStageBytes + lane * 128;
+    const float scale = args.scale;
+    bool ok = true;
+    bool pending = false;
+    // one 32 x 32 block of dQ (this warp's rows, 32 columns) -> staging -> bulk add
+    auto put_block = [&](const uint32_t (&g)[32], float* dst) {
+      if (pending) {
+        if (lane == 0) bulk_wait_read<0>();
+        __syncwarp();
+      }
+#pragma unroll
+      for (int v = 0; v < 8; ++v)
+        *reinterpret_cast<float4*>(stage_row + ((v ^ (lane & 7)) * 16)) =
+            make_float4(__uint_as_float(g[4 * v]) * scale, __uint_as_float(g[4 * v + 1]) * scale,
+                        __uint_as_float(g[4 * v + 2]) * scale, __uint_as_float(g[4 * v + 3]) * scale);
+      fence_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        bulk_reduce_add_f32(dst, stage, kDqStageBytes);
+        bulk_commit_group();
+      }
+      pending = true;
+    };
+    for (int it = 0; it < n_steps; ++it) {
+      ok = mbar_wait(bar(kBarDQFull), it & 1, abort_flag);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      // rows [32 qw, 32 qw + 32) of query block i0 + it: two contiguous 4 KiB blocks
+      float* dst = args.dq_acc + (static_cast<size_t>(bh) * args.n_pad + (i0 + it) * kBlk + 32 * qw) * kD;
+      uint32_t g[32];
+      tmem_ld32(tmem + lane_base + kColDQ, g);
+      tmem_ld_wait(g);
+      put_block(g, dst);
+      tmem_ld32(tmem + lane_base + kColDQ + 32, g);
+      tmem_ld_wait(g);
+      tc_fence_before();
+      mbar_arrive(bar(kBarDQEmpty));
+      put_block(g, dst + 1024);
+    }
+    if (lane == 0) bulk_wait<0>();
+    __syncwarp();
+    if (ok) {
+      ok = mbar_wait(bar(kBarDKDV), 0, abort_flag);
+      ok = __all_sync(0xffffffffu, ok);
+    }
+    if (ok) {
+      tc_fence_after();
+      const int key = jb * kBlk + qw * 32 + lane;
+      const bool live = key < args.N;
+      const size_t off = (static_cast<size_t>(bh) * args.N + key) * kD;
+#pragma unroll
+      for (int which = 0; which < 2; ++which) {
+        const uint32_t col = which == 0 ? kColDK : kColDV;
+        const float mul = which == 0 ? scale : 1.f;
+        __nv_bfloat16* out = (which == 0 ? args.dk : args.dv) + off;
+#pragma unroll
+        for (int c = 0; c < kD / 32; ++c) {
+          uint32_t g[32];
+          tmem_ld32(tmem + lane_base + col + c * 32, g);
+          tmem_ld_wait(g);
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            pk[e] = pack_bf16(__uint_as_float(g[2 * e]) * mul, __uint_as_float(g[2 * e + 1]) * mul);
+          if (live) {
+            uint4* o4 = reinterpret_cast<uint4*>(out + c * 32);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) o4[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+  if (threadIdx.x == 0 && *abort_flag) atomicExch(args.status, kStatusTimeout);
+}
+
+}  // namespace pipe
+
 // Workspace sections: D and lse2 (fp32 [BH, Npad] each), then the fp32 dQ
-// accumulator [BH, N, d]. Npad * 4 bytes is a multiple of 512, so every
-// section and every query block's vector slice is 512-byte aligned.
+// accumulator [BH, Npad, d] (blocked, acc_index). Npad * 4 bytes is a
+// multiple of 512, so every section and every query block's vector slice is
+// 512-byte aligned.
 struct Workspace {
   float* Dvec;
   float* lse2;
@@ -501,7 +946,7 @@ template <int D>
 int launch_pre_d(const Problem& p, const void* o, const float* lse, const void* dO,
                  void* workspace, cudaStream_t stream) {
   const Workspace w = carve(p, workspace);
-  const long long acc_vec4 = static_cast<long long>(p.B) * p.H * p.N * D / 4;
+  const long long acc_vec4 = w.pad_rows * D / 4;
   const long long work = w.pad_rows * (D / 8) > acc_vec4 ? w.pad_rows * (D / 8) : acc_vec4;
   long long blocks = (work + 255) / 256;
   if (blocks > 65536) blocks = 65536;
@@ -511,21 +956,7 @@ int launch_pre_d(const Problem& p, const void* o, const float* lse, const void* 
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
-template <int D>
-int launch_main_d(const Problem& p, const void* dO, void* dk, void* dv, void* workspace,
-                  cudaStream_t stream) {
-  using C = BwdCfg<D>;
-  const Workspace w = carve(p, workspace);
-  const int BH = p.B * p.H;
-  int* status = device_status_word();
-  if (!status) return FA_ERR_LAUNCH;
-  CUtensorMap mq, mk, mv, mdo;
-  if (!make_map_bhnd(&mq, p.q, BH, p.N, D) || !make_map_bhnd(&mk, p.k, BH, p.N, D) ||
-      !make_map_bhnd(&mv, p.v, BH, p.N, D) || !make_map_bhnd(&mdo, dO, BH, p.N, D))
-    return FA_ERR_LAUNCH;
-  auto kern = fa_bwd_main<D>;
-  if (!ensure_smem_attr(reinterpret_cast<const void*>(kern), C::kSmemBytes, D == 64 ? 2 : 3))
-    return FA_ERR_LAUNCH;
+BwdArgs make_args(const Problem& p, const Workspace& w, void* dk, void* dv, int* status) {
   BwdArgs a;
   a.lse2 = w.lse2;
   a.Dvec = w.Dvec;
@@ -535,14 +966,39 @@ int launch_main_d(const Problem& p, const void* dO, void* dk, void* dv, void* wo
   a.status = status;
   a.N = p.N;
   a.n_pad = w.n_pad;
-  a.BH = BH;
+  a.BH = p.B * p.H;
   a.causal = p.causal ? 1 : 0;
   a.n_blocks = w.n_pad / kBlk;
   a.scale = p.scale;
   a.scale_log2 = p.scale * kLog2e;
+  return a;
+}
+
+int launch_main_any(const Problem& p, const void* dO, void* dk, void* dv, void* workspace,
+                    cudaStream_t stream) {
+  const Workspace w = carve(p, workspace);
+  const int BH = p.B * p.H;
+  int* status = device_status_word();
+  if (!status) return FA_ERR_LAUNCH;
+  CUtensorMap mq, mk, mv, mdo;
+  if (!make_map_bhnd(&mq, p.q, BH, p.N, p.d) || !make_map_bhnd(&mk, p.k, BH, p.N, p.d) ||
+      !make_map_bhnd(&mv, p.v, BH, p.N, p.d) || !make_map_bhnd(&mdo, dO, BH, p.N, p.d))
+    return FA_ERR_LAUNCH;
+  const BwdArgs a = make_args(p, w, dk, dv, status);
   const long long grid = static_cast<long long>(a.n_blocks) * BH;
   if (grid > 0x7fffffffLL) return FA_ERR_INVALID;
-  kern<<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, mdo, a);
+  if (p.d == 64) {
+    auto kern = pipe::fa_bwd_main_d64;
+    if (!ensure_smem_attr(reinterpret_cast<const void*>(kern), pipe::kSmemBytes, 2))
+      return FA_ERR_LAUNCH;
+    kern<<<static_cast<unsigned>(grid), pipe::kThreads, pipe::kSmemBytes, stream>>>(mq, mk, mv, mdo, a);
+  } else {
+    using C = wide::BwdCfg<128>;
+    auto kern = wide::fa_bwd_main_d128<128>;
+    if (!ensure_smem_attr(reinterpret_cast<const void*>(kern), C::kSmemBytes, 3))
+      return FA_ERR_LAUNCH;
+    kern<<<static_cast<unsigned>(grid), wide::kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, mdo, a);
+  }
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
@@ -550,7 +1006,7 @@ int launch_main_d(const Problem& p, const void* dO, void* dk, void* dv, void* wo
 
 size_t bwd_workspace_bytes(long long B, long long H, long long N, long long d) {
   const long long n_pad = (N + kBlk - 1) / kBlk * kBlk;
-  return static_cast<size_t>(2 * B * H * n_pad) * 4 + static_cast<size_t>(B * H * N * d) * 4;
+  return static_cast<size_t>(2 * B * H * n_pad) * 4 + static_cast<size_t>(B * H * n_pad * d) * 4;
 }
 
 int launch_bwd_pre(const Problem& p, const void* o, const float* lse, const void* dO,
@@ -562,18 +1018,21 @@ int launch_bwd_pre(const Problem& p, const void* o, const float* lse, const void
 
 int launch_bwd_main(const Problem& p, const void* dO, void* dk, void* dv, void* workspace,
                     cudaStream_t stream) {
-  if (p.d == 64) return launch_main_d<64>(p, dO, dk, dv, workspace, stream);
-  if (p.d == 128) return launch_main_d<128>(p, dO, dk, dv, workspace, stream);
-  return FA_ERR_UNSUPPORTED;
+  if (p.d != 64 && p.d != 128) return FA_ERR_UNSUPPORTED;
+  return launch_main_any(p, dO, dk, dv, workspace, stream);
 }
 
 int launch_bwd_post(const Problem& p, void* dq, const void* workspace, cudaStream_t stream) {
   const Workspace w = carve(p, const_cast<void*>(workspace));
-  const long long acc_vec4 = static_cast<long long>(p.B) * p.H * p.N * p.d / 4;
-  long long blocks = (acc_vec4 + 255) / 256;
+  const long long n_vec4 = static_cast<long long>(p.B) * p.H * p.N * p.d / 4;
+  long long blocks = (n_vec4 + 255) / 256;
   if (blocks > 65536) blocks = 65536;
-  fa_bwd_post<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-      reinterpret_cast<const float4*>(w.acc), static_cast<uint2*>(dq), acc_vec4);
+  if (p.d == 64)
+    fa_bwd_post<64><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(w.acc, static_cast<uint2*>(dq), p.N, w.n_pad, n_vec4);
+  else if (p.d == 128)
+    fa_bwd_post<128><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(w.acc, static_cast<uint2*>(dq), p.N, w.n_pad, n_vec4);
+  else
+    return FA_ERR_UNSUPPORTED;
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 

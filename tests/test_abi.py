@@ -50,10 +50,10 @@ def test_workspace_bytes(lib):
     assert lib.fa_bwd_workspace_bytes(0, 1, 1, 64) == 0
     assert lib.fa_bwd_workspace_bytes(-1, 1, 1, 64) == 0
     # D and the log2-domain LSE, each fp32 over N rounded up to 128, then the
-    # fp32 dQ accumulator
+    # fp32 dQ accumulator over the same padded rows
     B, H, N, d = 2, 3, 100, 64
     n_pad = 128
-    assert lib.fa_bwd_workspace_bytes(B, H, N, d) == 2 * B * H * n_pad * 4 + B * H * N * d * 4
+    assert lib.fa_bwd_workspace_bytes(B, H, N, d) == 2 * B * H * n_pad * 4 + B * H * n_pad * d * 4
     assert lib.fa_bwd_workspace_bytes(1, 1, 256, 128) == 2 * 256 * 4 + 256 * 128 * 4
 
 
