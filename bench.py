@@ -220,13 +220,24 @@ class Runner:
         self.flush_buf.zero_()
 
 
-def timed_loop(runner, steps, warmup, barrier, stream):
+def timed_loop(runner, steps, warmup, barrier, stream, soak_s=0.0):
+    """W warm-up steps, an optional untimed soak of about `soak_s` seconds of
+    the same step (so that clocks sampled around the timed region reflect
+    sustained load), then `steps` steps timed with CUDA events."""
     torch = runner.torch
     with torch.cuda.stream(stream):
         for _ in range(warmup):
             runner.flush_l2()
             runner.step(stream)
     torch.cuda.synchronize()
+    if soak_s > 0:
+        t_end = time.perf_counter() + soak_s
+        with torch.cuda.stream(stream):
+            while time.perf_counter() < t_end:
+                for _ in range(50):
+                    runner.flush_l2()
+                    runner.step(stream)
+                torch.cuda.synchronize()
     mk = lambda: torch.cuda.Event(enable_timing=True)
     evs = [{"step": (mk(), mk()), "fwd": (mk(), mk()), "bwd_main": (mk(), mk())}
            for _ in range(steps)]
@@ -358,8 +369,10 @@ def run_ours(args):
                                      getattr(props, "pci_device_id", 0))
     sampler = ClockSampler(bus)
     sampler.start()
-    times, wall = timed_loop(runner, args.steps, max(args.warmup, 3), barrier, stream)
+    times, wall = timed_loop(runner, args.steps, max(args.warmup, 3), barrier, stream, soak_s=1.0)
     clocks = sampler.stop()
+    if clocks is not None:
+        clocks["window"] = "nvidia-smi every 200 ms over warm-up, a 1 s untimed soak and the timed steps"
     ms = sum(times["step"]) / len(times["step"])
     ms_fwd = sum(times["fwd"]) / len(times["fwd"])
     ms_bwd = sum(times["bwd_main"]) / len(times["bwd_main"]) if w.backward else 0.0

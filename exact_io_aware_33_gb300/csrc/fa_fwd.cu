@@ -13,8 +13,9 @@
 //   warps 4-7  softmax warpgroup of query tile 1
 //   warp  8    tcgen05 MMA issue (one thread) and TMEM allocation
 //   warp  9    TMA producer (one thread); warps 10-11 idle
-// The softmax warpgroups take 216 registers per thread, the third
-// warpgroup gives its registers back down to 56.
+// Every warp keeps the launch allocation (168 registers): lowering the MMA
+// warp's budget slows its issue loop, and the tensor core's issue queue is
+// only a few instructions deep, so that shows directly in the step time.
 // Each CTA owns 256 query rows of one (batch, head): two 128-row tiles that
 // ping-pong, so the tensor core works on one tile's QK^T / PV while the
 // other tile's softmax runs.
@@ -53,11 +54,6 @@ constexpr int kSoftmaxThreads = 128 * kQTiles;
 constexpr int kMmaWarp = kSoftmaxThreads / 32;
 constexpr int kLoadWarp = kMmaWarp + 1;
 constexpr int kThreads = kSoftmaxThreads + 128;  // + one warpgroup: MMA, TMA, two idle warps
-// Register budgets after the split (launch: 168 per thread x 384 threads).
-constexpr uint32_t kRegsSoftmax = 216;
-constexpr uint32_t kRegsOther = 56;
-static_assert(kRegsSoftmax * kSoftmaxThreads + kRegsOther * 128 <= 168 * kThreads,
-              "register split exceeds the launch allocation");
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr float kLn2 = 0.6931471805599453f;
 
@@ -153,7 +149,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  if (warp >= kMmaWarp) regs_decrease<kRegsOther>();
 
   if (warp == kLoadWarp) {
     // ------------------------------------------------------------ producer
@@ -276,7 +271,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp < kMmaWarp) {
     // ------------------------------------------------------------ softmax
-    regs_increase<kRegsSoftmax>();
     const int t = warp / 4;
     const int tile_row0 = pair * (kBlockM * kQTiles) + t * kBlockM;
     const int n_mine = tile_row0 >= N ? 0 : (args.causal ? tile_row0 / kBlockN + 1 : n_kv);
