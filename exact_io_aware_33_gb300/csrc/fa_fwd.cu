@@ -8,11 +8,11 @@
 // old sums by alpha = exp(m_old - m_new) when the maximum moves, and divides
 // once at the end. Scores S and probabilities P exist only in tensor memory.
 //
-// CTA organisation (384 threads, one CTA per SM):
+// CTA organisation (320 threads, one CTA per SM):
 //   warps 0-3  softmax warpgroup of query tile 0 (thread = row = TMEM lane)
 //   warps 4-7  softmax warpgroup of query tile 1
 //   warp  8    tcgen05 MMA issue (one thread) and TMEM allocation
-//   warp  9    TMA producer (one thread); warps 10-11 idle
+//   warp  9    TMA producer (one thread)
 // Every warp keeps the launch allocation (168 registers): lowering the MMA
 // warp's budget slows its issue loop, and the tensor core's issue queue is
 // only a few instructions deep, so that shows directly in the step time.
@@ -53,7 +53,7 @@ constexpr int kQTiles = 2;
 constexpr int kSoftmaxThreads = 128 * kQTiles;
 constexpr int kMmaWarp = kSoftmaxThreads / 32;
 constexpr int kLoadWarp = kMmaWarp + 1;
-constexpr int kThreads = kSoftmaxThreads + 128;  // + one warpgroup: MMA, TMA, two idle warps
+constexpr int kThreads = kSoftmaxThreads + 64;   // + the MMA warp and the TMA warp
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr float kLn2 = 0.6931471805599453f;
 
@@ -76,12 +76,20 @@ struct FwdCfg {
   static constexpr int kBarSFull = kBarVEmpty + kStages;
   static constexpr int kBarPFull = kBarSFull + kQTiles;
   static constexpr int kBarOFinal = kBarPFull + kQTiles;
-  static constexpr int kBarDrain = kBarOFinal + kQTiles;
+  static constexpr int kBarSFree = kBarOFinal + kQTiles;   // separate-P layout only
+  static constexpr int kBarPVDone = kBarSFree + kQTiles;   // separate-P layout only
+  static constexpr int kBarDrain = kBarPVDone + kQTiles;
   static constexpr int kNumBars = kBarDrain + 1;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kSmemBytes = kMiscOff + 16 + 1024;  // + slack to align the base
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColO = 256;
+  // With d = 64 the two S tiles and two O accumulators take 384 columns, so
+  // each tile's P gets 64 columns of its own at kColP: the softmax releases
+  // S as soon as it has loaded it and the next tile's QK^T overlaps the
+  // exponentials. With d = 128 the columns are full and P overwrites S.
+  static constexpr bool kSepP = (D == 64);
+  static constexpr uint32_t kColP = 384;
 };
 
 struct FwdArgs {
@@ -136,6 +144,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(C::kBarSFull + t), 1);
       mbar_init(bar(C::kBarPFull + t), 128);
       mbar_init(bar(C::kBarOFinal + t), 1);
+      mbar_init(bar(C::kBarSFree + t), 128);
+      mbar_init(bar(C::kBarPVDone + t), 1);
     }
     mbar_init(bar(C::kBarDrain), 1);
     *abort_flag = 0;
@@ -243,6 +253,43 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (n_t[t] > 0) issue_s(t, 0);
         mma_commit(bar(C::kBarKEmpty + 0));
       }
+      if constexpr (C::kSepP) {
+        // Per key tile j: QK^T of tile j+1 for each query tile as soon as its
+        // softmax holds S(j) in registers, then P.V of tile j once P(j) is
+        // written.
+        for (int j = 0; j < n_max && ok; ++j) {
+#pragma unroll
+          for (int t = 0; t < kQTiles; ++t) {
+            if (!ok || j + 1 >= n_t[t]) continue;
+            ok = mbar_wait(bar(C::kBarSFree + t), j & 1, abort_flag);
+            if (!ok) break;
+            ensure_k(j + 1);
+            if (!ok) break;
+            tc_fence_after();
+            issue_s(t, j + 1);
+          }
+          if (!ok) break;
+          if (j + 1 < n_max) mma_commit(bar(C::kBarKEmpty + (j + 1) % C::kStages));
+          ok = mbar_wait(bar(C::kBarVFull + j % C::kStages), (j / C::kStages) & 1, abort_flag);
+          tc_fence_after();
+#pragma unroll
+          for (int t = 0; t < kQTiles; ++t) {
+            if (!ok || j >= n_t[t]) continue;
+            ok = mbar_wait(bar(C::kBarPFull + t), j & 1, abort_flag);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t vb = base + C::kVOff + (j % C::kStages) * C::kTileBytes;
+#pragma unroll
+            for (int kk = 0; kk < kBlockN / 16; ++kk)
+              mma_ts(tmem + C::kColO + t * D, tmem + C::kColP + t * 64 + kk * 8,
+                     sdesc_sw128(vb + kk * 2048, C::kChunkBytes, 1024), kIdO,
+                     (j > 0 || kk > 0) ? 1u : 0u);
+            mma_commit(bar(C::kBarPVDone + t));
+          }
+          if (!ok) break;
+          mma_commit(bar(C::kBarVEmpty + j % C::kStages));
+        }
+      } else {
       for (int j = 0; j < n_max && ok; ++j) {
         ok = mbar_wait(bar(C::kBarVFull + j % C::kStages), (j / C::kStages) & 1, abort_flag);
         tc_fence_after();
@@ -265,6 +312,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(bar(C::kBarVEmpty + j % C::kStages));
         if (j + 1 < n_max) mma_commit(bar(C::kBarKEmpty + (j + 1) % C::kStages));
       }
+      }
       // Let every MMA this thread issued finish before TMEM is released.
       mma_commit(bar(C::kBarDrain));
       mbar_wait(bar(C::kBarDrain), 0, nullptr);
@@ -279,6 +327,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + lane_base + t * 128;
     const uint32_t tO = tmem + lane_base + C::kColO + t * D;
+    const uint32_t tP = tmem + lane_base + C::kColP + t * 64;  // separate-P layout only
     const float sl2 = args.scale_log2;
     const int diag_j = tile_row0 / kBlockN;
     const bool ragged = (N % kBlockN) != 0;
@@ -296,6 +345,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, sr[c]);
 #pragma unroll
       for (int c = 0; c < 4; ++c) tmem_ld_wait(sr[c]);
+      if constexpr (C::kSepP) {  // S(j) is in registers: the next QK^T may overwrite it
+        tc_fence_before();
+        mbar_arrive(bar(C::kBarSFree + t));
+      }
       float x[128];
 #pragma unroll
       for (int c = 0; c < 128; ++c) x[c] = __uint_as_float(sr[c >> 5][c & 31]);
@@ -320,9 +373,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float2 sl2x2 = make_float2(sl2, sl2);
       const float2 negm = make_float2(-m_use, -m_use);
       float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {  // P columns [32h, 32h+32) hold scores [64h, 64h+64)
-        uint32_t pk[32];
+      auto exp_half = [&](int h, uint32_t (&pk)[32]) {
 #pragma unroll
         for (int c = 0; c < 32; ++c) {
           const int e = 64 * h + 2 * c;
@@ -332,12 +383,32 @@ __global__ void __launch_bounds__(kThreads, 1)
           else acc0 = __fadd2_rn(acc0, pr);
           pk[c] = pack_bf16(pr.x, pr.y);
         }
-        tmem_st32(tS + 32 * h, pk);
+      };
+      uint32_t pk[32];
+      if constexpr (!C::kSepP) {
+        // P columns [32h, 32h+32) hold scores [64h, 64h+64), over S
+        exp_half(0, pk);
+        tmem_st32(tS, pk);
+        exp_half(1, pk);
+        tmem_st32(tS + 32, pk);
+      } else {
+        exp_half(0, pk);
+        // P(j-1) has been read and O accumulated once P.V(j-1) has completed
+        if (j > 0) {
+          ok = mbar_wait(bar(C::kBarPVDone + t), (j - 1) & 1, abort_flag);
+          ok = __all_sync(0xffffffffu, ok);
+          if (!ok) break;
+          tc_fence_after();
+        }
+        tmem_st32(tP, pk);
+        exp_half(1, pk);
+        tmem_st32(tP + 32, pk);
       }
       l = alpha * l + ((acc0.x + acc0.y) + (acc1.x + acc1.y));
 
-      // Rescale the accumulator when this warp's maximum moved. The S MMA of
-      // this tile was committed after the previous P.V, so O is settled.
+      // Rescale the accumulator when this warp's maximum moved. O is settled:
+      // with P over S, this tile's S MMA was committed after the previous
+      // P.V; with separate P, P.V(j-1) has completed (waited above).
       if (j > 0 && __any_sync(0xffffffffu, need)) {
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
@@ -359,7 +430,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(bar(C::kBarPFull + t));
     }
     if (ok && n_mine > 0) {
-      ok = mbar_wait(bar(C::kBarOFinal + t), 0, abort_flag);
+      if constexpr (C::kSepP)
+        ok = mbar_wait(bar(C::kBarPVDone + t), (n_mine - 1) & 1, abort_flag);
+      else
+        ok = mbar_wait(bar(C::kBarOFinal + t), 0, abort_flag);
       ok = __all_sync(0xffffffffu, ok);
       if (ok) {
         tc_fence_after();
