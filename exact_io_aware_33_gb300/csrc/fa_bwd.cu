@@ -74,70 +74,73 @@ __host__ __device__ __forceinline__ size_t acc_index(long long bh, int n, int c,
 // For every row of the padded [BH, Npad] grid: -D = -sum_c dO[c] * O[c] and
 // -LSE * log2(e) (rows past N get 0 and -inf, so that their recomputed
 // probabilities are exactly 0). Stored negated so the main kernel's packed
-// FMAs take them as addends. One group of D/8 lanes per row, each lane
-// reading 8 bf16 (16 bytes) of both tensors. Also zeroes dq_acc.
+// FMAs take them as addends. Grid (row blocks, BH): one group of D/8 lanes
+// per row, each lane reading 8 bf16 (16 bytes) of both tensors; the CTAs of
+// a head also zero its Npad x D slice of the dQ accumulator.
 template <int D>
 __global__ void __launch_bounds__(256) fa_bwd_pre(const __nv_bfloat16* __restrict__ o,
                                                   const __nv_bfloat16* __restrict__ dO,
                                                   const float* __restrict__ lse,
                                                   float* __restrict__ Dvec,
                                                   float* __restrict__ lse2, int N, int n_pad,
-                                                  long long pad_rows, float4* __restrict__ dq_acc,
-                                                  long long acc_vec4) {
-  constexpr int kTpr = D / 8;
-  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;  // multiple of 32
-  const long long tid0 = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-  const long long lanes = ((pad_rows * kTpr + 31) / 32) * 32;
-  for (long long t = tid0; t < lanes; t += stride) {
-    const long long prow = t / kTpr;
-    const int sub = static_cast<int>(t % kTpr);
-    const long long bh = prow / n_pad;
-    const int n = static_cast<int>(prow - bh * n_pad);
-    const bool live = prow < pad_rows && n < N;
-    float acc = 0.f;
-    if (live) {
-      const long long row = bh * N + n;
-      const uint4 a = *reinterpret_cast<const uint4*>(o + row * D + sub * 8);
-      const uint4 b = *reinterpret_cast<const uint4*>(dO + row * D + sub * 8);
-      const uint32_t aw[4] = {a.x, a.y, a.z, a.w};
-      const uint32_t bw[4] = {b.x, b.y, b.z, b.w};
+                                                  float* __restrict__ dq_acc, int BH) {
+  constexpr int kTpr = D / 8;               // lanes per row (8 or 16)
+  constexpr int kRowsPerCta = 256 / kTpr;
+  for (int bh = blockIdx.y; bh < BH; bh += gridDim.y) {
+  const int sub = threadIdx.x % kTpr;
+  const int n = blockIdx.x * kRowsPerCta + threadIdx.x / kTpr;  // < n_pad (grid covers n_pad)
+  const size_t head = static_cast<size_t>(bh) * N;
+  const bool live = n < N;
+  float acc = 0.f;
+  if (live) {
+    const size_t row = head + n;
+    const uint4 a = *reinterpret_cast<const uint4*>(o + row * D + sub * 8);
+    const uint4 b = *reinterpret_cast<const uint4*>(dO + row * D + sub * 8);
+    const uint32_t aw[4] = {a.x, a.y, a.z, a.w};
+    const uint32_t bw[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float2 fa2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&aw[e]));
-        const float2 fb2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&bw[e]));
-        acc = fmaf(fa2.x, fb2.x, acc);
-        acc = fmaf(fa2.y, fb2.y, acc);
-      }
-    }
-#pragma unroll
-    for (int off = kTpr / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (prow < pad_rows && sub == 0) {
-      Dvec[prow] = -acc;
-      lse2[prow] = live ? -lse[bh * N + n] * kLog2e : -INFINITY;
+    for (int e = 0; e < 4; ++e) {
+      const float2 fa2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&aw[e]));
+      const float2 fb2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&bw[e]));
+      acc = fmaf(fa2.x, fb2.x, acc);
+      acc = fmaf(fa2.y, fb2.y, acc);
     }
   }
-  for (long long i = tid0; i < acc_vec4; i += stride) dq_acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+  for (int off = kTpr / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (sub == 0 && n < n_pad) {
+    const size_t prow = static_cast<size_t>(bh) * n_pad + n;
+    Dvec[prow] = -acc;
+    lse2[prow] = live ? -lse[head + n] * kLog2e : -INFINITY;
+  }
+  // zero rows [n0, n0 + kRowsPerCta) of this head's accumulator slice
+  float4* z = reinterpret_cast<float4*>(dq_acc + (static_cast<size_t>(bh) * n_pad +
+                                                  static_cast<size_t>(blockIdx.x) * kRowsPerCta) * D);
+#pragma unroll
+  for (int i = threadIdx.x; i < kRowsPerCta * D / 4; i += 256) z[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
 }
 
 // ---------------------------------------------------------------- B2
 // dQ = bf16(accumulator), reading the blocked accumulator layout and
-// writing [BH, N, d] row-major; one thread per 4 columns of a row.
+// writing [BH, N, d] row-major. Grid (row blocks, BH); one thread per 8
+// columns of a row (two 16-byte loads, one 16-byte store).
 template <int D>
 __global__ void __launch_bounds__(256) fa_bwd_post(const float* __restrict__ acc,
-                                                   uint2* __restrict__ dq, int N, int n_pad,
-                                                   long long n_vec4) {
-  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
-  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n_vec4;
-       i += stride) {
-    const long long e = i * 4;
-    const int c = static_cast<int>(e % D);
-    const long long row = e / D;
-    const long long bh = row / N;
-    const int n = static_cast<int>(row - bh * N);
+                                                   uint4* __restrict__ dq, int N, int n_pad, int BH) {
+  constexpr int kTpr = D / 8;
+  constexpr int kRowsPerCta = 256 / kTpr;
+  const int n = blockIdx.x * kRowsPerCta + threadIdx.x / kTpr;
+  if (n >= N) return;
+  const int c = (threadIdx.x % kTpr) * 8;
+  for (int bh = blockIdx.y; bh < BH; bh += gridDim.y) {
     const float4 a = *reinterpret_cast<const float4*>(acc + acc_index<D>(bh, n, c, n_pad));
-    dq[i] = make_uint2(pack_bf16(a.x, a.y), pack_bf16(a.z, a.w));
+    const float4 b = *reinterpret_cast<const float4*>(acc + acc_index<D>(bh, n, c + 4, n_pad));
+    dq[((static_cast<size_t>(bh) * N + n) * D + c) / 8] =
+        make_uint4(pack_bf16(a.x, a.y), pack_bf16(a.z, a.w), pack_bf16(b.x, b.y), pack_bf16(b.z, b.w));
   }
 }
+
 // ---------------------------------------------------------------- B1, d = 128
 // With d = 128 the five accumulators (S^T, dP^T, dQ, dK, dV) need 640
 // tensor-memory columns of the 512, so dQ shares the dP^T columns and each
@@ -946,13 +949,12 @@ template <int D>
 int launch_pre_d(const Problem& p, const void* o, const float* lse, const void* dO,
                  void* workspace, cudaStream_t stream) {
   const Workspace w = carve(p, workspace);
-  const long long acc_vec4 = w.pad_rows * D / 4;
-  const long long work = w.pad_rows * (D / 8) > acc_vec4 ? w.pad_rows * (D / 8) : acc_vec4;
-  long long blocks = (work + 255) / 256;
-  if (blocks > 65536) blocks = 65536;
-  fa_bwd_pre<D><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-      static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dO), lse, w.Dvec,
-      w.lse2, p.N, w.n_pad, w.pad_rows, reinterpret_cast<float4*>(w.acc), acc_vec4);
+  constexpr int kRowsPerCta = 256 / (D / 8);
+  const int BH = p.B * p.H;
+  const dim3 grid(w.n_pad / kRowsPerCta, BH < 65535 ? BH : 65535);
+  fa_bwd_pre<D><<<grid, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(o),
+                                           static_cast<const __nv_bfloat16*>(dO), lse, w.Dvec,
+                                           w.lse2, p.N, w.n_pad, w.acc, BH);
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
@@ -1024,15 +1026,17 @@ int launch_bwd_main(const Problem& p, const void* dO, void* dk, void* dv, void* 
 
 int launch_bwd_post(const Problem& p, void* dq, const void* workspace, cudaStream_t stream) {
   const Workspace w = carve(p, const_cast<void*>(workspace));
-  const long long n_vec4 = static_cast<long long>(p.B) * p.H * p.N * p.d / 4;
-  long long blocks = (n_vec4 + 255) / 256;
-  if (blocks > 65536) blocks = 65536;
-  if (p.d == 64)
-    fa_bwd_post<64><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(w.acc, static_cast<uint2*>(dq), p.N, w.n_pad, n_vec4);
-  else if (p.d == 128)
-    fa_bwd_post<128><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(w.acc, static_cast<uint2*>(dq), p.N, w.n_pad, n_vec4);
-  else
+  const int BH = p.B * p.H;
+  const unsigned gy = BH < 65535 ? BH : 65535;
+  if (p.d == 64) {
+    const dim3 grid((p.N + 31) / 32, gy);
+    fa_bwd_post<64><<<grid, 256, 0, stream>>>(w.acc, static_cast<uint4*>(dq), p.N, w.n_pad, BH);
+  } else if (p.d == 128) {
+    const dim3 grid((p.N + 15) / 16, gy);
+    fa_bwd_post<128><<<grid, 256, 0, stream>>>(w.acc, static_cast<uint4*>(dq), p.N, w.n_pad, BH);
+  } else {
     return FA_ERR_UNSUPPORTED;
+  }
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
