@@ -18,6 +18,12 @@ tiled
     order the pages give it, with the causal mask and ragged tail tiles.
 finite_diff
     Central finite differences of L = sum(O * dO), for pinning the backward.
+general
+    The dense definition with Nq queries over Nk keys (causal queries are the
+    last Nq positions), an optional sliding window and key-range restriction.
+merge
+    The page's rule for merging partial softmax states, applied to the parts
+    of a split key range.
 
 Pins (what fixes each function other than itself) live in
 ``tests/test_oracle_pins.py``; each function's docstring names its pins.
@@ -29,6 +35,6 @@ Sources cited (title of the page, then its section):
   * "FlashAttention" (Road to Intelligence, Chapter 11)
 """
 
-from . import dense, tiled, finite_diff  # noqa: F401
+from . import dense, tiled, finite_diff, general, merge  # noqa: F401
 
-__all__ = ["dense", "tiled", "finite_diff"]
+__all__ = ["dense", "tiled", "finite_diff", "general", "merge"]
