@@ -265,6 +265,78 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
   return rc;
 }
 
+namespace {
+
+// Checks of the extended forward forms; sets *empty for B, H or Nq = 0.
+int check_fwd_ex(int B, int H, int Nq, int Nk, int d, int causal, int window, float scale,
+                 std::initializer_list<const void*> ptrs, bool* empty) {
+  *empty = false;
+  if (B < 0 || H < 0 || Nq < 0 || Nk < 0 || window < 0) return FA_ERR_INVALID;
+  if (!std::isfinite(scale) || scale < 0.f) return FA_ERR_INVALID;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (window > 0 && !causal) return FA_ERR_INVALID;
+  if (B == 0 || H == 0 || Nq == 0) {
+    *empty = true;
+    return FA_OK;
+  }
+  if (Nk == 0 || (causal && Nq > Nk)) return FA_ERR_INVALID;
+  const long long bh = static_cast<long long>(B) * H;
+  if (bh > (1LL << 31) - 1) return FA_ERR_INVALID;
+  if (bh * static_cast<long long>(Nq > Nk ? Nq : Nk) * d > (1LL << 46)) return FA_ERR_INVALID;
+  for (const void* ptr : ptrs)
+    if (!fa::aligned16(ptr)) return FA_ERR_INVALID;
+  fa::DeviceState* st = nullptr;
+  return fa::current_device(&st);
+}
+
+int sm_count() {
+  int dev = 0, sms = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess)
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  return sms > 0 ? sms : 148;
+}
+
+}  // namespace
+
+int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+              int Nq, int Nk, int d, int causal, int window, float scale, void* cuda_stream) {
+  bool empty = false;
+  int rc = check_fwd_ex(B, H, Nq, Nk, d, causal, window, scale, {q, k, v, o, lse}, &empty);
+  if (rc != FA_OK || empty) return rc;
+  fa::FwdProblem p{q, k, v, B, H, Nq, Nk, d, causal, window, scale};
+  return fa::launch_fwd_general(p, o, lse, nullptr, nullptr, 1,
+                                static_cast<cudaStream_t>(cuda_stream));
+}
+
+int fa_decode_num_splits(int B, int H, int Nq, int Nk, int d, int n_splits) {
+  if (B <= 0 || H <= 0 || Nq <= 0 || Nk <= 0 || d <= 0) return 0;
+  fa::FwdProblem p{nullptr, nullptr, nullptr, B, H, Nq, Nk, d, 0, 0, 1.f};
+  return fa::fwd_split_count(p, n_splits, sm_count());
+}
+
+size_t fa_decode_workspace_bytes(int B, int H, int Nq, int Nk, int d, int n_splits) {
+  const int s = fa_decode_num_splits(B, H, Nq, Nk, d, n_splits);
+  if (s <= 0) return 0;
+  return static_cast<size_t>(s) * B * H * Nq * (static_cast<size_t>(d) + 1) * 4;
+}
+
+int fa_decode_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                      int H, int Nq, int Nk, int d, int causal, int window, float scale,
+                      int n_splits, void* workspace, size_t ws_bytes, void* cuda_stream) {
+  bool empty = false;
+  int rc = check_fwd_ex(B, H, Nq, Nk, d, causal, window, scale, {q, k, v, o, lse}, &empty);
+  if (rc != FA_OK || empty) return rc;
+  const size_t need = fa_decode_workspace_bytes(B, H, Nq, Nk, d, n_splits);
+  if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || ws_bytes < need)
+    return FA_ERR_WORKSPACE;
+  const int s = fa_decode_num_splits(B, H, Nq, Nk, d, n_splits);
+  fa::FwdProblem p{q, k, v, B, H, Nq, Nk, d, causal, window, scale};
+  float* part_o = static_cast<float*>(workspace);
+  float* part_lse = part_o + static_cast<size_t>(s) * B * H * Nq * d;
+  return fa::launch_fwd_general(p, o, lse, part_o, part_lse, s,
+                                static_cast<cudaStream_t>(cuda_stream));
+}
+
 int fa_get_last_device_status(void) {
   fa::DeviceState* st = nullptr;
   if (fa::current_device(&st) != FA_OK) return FA_ERR_LAUNCH;

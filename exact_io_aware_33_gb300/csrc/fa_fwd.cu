@@ -93,14 +93,20 @@ struct FwdCfg {
 };
 
 struct FwdArgs {
-  __nv_bfloat16* o;
-  float* lse;
+  __nv_bfloat16* o;    // [BH, Nq, D] (whole-range launch)
+  float* lse;          // [BH, Nq]
+  float* part_o;       // [splits, BH, Nq, D] fp32 normalised partial outputs (split launch)
+  float* part_lse;     // [splits, BH, Nq] natural-log partial LSE (split launch)
   int* status;
-  int N;
+  int Nq, Nk;
+  int kv_off;          // Nk - Nq: causal query i sits at key position i + kv_off
+  int window;          // 0 = none; else keys j <= i + kv_off - window are masked
   int BH;
   int causal;
   int num_pairs;
-  float scale_log2;  // scale * log2(e), > 0
+  int split_tiles;     // key tiles per split (all of them when not split)
+  int split_mode;      // 1: write fp32 partial states instead of O / LSE
+  float scale_log2;    // scale * log2(e), > 0
 };
 
 template <int D>
@@ -116,18 +122,48 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base_ptr + C::kMiscOff);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(base_ptr + C::kMiscOff + 4);
 
-  const int N = args.N;
+  // Key tiles each query tile needs: the causal limit (keys up to the last
+  // row's position), the window (keys after the first row's position minus
+  // the window), and this CTA's split of the key range. The CTA streams the
+  // union [j_first, j_first + n_stream) of its two tiles' ranges once; tile
+  // t takes part in stream steps [a_t, a_t + n_t).
+  const int Nq = args.Nq, Nk = args.Nk;
   const int bh = blockIdx.x % args.BH;
   const int pair = args.num_pairs - 1 - static_cast<int>(blockIdx.x / args.BH);
-  const int n_kv = (N + kBlockN - 1) / kBlockN;
-  int q_row0[kQTiles], n_t[kQTiles];
+  const int n_kv = (Nk + kBlockN - 1) / kBlockN;
+  const int split_lo = blockIdx.y * args.split_tiles;
+  const int split_hi = min(n_kv, split_lo + args.split_tiles);
+  int q_row0[kQTiles], lo_t[kQTiles], n_t[kQTiles];
 #pragma unroll
   for (int t = 0; t < kQTiles; ++t) {
     q_row0[t] = pair * (kBlockM * kQTiles) + t * kBlockM;
-    if (q_row0[t] >= N) n_t[t] = 0;
-    else n_t[t] = args.causal ? (q_row0[t] / kBlockN + 1) : n_kv;
+    int lo = split_lo, hi = split_hi;
+    if (args.causal) {
+      const int last_row = min(q_row0[t] + kBlockM, Nq) - 1;
+      hi = min(hi, (last_row + args.kv_off) / kBlockN + 1);
+    }
+    if (args.window) {
+      const int first_key = q_row0[t] + args.kv_off - args.window + 1;
+      if (first_key > 0) lo = max(lo, first_key / kBlockN);
+    }
+    lo_t[t] = lo;
+    n_t[t] = (q_row0[t] >= Nq || hi <= lo) ? 0 : hi - lo;
   }
-  const int n_max = n_t[0] > n_t[1] ? n_t[0] : n_t[1];
+  int j_first = 0, j_end = 0;
+  {
+    bool any = false;
+#pragma unroll
+    for (int t = 0; t < kQTiles; ++t) {
+      if (n_t[t] == 0) continue;
+      if (!any || lo_t[t] < j_first) j_first = lo_t[t];
+      if (!any || lo_t[t] + n_t[t] > j_end) j_end = lo_t[t] + n_t[t];
+      any = true;
+    }
+  }
+  const int n_stream = j_end - j_first;
+  // stream steps [a_t, b_t) of each query tile (empty when n_t = 0)
+  const int a0 = lo_t[0] - j_first, b0 = a0 + n_t[0];
+  const int a1 = lo_t[1] - j_first, b1 = a1 + n_t[1];
 
   const int warp = warp_id();
   const int lane = lane_id();
@@ -180,34 +216,35 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       int issued = 0;
       bool ok = true;
-      for (int j = 0; j < n_max && ok; ++j) {
-        const int s = j % C::kStages;
-        const uint32_t ph = ((j / C::kStages) + 1) & 1;
-        if (j >= C::kStages) ok = mbar_wait(bar(C::kBarKEmpty + s), ph, abort_flag);
+      for (int jj = 0; jj < n_stream && ok; ++jj) {
+        const int s = jj % C::kStages;
+        const uint32_t ph = ((jj / C::kStages) + 1) & 1;
+        const int key0 = (j_first + jj) * kBlockN;
+        if (jj >= C::kStages) ok = mbar_wait(bar(C::kBarKEmpty + s), ph, abort_flag);
         if (!ok) break;
         mbar_arrive_expect_tx(bar(C::kBarKFull + s), C::kTileBytes);
         for (int c = 0; c < C::kChunks; ++c)
           tma_load_3d(base + C::kKOff + s * C::kTileBytes + c * C::kChunkBytes, &tmK,
-                      bar(C::kBarKFull + s), c * 64, j * kBlockN, bh);
-        if (j >= C::kStages) ok = mbar_wait(bar(C::kBarVEmpty + s), ph, abort_flag);
+                      bar(C::kBarKFull + s), c * 64, key0, bh);
+        if (jj >= C::kStages) ok = mbar_wait(bar(C::kBarVEmpty + s), ph, abort_flag);
         if (!ok) {
-          issued = 2 * j + 1;
+          issued = 2 * jj + 1;
           break;
         }
         mbar_arrive_expect_tx(bar(C::kBarVFull + s), C::kTileBytes);
         for (int c = 0; c < C::kChunks; ++c)
           tma_load_3d(base + C::kVOff + s * C::kTileBytes + c * C::kChunkBytes, &tmV,
-                      bar(C::kBarVFull + s), c * 64, j * kBlockN, bh);
-        issued = 2 * j + 2;
+                      bar(C::kBarVFull + s), c * 64, key0, bh);
+        issued = 2 * jj + 2;
       }
       if (*abort_flag) {
         // Let every copy this thread started land before the CTA exits.
         mbar_wait(bar(C::kBarQFull), 0, nullptr);
         for (int x = issued - 1; x >= 0 && x >= issued - 2 * C::kStages; --x) {
-          const int j = x >> 1;
-          const int s = j % C::kStages;
+          const int jj = x >> 1;
+          const int s = jj % C::kStages;
           const int b = (x & 1) ? (C::kBarVFull + s) : (C::kBarKFull + s);
-          mbar_wait(bar(b), (j / C::kStages) & 1, nullptr);
+          mbar_wait(bar(b), (jj / C::kStages) & 1, nullptr);
         }
       }
     }
@@ -216,19 +253,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t kIdS = idesc_bf16_f32(kBlockM, kBlockN, false, false);
       constexpr uint32_t kIdO = idesc_bf16_f32(kBlockM, D, false, true);
-      bool ok = mbar_wait(bar(C::kBarQFull), 0, abort_flag);
+      bool ok = n_stream > 0 ? mbar_wait(bar(C::kBarQFull), 0, abort_flag) : false;
       tc_fence_after();
       int k_ready = -1;
-      auto ensure_k = [&](int j) {
-        if (ok && j > k_ready) {
-          ok = mbar_wait(bar(C::kBarKFull + j % C::kStages), (j / C::kStages) & 1, abort_flag);
+      auto ensure_k = [&](int jj) {
+        if (ok && jj > k_ready) {
+          ok = mbar_wait(bar(C::kBarKFull + jj % C::kStages), (jj / C::kStages) & 1, abort_flag);
           tc_fence_after();
-          k_ready = j;
+          k_ready = jj;
         }
       };
-      auto issue_s = [&](int t, int j) {
+      // S_t = Q_t K^T for stream step jj
+      auto issue_s = [&](int t, int jj) {
         const uint32_t qb = base + C::kQOff + t * C::kTileBytes;
-        const uint32_t kb = base + C::kKOff + (j % C::kStages) * C::kTileBytes;
+        const uint32_t kb = base + C::kKOff + (jj % C::kStages) * C::kTileBytes;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
@@ -237,81 +275,153 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mma_commit(bar(C::kBarSFull + t));
       };
-      auto issue_pv = [&](int t, int j) {
-        const uint32_t vb = base + C::kVOff + (j % C::kStages) * C::kTileBytes;
+      // O_t (+)= P_t V for stream step jj; P_t from its TMEM columns
+      auto issue_pv = [&](int t, int jj, bool first) {
+        const uint32_t vb = base + C::kVOff + (jj % C::kStages) * C::kTileBytes;
+        const uint32_t pcol = C::kSepP ? C::kColP + t * 64 : t * 128;
 #pragma unroll
-        for (int kk = 0; kk < kBlockN / 16; ++kk) {
-          mma_ts(tmem + C::kColO + t * D, tmem + t * 128 + kk * 8,
+        for (int kk = 0; kk < kBlockN / 16; ++kk)
+          mma_ts(tmem + C::kColO + t * D, tmem + pcol + kk * 8,
                  sdesc_sw128(vb + kk * 2048, C::kChunkBytes, 1024), kIdO,
-                 (j > 0 || kk > 0) ? 1u : 0u);
-        }
+                 (!first || kk > 0) ? 1u : 0u);
+      };
+      auto step_of = [&](int t, int jj) -> int {  // tile-local step, or -1
+        const int a = t == 0 ? a0 : a1, b = t == 0 ? b0 : b1;
+        return (jj >= a && jj < b) ? jj - a : -1;
       };
       ensure_k(0);
       if (ok) {
 #pragma unroll
         for (int t = 0; t < kQTiles; ++t)
-          if (n_t[t] > 0) issue_s(t, 0);
+          if (step_of(t, 0) == 0) issue_s(t, 0);
         mma_commit(bar(C::kBarKEmpty + 0));
       }
+      // The MMA thread shares its scheduler with busy softmax warps and the
+      // tensor core's issue queue is short, so its loop is kept lean: when
+      // both query tiles start at stream step 0 (no window) a tile's step is
+      // the stream step itself.
+      const bool aligned = (a0 == 0 && a1 == 0);
       if constexpr (C::kSepP) {
-        // Per key tile j: QK^T of tile j+1 for each query tile as soon as its
-        // softmax holds S(j) in registers, then P.V of tile j once P(j) is
-        // written.
-        for (int j = 0; j < n_max && ok; ++j) {
+        if (aligned) {
+          for (int jj = 0; jj < n_stream && ok; ++jj) {
+#pragma unroll
+            for (int t = 0; t < kQTiles; ++t) {
+              if (!ok || jj + 1 >= (t == 0 ? b0 : b1)) continue;
+              ok = mbar_wait(bar(C::kBarSFree + t), jj & 1, abort_flag);
+              if (!ok) break;
+              ensure_k(jj + 1);
+              if (!ok) break;
+              tc_fence_after();
+              issue_s(t, jj + 1);
+            }
+            if (!ok) break;
+            if (jj + 1 < n_stream) mma_commit(bar(C::kBarKEmpty + (jj + 1) % C::kStages));
+            ok = mbar_wait(bar(C::kBarVFull + jj % C::kStages), (jj / C::kStages) & 1, abort_flag);
+            tc_fence_after();
+#pragma unroll
+            for (int t = 0; t < kQTiles; ++t) {
+              if (!ok || jj >= (t == 0 ? b0 : b1)) continue;
+              ok = mbar_wait(bar(C::kBarPFull + t), jj & 1, abort_flag);
+              if (!ok) break;
+              tc_fence_after();
+              issue_pv(t, jj, jj == 0);
+              mma_commit(bar(C::kBarPVDone + t));
+            }
+            if (!ok) break;
+            mma_commit(bar(C::kBarVEmpty + jj % C::kStages));
+          }
+        }
+        // General case: per stream step jj, QK^T of step jj+1 for each query
+        // tile as soon as its softmax holds S of step jj in registers, then
+        // P.V of step jj once P is written.
+        for (int jj = 0; jj < n_stream && ok && !aligned; ++jj) {
 #pragma unroll
           for (int t = 0; t < kQTiles; ++t) {
-            if (!ok || j + 1 >= n_t[t]) continue;
-            ok = mbar_wait(bar(C::kBarSFree + t), j & 1, abort_flag);
+            const int u = step_of(t, jj + 1);
+            if (!ok || u < 0) continue;
+            if (u > 0) ok = mbar_wait(bar(C::kBarSFree + t), (u - 1) & 1, abort_flag);
             if (!ok) break;
-            ensure_k(j + 1);
+            ensure_k(jj + 1);
             if (!ok) break;
             tc_fence_after();
-            issue_s(t, j + 1);
+            issue_s(t, jj + 1);
           }
           if (!ok) break;
-          if (j + 1 < n_max) mma_commit(bar(C::kBarKEmpty + (j + 1) % C::kStages));
-          ok = mbar_wait(bar(C::kBarVFull + j % C::kStages), (j / C::kStages) & 1, abort_flag);
+          if (jj + 1 < n_stream) mma_commit(bar(C::kBarKEmpty + (jj + 1) % C::kStages));
+          ok = mbar_wait(bar(C::kBarVFull + jj % C::kStages), (jj / C::kStages) & 1, abort_flag);
           tc_fence_after();
 #pragma unroll
           for (int t = 0; t < kQTiles; ++t) {
-            if (!ok || j >= n_t[t]) continue;
-            ok = mbar_wait(bar(C::kBarPFull + t), j & 1, abort_flag);
+            const int u = step_of(t, jj);
+            if (!ok || u < 0) continue;
+            ok = mbar_wait(bar(C::kBarPFull + t), u & 1, abort_flag);
             if (!ok) break;
             tc_fence_after();
-            const uint32_t vb = base + C::kVOff + (j % C::kStages) * C::kTileBytes;
-#pragma unroll
-            for (int kk = 0; kk < kBlockN / 16; ++kk)
-              mma_ts(tmem + C::kColO + t * D, tmem + C::kColP + t * 64 + kk * 8,
-                     sdesc_sw128(vb + kk * 2048, C::kChunkBytes, 1024), kIdO,
-                     (j > 0 || kk > 0) ? 1u : 0u);
+            issue_pv(t, jj, u == 0);
             mma_commit(bar(C::kBarPVDone + t));
           }
           if (!ok) break;
-          mma_commit(bar(C::kBarVEmpty + j % C::kStages));
+          mma_commit(bar(C::kBarVEmpty + jj % C::kStages));
         }
       } else {
-      for (int j = 0; j < n_max && ok; ++j) {
-        ok = mbar_wait(bar(C::kBarVFull + j % C::kStages), (j / C::kStages) & 1, abort_flag);
-        tc_fence_after();
+        // P overwrites S: each tile's next QK^T is issued after its P.V, so
+        // the P.V reads P before the new S lands in the same columns.
+        if (aligned) {
+          for (int jj = 0; jj < n_stream && ok; ++jj) {
+            ok = mbar_wait(bar(C::kBarVFull + jj % C::kStages), (jj / C::kStages) & 1, abort_flag);
+            tc_fence_after();
 #pragma unroll
-        for (int t = 0; t < kQTiles; ++t) {
-          if (!ok || j >= n_t[t]) continue;
-          ok = mbar_wait(bar(C::kBarPFull + t), j & 1, abort_flag);
-          if (!ok) break;
-          tc_fence_after();
-          issue_pv(t, j);
-          if (j + 1 < n_t[t]) {
-            ensure_k(j + 1);
+            for (int t = 0; t < kQTiles; ++t) {
+              const int bt = t == 0 ? b0 : b1;
+              if (!ok || jj >= bt) continue;
+              ok = mbar_wait(bar(C::kBarPFull + t), jj & 1, abort_flag);
+              if (!ok) break;
+              tc_fence_after();
+              issue_pv(t, jj, jj == 0);
+              if (jj + 1 < bt) {
+                ensure_k(jj + 1);
+                if (!ok) break;
+                issue_s(t, jj + 1);
+              } else {
+                mma_commit(bar(C::kBarOFinal + t));
+              }
+            }
             if (!ok) break;
-            issue_s(t, j + 1);
-          } else {
-            mma_commit(bar(C::kBarOFinal + t));
+            mma_commit(bar(C::kBarVEmpty + jj % C::kStages));
+            if (jj + 1 < n_stream) mma_commit(bar(C::kBarKEmpty + (jj + 1) % C::kStages));
           }
         }
-        if (!ok) break;
-        mma_commit(bar(C::kBarVEmpty + j % C::kStages));
-        if (j + 1 < n_max) mma_commit(bar(C::kBarKEmpty + (j + 1) % C::kStages));
-      }
+        for (int jj = 0; jj < n_stream && ok && !aligned; ++jj) {
+          ok = mbar_wait(bar(C::kBarVFull + jj % C::kStages), (jj / C::kStages) & 1, abort_flag);
+          tc_fence_after();
+#pragma unroll
+          for (int t = 0; t < kQTiles; ++t) {
+            const int u = step_of(t, jj);
+            if (!ok || u < 0) continue;
+            ok = mbar_wait(bar(C::kBarPFull + t), u & 1, abort_flag);
+            if (!ok) break;
+            tc_fence_after();
+            issue_pv(t, jj, u == 0);
+            if (jj + 1 < (t == 0 ? b0 : b1)) {
+              ensure_k(jj + 1);
+              if (!ok) break;
+              issue_s(t, jj + 1);
+            } else {
+              mma_commit(bar(C::kBarOFinal + t));
+            }
+          }
+          if (!ok) break;
+#pragma unroll
+          for (int t = 0; t < kQTiles; ++t) {  // a tile whose range starts at step jj+1
+            if (!ok || step_of(t, jj + 1) != 0) continue;
+            ensure_k(jj + 1);
+            if (!ok) break;
+            issue_s(t, jj + 1);
+          }
+          if (!ok) break;
+          mma_commit(bar(C::kBarVEmpty + jj % C::kStages));
+          if (jj + 1 < n_stream) mma_commit(bar(C::kBarKEmpty + (jj + 1) % C::kStages));
+        }
       }
       // Let every MMA this thread issued finish before TMEM is released.
       mma_commit(bar(C::kBarDrain));
@@ -320,23 +430,26 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp < kMmaWarp) {
     // ------------------------------------------------------------ softmax
     const int t = warp / 4;
-    const int tile_row0 = pair * (kBlockM * kQTiles) + t * kBlockM;
-    const int n_mine = tile_row0 >= N ? 0 : (args.causal ? tile_row0 / kBlockN + 1 : n_kv);
-    const int row_in_tile = threadIdx.x & 127;
-    const int row = tile_row0 + row_in_tile;
+    const int n_mine = t == 0 ? n_t[0] : n_t[1];
+    const int tile_row0 = t == 0 ? q_row0[0] : q_row0[1];
+    const int key_tile0 = j_first + (t == 0 ? a0 : a1);  // first key tile of this query tile
+    const int row = tile_row0 + (threadIdx.x & 127);
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + lane_base + t * 128;
     const uint32_t tO = tmem + lane_base + C::kColO + t * D;
     const uint32_t tP = tmem + lane_base + C::kColP + t * 64;  // separate-P layout only
     const float sl2 = args.scale_log2;
-    const int diag_j = tile_row0 / kBlockN;
-    const bool ragged = (N % kBlockN) != 0;
+    // keys visible to this row: pos - window < key <= pos (pos = row + kv_off)
+    const int pos = row + args.kv_off;
+    const int key_hi = args.causal ? min(Nk, pos + 1) : Nk;          // exclusive
+    const int key_lo = args.window ? pos - args.window + 1 : -(1 << 30);
 
     float m_ref = -INFINITY;  // log2-domain reference maximum
     float l = 0.f;
     bool ok = true;
-    for (int j = 0; j < n_mine; ++j) {
-      ok = mbar_wait(bar(C::kBarSFull + t), j & 1, abort_flag);
+    for (int u = 0; u < n_mine; ++u) {
+      const int key0 = (key_tile0 + u) * kBlockN;
+      ok = mbar_wait(bar(C::kBarSFull + t), u & 1, abort_flag);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
@@ -345,7 +458,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, sr[c]);
 #pragma unroll
       for (int c = 0; c < 4; ++c) tmem_ld_wait(sr[c]);
-      if constexpr (C::kSepP) {  // S(j) is in registers: the next QK^T may overwrite it
+      if constexpr (C::kSepP) {  // S is in registers: the next QK^T may overwrite it
         tc_fence_before();
         mbar_arrive(bar(C::kBarSFree + t));
       }
@@ -353,13 +466,21 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int c = 0; c < 128; ++c) x[c] = __uint_as_float(sr[c >> 5][c & 31]);
 
-      const bool need_mask = (args.causal && j == diag_j) || (ragged && j == n_kv - 1);
-      if (need_mask) {
-        int lim = N - j * kBlockN;
-        if (args.causal) lim = min(lim, row - j * kBlockN + 1);
+      if (args.window == 0) {
+        // only the causal boundary tiles and the ragged last tile need a mask
+        if ((args.causal && key0 + kBlockN - 1 > tile_row0 + args.kv_off) || key0 + kBlockN > Nk) {
+          const int lim = key_hi - key0;
 #pragma unroll
-        for (int c = 0; c < 128; ++c)
-          if (c >= lim) x[c] = -INFINITY;
+          for (int c = 0; c < 128; ++c)
+            if (c >= lim) x[c] = -INFINITY;
+        }
+      } else {
+        const int lim_hi = key_hi - key0, lim_lo = key_lo - key0;
+        if (lim_hi < kBlockN || lim_lo > 0) {
+#pragma unroll
+          for (int c = 0; c < 128; ++c)
+            if (c >= lim_hi || c < lim_lo) x[c] = -INFINITY;
+        }
       }
       const float m_tile =
           max3(fmaxf(max32(x), max32(x + 32)), max32(x + 64), max32(x + 96)) * sl2;
@@ -393,9 +514,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_st32(tS + 32, pk);
       } else {
         exp_half(0, pk);
-        // P(j-1) has been read and O accumulated once P.V(j-1) has completed
-        if (j > 0) {
-          ok = mbar_wait(bar(C::kBarPVDone + t), (j - 1) & 1, abort_flag);
+        // the previous step's P has been read and O accumulated once its P.V completed
+        if (u > 0) {
+          ok = mbar_wait(bar(C::kBarPVDone + t), (u - 1) & 1, abort_flag);
           ok = __all_sync(0xffffffffu, ok);
           if (!ok) break;
           tc_fence_after();
@@ -408,8 +529,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       // Rescale the accumulator when this warp's maximum moved. O is settled:
       // with P over S, this tile's S MMA was committed after the previous
-      // P.V; with separate P, P.V(j-1) has completed (waited above).
-      if (j > 0 && __any_sync(0xffffffffu, need)) {
+      // P.V; with separate P, the previous P.V has completed (waited above).
+      if (u > 0 && __any_sync(0xffffffffu, need)) {
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t o[32];
@@ -429,6 +550,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       mbar_arrive(bar(C::kBarPFull + t));
     }
+    const bool live = row < Nq;
+    const size_t prow = (static_cast<size_t>(blockIdx.y) * args.BH + bh) * Nq + row;  // split launch
     if (ok && n_mine > 0) {
       if constexpr (C::kSepP)
         ok = mbar_wait(bar(C::kBarPVDone + t), (n_mine - 1) & 1, abort_flag);
@@ -438,34 +561,57 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ok) {
         tc_fence_after();
         const float inv_l = l > 0.f ? 1.0f / l : 0.f;
-        const bool live = row < N;
-        __nv_bfloat16* orow = args.o + (static_cast<size_t>(bh) * N + row) * D;
+        const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
+        const float lse_row = l > 0.f ? (m_use + log2f(l)) * kLn2 : -INFINITY;
+        const float2 il2 = make_float2(inv_l, inv_l);
+        if (args.split_mode) {
+          float* orow = args.part_o + prow * D;
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t o[32];
-          tmem_ld32(tO + c * 32, o);
-          tmem_ld_wait(o);
-          uint32_t pk[16];
-          const float2 il2 = make_float2(inv_l, inv_l);
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld32(tO + c * 32, o);
+            tmem_ld_wait(o);
+            if (live) {
+              float4* dst = reinterpret_cast<float4*>(orow + c * 32);
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const float2 v =
-                __fmul2_rn(make_float2(__uint_as_float(o[2 * e]), __uint_as_float(o[2 * e + 1])), il2);
-            pk[e] = pack_bf16(v.x, v.y);
+              for (int e = 0; e < 8; ++e) {
+                const float2 v0 = __fmul2_rn(make_float2(__uint_as_float(o[4 * e]), __uint_as_float(o[4 * e + 1])), il2);
+                const float2 v1 = __fmul2_rn(make_float2(__uint_as_float(o[4 * e + 2]), __uint_as_float(o[4 * e + 3])), il2);
+                dst[e] = make_float4(v0.x, v0.y, v1.x, v1.y);
+              }
+            }
           }
-          if (live) {
-            uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+          if (live) args.part_lse[prow] = lse_row;
+        } else {
+          __nv_bfloat16* orow = args.o + (static_cast<size_t>(bh) * Nq + row) * D;
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-              dst[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld32(tO + c * 32, o);
+            tmem_ld_wait(o);
+            uint32_t pko[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const float2 v =
+                  __fmul2_rn(make_float2(__uint_as_float(o[2 * e]), __uint_as_float(o[2 * e + 1])), il2);
+              pko[e] = pack_bf16(v.x, v.y);
+            }
+            if (live) {
+              uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                dst[e] = make_uint4(pko[4 * e], pko[4 * e + 1], pko[4 * e + 2], pko[4 * e + 3]);
+            }
           }
-        }
-        if (live) {
-          const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
-          args.lse[static_cast<size_t>(bh) * N + row] =
-              l > 0.f ? (m_use + log2f(l)) * kLn2 : -INFINITY;
+          if (live) args.lse[static_cast<size_t>(bh) * Nq + row] = lse_row;
         }
       }
+    } else if (ok && n_mine == 0 && args.split_mode && live) {
+      // no key of this split is visible to the tile: an empty partial state
+      float4* dst = reinterpret_cast<float4*>(args.part_o + prow * D);
+#pragma unroll
+      for (int e = 0; e < D / 4; ++e) dst[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+      args.part_lse[prow] = -INFINITY;
     }
   }
 
@@ -479,43 +625,131 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0 && *abort_flag) atomicExch(args.status, kStatusTimeout);
 }
 
+// Merges the fp32 partial states of a split key range ("FlashAttention --
+// the same attention, made memory-aware", section 03: rescale each part by
+// exp(m_part - m_new) and sum). In the saved-statistic form a part is
+// (O_s, LSE_s) and the result is LSE = log sum_s exp(LSE_s),
+// O = sum_s exp(LSE_s - LSE) O_s. One thread per 8 columns of a row.
 template <int D>
-int launch_fwd_d(const Problem& p, void* o, float* lse, cudaStream_t stream) {
+__global__ void __launch_bounds__(256) fa_merge_splits(const float* __restrict__ part_o,
+                                                       const float* __restrict__ part_lse,
+                                                       __nv_bfloat16* __restrict__ o,
+                                                       float* __restrict__ lse, int Nq, int BH,
+                                                       int n_splits) {
+  constexpr int kTpr = D / 8;
+  constexpr int kRowsPerCta = 256 / kTpr;
+  const int row = blockIdx.x * kRowsPerCta + threadIdx.x / kTpr;
+  if (row >= Nq) return;
+  const int c = (threadIdx.x % kTpr) * 8;
+  for (int bh = blockIdx.y; bh < BH; bh += gridDim.y) {
+    float m = -INFINITY;
+    for (int s = 0; s < n_splits; ++s)
+      m = fmaxf(m, part_lse[(static_cast<size_t>(s) * BH + bh) * Nq + row]);
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    float sum = 0.f;
+    if (m != -INFINITY) {
+      for (int s = 0; s < n_splits; ++s) {
+        const size_t pr = (static_cast<size_t>(s) * BH + bh) * Nq + row;
+        const float ls = part_lse[pr];
+        if (ls == -INFINITY) continue;
+        const float w = __expf(ls - m);
+        sum += w;
+        const float4 a = *reinterpret_cast<const float4*>(part_o + pr * D + c);
+        const float4 b = *reinterpret_cast<const float4*>(part_o + pr * D + c + 4);
+        acc[0] = fmaf(w, a.x, acc[0]); acc[1] = fmaf(w, a.y, acc[1]);
+        acc[2] = fmaf(w, a.z, acc[2]); acc[3] = fmaf(w, a.w, acc[3]);
+        acc[4] = fmaf(w, b.x, acc[4]); acc[5] = fmaf(w, b.y, acc[5]);
+        acc[6] = fmaf(w, b.z, acc[6]); acc[7] = fmaf(w, b.w, acc[7]);
+      }
+    }
+    const float inv = sum > 0.f ? 1.0f / sum : 0.f;
+    const size_t orow = static_cast<size_t>(bh) * Nq + row;
+    *reinterpret_cast<uint4*>(o + orow * D + c) =
+        make_uint4(pack_bf16(acc[0] * inv, acc[1] * inv), pack_bf16(acc[2] * inv, acc[3] * inv),
+                   pack_bf16(acc[4] * inv, acc[5] * inv), pack_bf16(acc[6] * inv, acc[7] * inv));
+    if (c == 0) lse[orow] = sum > 0.f ? m + logf(sum) : -INFINITY;
+  }
+}
+
+template <int D>
+int launch_fwd_d(const FwdProblem& p, void* o, float* lse, float* part_o, float* part_lse,
+                 int n_splits, cudaStream_t stream) {
   using C = FwdCfg<D>;
   const int BH = p.B * p.H;
   CUtensorMap mq, mk, mv;
-  if (!make_map_bhnd(&mq, p.q, BH, p.N, D) || !make_map_bhnd(&mk, p.k, BH, p.N, D) ||
-      !make_map_bhnd(&mv, p.v, BH, p.N, D))
+  if (!make_map_bhnd(&mq, p.q, BH, p.Nq, D) || !make_map_bhnd(&mk, p.k, BH, p.Nk, D) ||
+      !make_map_bhnd(&mv, p.v, BH, p.Nk, D))
     return -3;
   int* status = device_status_word();
   if (!status) return -3;
   auto kern = fa_fwd_kernel<D>;
   if (!ensure_smem_attr(reinterpret_cast<const void*>(kern), C::kSmemBytes, D == 64 ? 0 : 1))
     return -3;
+  const int n_kv = (p.Nk + kBlockN - 1) / kBlockN;
+  if (n_splits < 1) n_splits = 1;
+  if (n_splits > n_kv) n_splits = n_kv;
+  const int split_tiles = (n_kv + n_splits - 1) / n_splits;
+  n_splits = (n_kv + split_tiles - 1) / split_tiles;  // no empty trailing split
   FwdArgs a;
   a.o = static_cast<__nv_bfloat16*>(o);
   a.lse = lse;
+  a.part_o = part_o;
+  a.part_lse = part_lse;
   a.status = status;
-  a.N = p.N;
+  a.Nq = p.Nq;
+  a.Nk = p.Nk;
+  a.kv_off = p.Nk - p.Nq;
+  a.window = p.window;
   a.BH = BH;
   a.causal = p.causal ? 1 : 0;
-  a.num_pairs = (p.N + kBlockM * kQTiles - 1) / (kBlockM * kQTiles);
+  a.num_pairs = (p.Nq + kBlockM * kQTiles - 1) / (kBlockM * kQTiles);
+  a.split_tiles = split_tiles;
+  a.split_mode = part_o != nullptr ? 1 : 0;
   // scale 0 (uniform weights) runs as a tiny positive scale: exp2 of a
   // |value| below 2^-25 rounds to exactly 1 in fp32.
   const float sl2 = p.scale * 1.4426950408889634f;
   a.scale_log2 = sl2 > 1e-30f ? sl2 : 1e-30f;
-  const long long grid = static_cast<long long>(a.num_pairs) * BH;
-  if (grid > 0x7fffffffLL) return -1;
-  kern<<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, a);
-  return cudaGetLastError() == cudaSuccess ? 0 : -3;
+  const long long gx = static_cast<long long>(a.num_pairs) * BH;
+  if (gx > 0x7fffffffLL || n_splits > 65535) return -1;
+  const dim3 grid(static_cast<unsigned>(gx), a.split_mode ? n_splits : 1);
+  kern<<<grid, kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, a);
+  if (cudaGetLastError() != cudaSuccess) return -3;
+  if (a.split_mode) {
+    constexpr int kRowsPerCta = 256 / (D / 8);
+    const dim3 mgrid((p.Nq + kRowsPerCta - 1) / kRowsPerCta, BH < 65535 ? BH : 65535);
+    fa_merge_splits<D><<<mgrid, 256, 0, stream>>>(part_o, part_lse, static_cast<__nv_bfloat16*>(o),
+                                                   lse, p.Nq, BH, n_splits);
+    if (cudaGetLastError() != cudaSuccess) return -3;
+  }
+  return 0;
 }
 
 }  // namespace
 
-int launch_fwd(const Problem& p, void* o, float* lse, cudaStream_t stream) {
-  if (p.d == 64) return launch_fwd_d<64>(p, o, lse, stream);
-  if (p.d == 128) return launch_fwd_d<128>(p, o, lse, stream);
+int fwd_split_count(const FwdProblem& p, int n_splits, int sms) {
+  const int n_kv = (p.Nk + kBlockN - 1) / kBlockN;
+  if (n_splits <= 0) {
+    // enough CTAs for about two per SM, with at least two key tiles per split
+    const long long ctas = static_cast<long long>((p.Nq + 255) / 256) * p.B * p.H;
+    long long s = (2LL * sms + ctas - 1) / ctas;
+    if (s > n_kv / 2) s = n_kv / 2;
+    n_splits = s < 1 ? 1 : static_cast<int>(s);
+  }
+  if (n_splits > n_kv) n_splits = n_kv;
+  const int split_tiles = (n_kv + n_splits - 1) / n_splits;
+  return (n_kv + split_tiles - 1) / split_tiles;
+}
+
+int launch_fwd_general(const FwdProblem& p, void* o, float* lse, float* part_o, float* part_lse,
+                       int n_splits, cudaStream_t stream) {
+  if (p.d == 64) return launch_fwd_d<64>(p, o, lse, part_o, part_lse, n_splits, stream);
+  if (p.d == 128) return launch_fwd_d<128>(p, o, lse, part_o, part_lse, n_splits, stream);
   return -2;
+}
+
+int launch_fwd(const Problem& p, void* o, float* lse, cudaStream_t stream) {
+  FwdProblem g{p.q, p.k, p.v, p.B, p.H, p.N, p.N, p.d, p.causal, 0, p.scale};
+  return launch_fwd_general(g, o, lse, nullptr, nullptr, 1, stream);
 }
 
 }  // namespace fa

@@ -18,6 +18,18 @@ struct Problem {
   float scale;
 };
 
+// Forward problem with Nq queries over Nk keys (causal queries are the last
+// Nq positions) and an optional left window of `window` keys.
+struct FwdProblem {
+  const void* q;
+  const void* k;
+  const void* v;
+  int B, H, Nq, Nk, d;
+  int causal;
+  int window;
+  float scale;
+};
+
 // Encodes a 3-D tiled TMA map over a bf16 [BH, N, d] tensor with boxes of
 // 128 rows x 64 columns and 128-byte swizzle. Returns false on failure.
 bool make_map_bhnd(CUtensorMap* map, const void* ptr, int BH, int N, int d);
@@ -32,6 +44,15 @@ int* device_status_word();
 bool ensure_smem_attr(const void* func, int bytes, int slot);
 
 int launch_fwd(const Problem& p, void* o, float* lse, cudaStream_t stream);
+// part_o / part_lse == nullptr: one pass over the whole key range writing o and
+// lse; otherwise the key range is split into n_splits parts whose fp32 states
+// go to part_o [splits, BH, Nq, d] and part_lse [splits, BH, Nq] and are then
+// merged into o and lse.
+int launch_fwd_general(const FwdProblem& p, void* o, float* lse, float* part_o, float* part_lse,
+                       int n_splits, cudaStream_t stream);
+// The number of splits a split launch uses (n_splits <= 0: chosen from the
+// problem size and the SM count).
+int fwd_split_count(const FwdProblem& p, int n_splits, int sms);
 int launch_bwd_pre(const Problem& p, const void* o, const float* lse, const void* dO,
                    void* workspace, cudaStream_t stream);
 int launch_bwd_main(const Problem& p, const void* dO, void* dk, void* dv, void* workspace,

@@ -156,6 +156,52 @@ int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, c
 /* Workspace bytes fa_bwd_stream needs for these sizes (0 when empty). */
 size_t fa_bwd_workspace_bytes(int B, int H, int N, int d);
 
+/*
+ * Extended forward: Nq queries over Nk keys, optional sliding window.
+ *   q       : in,  bf16 [B,H,Nq,d]
+ *   k, v    : in,  bf16 [B,H,Nk,d]   (e.g. a key/value cache)
+ *   o       : out, bf16 [B,H,Nq,d]
+ *   lse     : out, fp32 [B,H,Nq]     natural-log log-sum-exp of each row
+ * With causal != 0 the queries are the last Nq positions of the Nk keys:
+ * query i sits at position p = i + Nk - Nq and sees keys j <= p (Nq <= Nk
+ * required). window = W >= 1 (causal only) further keeps only the keys
+ * p - W < j <= p; window = 0 means no window. Key tiles wholly outside a
+ * query tile's range are neither loaded nor multiplied.
+ * Sources: "Flash Attention: IO-Aware Exact Attention", section "What
+ * changes in FlashAttention-2" (KV caching for decode-time history;
+ * sliding-window attention changes which historical keys participate);
+ * "FlashAttention -- the same attention, made memory-aware", section 00
+ * (the causal mask).
+ * Errors as fa_fwd; additionally FA_ERR_INVALID for window < 0, a window
+ * without causal, Nk = 0 with Nq > 0, or causal with Nq > Nk.
+ */
+int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+              int Nq, int Nk, int d, int causal, int window, float scale, void* cuda_stream);
+
+/*
+ * Split-key-range forward for decode (few queries over a long key/value
+ * cache): the keys are cut into n_splits contiguous ranges of whole 128-key
+ * tiles, each (range, batch-head) is reduced by its own CTA to a partial
+ * state (fp32 output normalised within the range, and its LSE), and a second
+ * kernel merges the parts with the rule of "FlashAttention -- the same
+ * attention, made memory-aware", section 03 (rescale each part by
+ * exp(m_part - m_new) and sum): LSE = log sum_s exp(LSE_s),
+ * O = sum_s exp(LSE_s - LSE) O_s. Arguments and masks as fa_fwd_ex.
+ *   n_splits  : requested number of ranges; <= 0 chooses one from the
+ *               problem size and the device's SM count; clamped to the
+ *               number of key tiles (fa_decode_num_splits gives the count
+ *               actually used).
+ *   workspace : device memory of at least fa_decode_workspace_bytes(...)
+ *               bytes, 256-byte aligned, owned by the caller (partial
+ *               outputs [splits,B,H,Nq,d] fp32 then partial LSE
+ *               [splits,B,H,Nq] fp32); FA_ERR_WORKSPACE otherwise.
+ */
+int fa_decode_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                      int H, int Nq, int Nk, int d, int causal, int window, float scale,
+                      int n_splits, void* workspace, size_t ws_bytes, void* cuda_stream);
+int fa_decode_num_splits(int B, int H, int Nq, int Nk, int d, int n_splits);
+size_t fa_decode_workspace_bytes(int B, int H, int Nq, int Nk, int d, int n_splits);
+
 /* Static description of a return code. Never NULL. */
 const char* fa_strerror(int code);
 
