@@ -57,6 +57,7 @@ SIGNATURES = {
     "fa_bwd_finish_stream": (_I, [_P, _I, _I, _I, _I, _P, _S, _P]),
     "fa_bwd_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P]),
     "fa_bwd_workspace_bytes": (_S, [_I, _I, _I, _I]),
+    "fa_bwd_ex": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _S, _P]),
     "fa_fwd_ex": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P]),
     "fa_decode_splitkv": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P, _S, _P]),
     "fa_decode_num_splits": (_I, [_I, _I, _I, _I, _I, _I]),
@@ -298,3 +299,31 @@ def fa_decode_splitkv(q, k, v, causal: bool = False, window: int = 0, scale: flo
                                    ctypes.c_size_t(workspace.numel()), _stream_handle(stream, q.device))
     _check(rc, "fa_decode_splitkv")
     return out, lse
+
+
+def fa_bwd_ex(q, k, v, o, lse, do, causal: bool = False, window: int = 0,
+              scale: float | None = None, dq=None, dk=None, dv=None, workspace=None, stream=None):
+    """Backward with an optional causal sliding window; returns (dq, dk, dv)."""
+    import torch
+    if q.dim() != 4:
+        raise ValueError("q must be [B, H, N, d]")
+    B, H, N, d = q.shape
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("do", do)):
+        _check_tensor(t, name, (B, H, N, d), torch.bfloat16)
+    _check_tensor(lse, "lse", (B, H, N), torch.float32)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    lib = load_library()
+    need = lib.fa_bwd_workspace_bytes(B, H, N, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    with torch.cuda.device(q.device):
+        rc = lib.fa_bwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do), _ptr(dq),
+                           _ptr(dk), _ptr(dv), B, H, N, d, int(bool(causal)), int(window),
+                           float(scale), _ptr(workspace), ctypes.c_size_t(workspace.numel()),
+                           _stream_handle(stream, q.device))
+    _check(rc, "fa_bwd_ex")
+    return dq, dk, dv

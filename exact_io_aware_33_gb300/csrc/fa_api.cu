@@ -244,6 +244,23 @@ int fa_bwd_stream(const void* q, const void* k, const void* v, const void* o, co
   return rc;
 }
 
+int fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const float* lse,
+              const void* dO, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+              int causal, int window, float scale, void* workspace, size_t ws_bytes,
+              void* cuda_stream) {
+  if (window < 0 || (window > 0 && !causal)) return FA_ERR_INVALID;
+  bool empty = false;
+  int rc = check_bwd(B, H, N, d, scale, {q, k, v, o, lse, dO, dq, dk, dv}, workspace, ws_bytes,
+                     &empty);
+  if (rc != FA_OK || empty) return rc;
+  const cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+  Problem p{q, k, v, B, H, N, d, causal, scale, window};
+  rc = fa::launch_bwd_pre(p, o, lse, dO, workspace, st);
+  if (rc == FA_OK) rc = fa::launch_bwd_main(p, dO, dk, dv, workspace, st);
+  if (rc == FA_OK) rc = fa::launch_bwd_post(p, dq, workspace, st);
+  return rc;
+}
+
 int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
            const void* dO, void* dq, void* dk, void* dv, int B, int H, int N, int d, int causal,
            float scale) {

@@ -34,6 +34,7 @@
 // reduction from a bank-conflict-free shared staging tile.
 
 #include <cuda_bf16.h>
+#include <type_traits>
 #include <cuda_runtime.h>
 
 #include "fa.h"
@@ -57,10 +58,40 @@ struct BwdArgs {
   int n_pad;
   int BH;
   int causal;
+  int window;          // 0 = none; else (causal) keys j <= i - window are masked
   int n_blocks;
   float scale;
   float scale_log2;
 };
+
+// One past the last query block that sees a key of key block jb: with a
+// window W the queries of block i reach back W - 1 positions, so only blocks
+// with a query before jb*128 + 127 + W remain.
+__device__ __forceinline__ int bwd_query_blocks_end(const BwdArgs& a, int jb) {
+  if (!a.window) return a.n_blocks;
+  const int last_query = jb * kBlk + kBlk - 1 + a.window - 1;
+  const int end = last_query / kBlk + 1;
+  return end < a.n_blocks ? end : a.n_blocks;
+}
+
+// Mask of the recomputed probabilities of key block jb against query block
+// i, for the key at row key_row of the block: with d = query - key position,
+// causal drops d < 0 and a window of W drops d >= W, i.e. the query column
+// qc (within the block) is visible iff qc_lo <= qc < qc_hi. Only blocks that
+// straddle a boundary (active) need the per-element test.
+struct RowMask {
+  int qc_lo, qc_hi;
+  bool active;
+};
+__device__ __forceinline__ RowMask bwd_row_mask(const BwdArgs& a, int i, int jb, int key_row) {
+  RowMask m;
+  const int delta = (i - jb) * kBlk;  // query position minus key position at qc = key_row
+  // smallest and largest d in the block: delta - 127 and delta + 127
+  m.active = (a.causal && delta < kBlk - 1) || (a.window && delta + kBlk - 1 >= a.window);
+  m.qc_lo = a.causal ? key_row - delta : -(1 << 30);
+  m.qc_hi = a.window ? key_row - delta + a.window : (1 << 30);
+  return m;
+}
 
 // Index (in floats) of dQ accumulator element (bh, row n, column c); c is
 // a multiple of 4 when the caller accesses 16 bytes.
@@ -228,7 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int bh = blockIdx.x % args.BH;
   const int jb = static_cast<int>(blockIdx.x / args.BH);  // key block (heaviest first)
   const int i0 = args.causal ? jb : 0;
-  const int n_steps = args.n_blocks - i0;
+  const int n_steps = bwd_query_blocks_end(args, jb) - i0;
   const int warp = warp_id();
   const int lane = lane_id();
 
@@ -396,7 +427,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
-      const bool diag = args.causal && it == 0;
+      const RowMask rm = bwd_row_mask(args, i0 + it, jb, key_row);
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         uint32_t sr[32], dr[32];
@@ -414,9 +445,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float2 a = __ffma2_rn(make_float2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])),
                                       sl2x2, nl);
           float2 p = make_float2(ex2(a.x), ex2(a.y));
-          if (diag) {  // causal diagonal block: query before key is masked
-            if (qc < key_row) p.x = 0.f;
-            if (qc + 1 < key_row) p.y = 0.f;
+          if (rm.active) {  // causal diagonal or window boundary block
+            if (qc < rm.qc_lo || qc >= rm.qc_hi) p.x = 0.f;
+            if (qc + 1 < rm.qc_lo || qc + 1 >= rm.qc_hi) p.y = 0.f;
           }
           const float2 g = __fmul2_rn(
               p, __fadd2_rn(make_float2(__uint_as_float(dr[e]), __uint_as_float(dr[e + 1])), nd));
@@ -597,7 +628,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int bh = blockIdx.x % args.BH;
   const int jb = static_cast<int>(blockIdx.x / args.BH);  // key block (heaviest first)
   const int i0 = args.causal ? jb : 0;
-  const int n_steps = args.n_blocks - i0;
+  const int n_steps = bwd_query_blocks_end(args, jb) - i0;
   const int warp = warp_id();
   const int lane = lane_id();
 
@@ -775,9 +806,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       mbar_arrive(bar(kBarSFree));
 
+      const RowMask rm = bwd_row_mask(args, i0 + it, jb, key_row);
+      const bool win = args.window != 0 && rm.active;
       const bool diag = args.causal && it == 0;
       uint32_t pp[32], dd[32];
-      auto half = [&](const uint32_t (&sr)[32], const uint32_t (&dr)[32], int c) {
+      // kind 0: no mask; 1: causal diagonal block; 2: window boundary block.
+      // A compile-time kind keeps the unmasked blocks free of per-element tests.
+      auto half = [&](auto kind, const uint32_t (&sr)[32], const uint32_t (&dr)[32], int c) {
+        constexpr int kKind = decltype(kind)::value;
 #pragma unroll
         for (int e = 0; e < 32; e += 4) {
           const int ql = c * 32 + e;     // query column within this warpgroup's half
@@ -792,7 +828,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float2 a = __ffma2_rn(make_float2(__uint_as_float(sr[x]), __uint_as_float(sr[x + 1])),
                                         sl2x2, nl2);
             float2 p = make_float2(ex2(a.x), ex2(a.y));
-            if (diag) {  // causal diagonal block: a query before the key is masked
+            if constexpr (kKind == 2) {  // window boundary (or causal diagonal) block
+              const int q0 = qc + 2 * u;
+              if (q0 < rm.qc_lo || q0 >= rm.qc_hi) p.x = 0.f;
+              if (q0 + 1 < rm.qc_lo || q0 + 1 >= rm.qc_hi) p.y = 0.f;
+            } else if constexpr (kKind == 1) {  // causal diagonal: a query before the key is masked
               if (qc + 2 * u < key_row) p.x = 0.f;
               if (qc + 2 * u + 1 < key_row) p.y = 0.f;
             }
@@ -803,8 +843,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       };
-      half(s0, d0, 0);
-      half(s1, d1, 1);
+      if (win) {
+        half(std::integral_constant<int, 2>{}, s0, d0, 0);
+        half(std::integral_constant<int, 2>{}, s1, d1, 1);
+      } else if (diag) {
+        half(std::integral_constant<int, 1>{}, s0, d0, 0);
+        half(std::integral_constant<int, 1>{}, s1, d1, 1);
+      } else {
+        half(std::integral_constant<int, 0>{}, s0, d0, 0);
+        half(std::integral_constant<int, 0>{}, s1, d1, 1);
+      }
 
       // P^T into its own columns once the previous step's dV MMA has read them
       if (it > 0) {
@@ -970,6 +1018,7 @@ BwdArgs make_args(const Problem& p, const Workspace& w, void* dk, void* dv, int*
   a.n_pad = w.n_pad;
   a.BH = p.B * p.H;
   a.causal = p.causal ? 1 : 0;
+  a.window = p.window;
   a.n_blocks = w.n_pad / kBlk;
   a.scale = p.scale;
   a.scale_log2 = p.scale * kLog2e;

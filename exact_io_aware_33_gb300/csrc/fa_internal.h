@@ -16,6 +16,7 @@ struct Problem {
   int B, H, N, d;
   int causal;
   float scale;
+  int window = 0;  // backward only: 0 = none, else a causal window of this many keys
 };
 
 // Forward problem with Nq queries over Nk keys (causal queries are the last

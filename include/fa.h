@@ -25,7 +25,8 @@
  *  - q, k, v, o, dO, dq, dk, dv: bfloat16, shape [B, H, N, d], contiguous
  *    row-major (d fastest). lse and the backward's D: float32 [B, H, N].
  *  - d must be 64 or 128. N may be any length (ragged tail tiles are
- *    masked); keys and queries have the same length N.
+ *    masked). Keys and queries have the same length N, except in
+ *    fa_fwd_ex and fa_decode_splitkv, which take Nq queries over Nk keys.
  *  - causal != 0 masks key j for query i when j > i (the diagonal is
  *    visible). scale multiplies Q K^T before masking and softmax; it must be
  *    finite and >= 0 (0 gives uniform weights over the visible keys).
@@ -103,9 +104,10 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
  * fa_bwd on `cuda_stream` with a caller-provided device workspace of at
  * least fa_bwd_workspace_bytes(B,H,N,d) bytes, 256-byte aligned. The
  * workspace holds D = rowsum(dO * O) and the LSE in log2 units (fp32, each
- * over N rounded up to 128 per head) and the fp32 dQ accumulator
- * ([B,H,N,d]); its contents on entry do not matter and on return are
- * unspecified. Two calls in flight at once need two workspaces.
+ * over N rounded up to 128 per head) and the fp32 dQ accumulator (the same
+ * padded rows x d, in a blocked layout of the library's choosing); its
+ * contents on entry do not matter and on return are unspecified. Two calls
+ * in flight at once need two workspaces.
  */
 int fa_bwd_stream(const void* q, const void* k, const void* v, const void* o, const float* lse,
                   const void* dO, void* dq, void* dk, void* dv, int B, int H, int N, int d,
@@ -177,6 +179,18 @@ size_t fa_bwd_workspace_bytes(int B, int H, int N, int d);
  */
 int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
               int Nq, int Nk, int d, int causal, int window, float scale, void* cuda_stream);
+
+/*
+ * Backward of fa_fwd_ex for training (Nq = Nk = N) with an optional causal
+ * sliding window of `window` keys (0 = none): arguments, workspace and
+ * results as fa_bwd_stream. Key/value blocks skip the query blocks that
+ * see none of their keys, and the boundary blocks are masked per element.
+ * FA_ERR_INVALID for window < 0 or a window without causal.
+ */
+int fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const float* lse,
+              const void* dO, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+              int causal, int window, float scale, void* workspace, size_t ws_bytes,
+              void* cuda_stream);
 
 /*
  * Split-key-range forward for decode (few queries over a long key/value
