@@ -72,6 +72,95 @@ def measured_peaks():
         return FALLBACK_PEAK_TFLOPS, 1700.0, "fallback"
 
 
+def measured_hbm_gbs():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def window_pairs(N, window):
+    """Visible (query, key) pairs of one head under a causal window."""
+    w = min(window, N)
+    return w * (w + 1) // 2 + (N - w) * w
+
+
+def time_calls(fn, reps, warmup, stream, flush=None):
+    """Median ms of fn() over `reps` launches on `stream` (CUDA events)."""
+    import statistics
+    import torch
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(reps):
+        if flush is not None:
+            flush()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b))
+    return statistics.median(ts)
+
+
+def decode_leg(dev, stream, reps=20):
+    """Split-key-range decode: 8 sequences x 32 heads, one query over 32768
+    cached keys (d = 128, causal). HBM-bound: every key and value is read
+    once; the roofline counts K, V, Q, O and the fp32 partial states."""
+    import torch
+    import exact_io_aware_33_gb300 as fa
+    B, H, Nq, Nk, d = 8, 32, 1, 32768, 128
+    # drawn on the device (seeded): 2 x 1 G values would take long on the host
+    g = torch.Generator(device=dev).manual_seed(4242)
+    q = torch.randn(B, H, Nq, d, generator=g, device=dev).to(torch.bfloat16)
+    k = torch.randn(B, H, Nk, d, generator=g, device=dev).to(torch.bfloat16)
+    v = torch.randn(B, H, Nk, d, generator=g, device=dev).to(torch.bfloat16)
+    o = torch.empty_like(q)
+    lse = torch.empty(B, H, Nq, dtype=torch.float32, device=dev)
+    splits = fa.fa_decode_num_splits(B, H, Nq, Nk, d, 0)
+    ws = torch.empty(fa.fa_decode_workspace_bytes(B, H, Nq, Nk, d, 0), dtype=torch.uint8, device=dev)
+    with torch.cuda.stream(stream):
+        ms = time_calls(lambda: fa.fa_decode_splitkv(q, k, v, causal=True, n_splits=0, out=o, lse=lse,
+                                                     workspace=ws, stream=stream), reps, 3, stream)
+    part = splits * B * H * Nq * (d + 1) * 4
+    algo = 2 * B * H * Nk * d * 2 + 2 * B * H * Nq * d * 2 + B * H * Nq * 4 + 2 * part
+    peak, src = measured_hbm_gbs()
+    gbs = algo / (ms * 1e-3) / 1e9
+    return {"workload": "decode_b8h32_nq1_nk32768_d128_causal", "splits": splits, "ms": round(ms, 4),
+            "bytes": algo, "gbs": round(gbs, 1), "peak_gbs": peak, "frac": round(gbs / peak, 4),
+            "bound": "hbm", "peak_source": f"{src} copy bandwidth (MEASURED_PEAKS.json)",
+            "l2": "inputs (4.3 GB) larger than L2"}
+
+
+def window_leg(dev, stream, flush, reps=10):
+    """Causal sliding window W = 1024 on B=1 H=16 N=8192 d=128: forward and
+    backward; FLOPs count visible pairs only (4 d per pair forward, 2.5x
+    that backward)."""
+    import torch
+    import exact_io_aware_33_gb300 as fa
+    B, H, N, d, W = 1, 16, 8192, 128, 1024
+    x = si.make_small(B, H, N, d, seed=77, with_grad=True)
+    q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "do"))
+    o = torch.empty_like(q)
+    lse = torch.empty(B, H, N, dtype=torch.float32, device=dev)
+    dq, dk, dv = (torch.empty_like(q) for _ in range(3))
+    ws = torch.empty(fa.fa_bwd_workspace_bytes(B, H, N, d), dtype=torch.uint8, device=dev)
+    with torch.cuda.stream(stream):
+        ms_f = time_calls(lambda: fa.fa_fwd_ex(q, k, v, causal=True, window=W, out=o, lse=lse,
+                                               stream=stream), reps, 3, stream, flush)
+        ms_b = time_calls(lambda: fa.fa_bwd_ex(q, k, v, o, lse, do, causal=True, window=W, dq=dq,
+                                               dk=dk, dv=dv, workspace=ws, stream=stream),
+                          reps, 3, stream, flush)
+    f_fwd = 4.0 * d * B * H * window_pairs(N, W)
+    return {"workload": "window_causal_b1h16_n8192_d128_w1024", "fwd_ms": round(ms_f, 4),
+            "fwd_tflops": round(f_fwd / (ms_f * 1e-3) / 1e12, 1), "bwd_ms": round(ms_b, 4),
+            "bwd_tflops": round(2.5 * f_fwd / (ms_b * 1e-3) / 1e12, 1),
+            "note": "backward = preprocess + main + finish"}
+
+
 def max_over_ranks(values, device, world):
     """Element-wise maximum of per-rank floats (the slowest rank's times)."""
     if world <= 1:
@@ -427,6 +516,8 @@ def run_ours(args):
         out["fwd_long"] = {"workload": wl.name, "ms": round(ms_l, 4), "tflops": round(tf_l, 1),
                            "frac": round(tf_l / peak, 4)}
         del rl
+        out["decode"] = decode_leg(dev, stream)
+        out["window"] = window_leg(dev, stream, runner.flush_l2)
         if world == 1:
             out["cpu_baseline"] = cpu_baseline(w)
     print(json.dumps(out), flush=True)

@@ -729,11 +729,28 @@ int launch_fwd_d(const FwdProblem& p, void* o, float* lse, float* part_o, float*
 int fwd_split_count(const FwdProblem& p, int n_splits, int sms) {
   const int n_kv = (p.Nk + kBlockN - 1) / kBlockN;
   if (n_splits <= 0) {
-    // enough CTAs for about two per SM, with at least two key tiles per split
+    // One CTA per SM at a time: pick the smallest split count that gives at
+    // least two CTAs per SM and fills the last wave to 90 % or more (the
+    // best-filled count otherwise), keeping at least four key tiles per split.
     const long long ctas = static_cast<long long>((p.Nq + 255) / 256) * p.B * p.H;
-    long long s = (2LL * sms + ctas - 1) / ctas;
-    if (s > n_kv / 2) s = n_kv / 2;
-    n_splits = s < 1 ? 1 : static_cast<int>(s);
+    const int s_max = n_kv / 4 > 1 ? n_kv / 4 : 1;
+    int best = 1;
+    double best_fill = 0.0;
+    for (int s = 1; s <= s_max && s <= 256; ++s) {
+      const int tiles = (n_kv + s - 1) / s, eff_s = (n_kv + tiles - 1) / tiles;
+      if (eff_s != s) continue;  // would leave an empty trailing split
+      const double waves = static_cast<double>(ctas * s) / sms;
+      const double fill = waves / static_cast<double>(static_cast<long long>(waves + 0.999999));
+      if (waves >= 2.0 && fill >= 0.9) {
+        best = s;
+        break;
+      }
+      if (fill > best_fill + 1e-9) {
+        best_fill = fill;
+        best = s;
+      }
+    }
+    n_splits = best;
   }
   if (n_splits > n_kv) n_splits = n_kv;
   const int split_tiles = (n_kv + n_splits - 1) / n_splits;
