@@ -120,7 +120,7 @@ def decode_leg(dev, stream, reps=20):
     v = torch.randn(B, H, Nk, d, generator=g, device=dev).to(torch.bfloat16)
     o = torch.empty_like(q)
     lse = torch.empty(B, H, Nq, dtype=torch.float32, device=dev)
-    splits = fa.fa_decode_num_splits(B, H, Nq, Nk, d, 0)
+    splits = fa.fa_decode_num_splits(B, H, Nq, Nk, 0)
     ws = torch.empty(fa.fa_decode_workspace_bytes(B, H, Nq, Nk, d, 0), dtype=torch.uint8, device=dev)
     with torch.cuda.stream(stream):
         ms = time_calls(lambda: fa.fa_decode_splitkv(q, k, v, causal=True, n_splits=0, out=o, lse=lse,

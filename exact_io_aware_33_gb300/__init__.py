@@ -57,10 +57,10 @@ SIGNATURES = {
     "fa_bwd_finish_stream": (_I, [_P, _I, _I, _I, _I, _P, _S, _P]),
     "fa_bwd_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P]),
     "fa_bwd_workspace_bytes": (_S, [_I, _I, _I, _I]),
-    "fa_bwd_ex": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _S, _P]),
-    "fa_fwd_ex": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P]),
-    "fa_decode_splitkv": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P, _S, _P]),
-    "fa_decode_num_splits": (_I, [_I, _I, _I, _I, _I, _I]),
+    "fa_bwd_ex": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _S, _P]),
+    "fa_fwd_ex": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F, _P]),
+    "fa_decode_splitkv": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P, _S, _P]),
+    "fa_decode_num_splits": (_I, [_I, _I, _I, _I, _I]),
     "fa_decode_workspace_bytes": (_S, [_I, _I, _I, _I, _I, _I]),
     "fa_strerror": (ctypes.c_char_p, [_I]),
     "fa_get_last_device_status": (_I, []),
@@ -243,59 +243,59 @@ def fa_bwd_noalloc(q, k, v, o, lse, do, causal: bool = False, scale: float | Non
 
 def _fwd_ex_args(q, k, v, causal, window, scale):
     import torch
-    if q.dim() != 4 or k.dim() != 4:
+    if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
         raise ValueError("q, k, v must be [B, H, N, d]")
     B, H, Nq, d = q.shape
-    Nk = k.shape[2]
+    Nk, dv = k.shape[2], v.shape[3]
     _check_tensor(q, "q", (B, H, Nq, d), torch.bfloat16)
     _check_tensor(k, "k", (B, H, Nk, d), torch.bfloat16)
-    _check_tensor(v, "v", (B, H, Nk, d), torch.bfloat16)
+    _check_tensor(v, "v", (B, H, Nk, dv), torch.bfloat16)
     if scale is None:
         scale = 1.0 / math.sqrt(d)
-    return B, H, Nq, Nk, d, int(bool(causal)), int(window), float(scale)
+    return B, H, Nq, Nk, d, dv, int(bool(causal)), int(window), float(scale)
 
 
 def fa_fwd_ex(q, k, v, causal: bool = False, window: int = 0, scale: float | None = None,
               out=None, lse=None, stream=None):
     """Forward with Nq queries over Nk keys and an optional window; (o, lse)."""
     import torch
-    B, H, Nq, Nk, d, c, w, sc = _fwd_ex_args(q, k, v, causal, window, scale)
-    out = torch.empty_like(q) if out is None else out
+    B, H, Nq, Nk, d, dv, c, w, sc = _fwd_ex_args(q, k, v, causal, window, scale)
+    out = torch.empty((B, H, Nq, dv), dtype=torch.bfloat16, device=q.device) if out is None else out
     lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device) if lse is None else lse
-    _check_tensor(out, "out", (B, H, Nq, d), torch.bfloat16)
+    _check_tensor(out, "out", (B, H, Nq, dv), torch.bfloat16)
     _check_tensor(lse, "lse", (B, H, Nq), torch.float32)
     lib = load_library()
     with torch.cuda.device(q.device):
-        rc = lib.fa_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, Nq, Nk, d, c, w,
-                           sc, _stream_handle(stream, q.device))
+        rc = lib.fa_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, Nq, Nk, d, dv, c,
+                           w, sc, _stream_handle(stream, q.device))
     _check(rc, "fa_fwd_ex")
     return out, lse
 
 
-def fa_decode_num_splits(B: int, H: int, Nq: int, Nk: int, d: int, n_splits: int = 0) -> int:
-    return load_library().fa_decode_num_splits(B, H, Nq, Nk, d, n_splits)
+def fa_decode_num_splits(B: int, H: int, Nq: int, Nk: int, n_splits: int = 0) -> int:
+    return load_library().fa_decode_num_splits(B, H, Nq, Nk, n_splits)
 
 
-def fa_decode_workspace_bytes(B: int, H: int, Nq: int, Nk: int, d: int, n_splits: int = 0) -> int:
-    return load_library().fa_decode_workspace_bytes(B, H, Nq, Nk, d, n_splits)
+def fa_decode_workspace_bytes(B: int, H: int, Nq: int, Nk: int, dv: int, n_splits: int = 0) -> int:
+    return load_library().fa_decode_workspace_bytes(B, H, Nq, Nk, dv, n_splits)
 
 
 def fa_decode_splitkv(q, k, v, causal: bool = False, window: int = 0, scale: float | None = None,
                       n_splits: int = 0, out=None, lse=None, workspace=None, stream=None):
     """Split-key-range forward (decode over a long key/value cache); (o, lse)."""
     import torch
-    B, H, Nq, Nk, d, c, w, sc = _fwd_ex_args(q, k, v, causal, window, scale)
-    out = torch.empty_like(q) if out is None else out
+    B, H, Nq, Nk, d, dv, c, w, sc = _fwd_ex_args(q, k, v, causal, window, scale)
+    out = torch.empty((B, H, Nq, dv), dtype=torch.bfloat16, device=q.device) if out is None else out
     lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device) if lse is None else lse
-    _check_tensor(out, "out", (B, H, Nq, d), torch.bfloat16)
+    _check_tensor(out, "out", (B, H, Nq, dv), torch.bfloat16)
     _check_tensor(lse, "lse", (B, H, Nq), torch.float32)
     lib = load_library()
-    need = lib.fa_decode_workspace_bytes(B, H, Nq, Nk, d, n_splits)
+    need = lib.fa_decode_workspace_bytes(B, H, Nq, Nk, dv, n_splits)
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
     with torch.cuda.device(q.device):
         rc = lib.fa_decode_splitkv(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, Nq, Nk,
-                                   d, c, w, sc, int(n_splits), _ptr(workspace),
+                                   d, dv, c, w, sc, int(n_splits), _ptr(workspace),
                                    ctypes.c_size_t(workspace.numel()), _stream_handle(stream, q.device))
     _check(rc, "fa_decode_splitkv")
     return out, lse
@@ -308,8 +308,11 @@ def fa_bwd_ex(q, k, v, o, lse, do, causal: bool = False, window: int = 0,
     if q.dim() != 4:
         raise ValueError("q must be [B, H, N, d]")
     B, H, N, d = q.shape
-    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("do", do)):
+    d_v = v.shape[3]
+    for name, t in (("q", q), ("k", k)):
         _check_tensor(t, name, (B, H, N, d), torch.bfloat16)
+    for name, t in (("v", v), ("o", o), ("do", do)):
+        _check_tensor(t, name, (B, H, N, d_v), torch.bfloat16)
     _check_tensor(lse, "lse", (B, H, N), torch.float32)
     if scale is None:
         scale = 1.0 / math.sqrt(d)
@@ -322,7 +325,7 @@ def fa_bwd_ex(q, k, v, o, lse, do, causal: bool = False, window: int = 0,
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
     with torch.cuda.device(q.device):
         rc = lib.fa_bwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do), _ptr(dq),
-                           _ptr(dk), _ptr(dv), B, H, N, d, int(bool(causal)), int(window),
+                           _ptr(dk), _ptr(dv), B, H, N, d, d_v, int(bool(causal)), int(window),
                            float(scale), _ptr(workspace), ctypes.c_size_t(workspace.numel()),
                            _stream_handle(stream, q.device))
     _check(rc, "fa_bwd_ex")

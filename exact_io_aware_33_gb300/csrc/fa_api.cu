@@ -246,15 +246,16 @@ int fa_bwd_stream(const void* q, const void* k, const void* v, const void* o, co
 
 int fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const float* lse,
               const void* dO, void* dq, void* dk, void* dv, int B, int H, int N, int d,
-              int causal, int window, float scale, void* workspace, size_t ws_bytes,
+              int d_v, int causal, int window, float scale, void* workspace, size_t ws_bytes,
               void* cuda_stream) {
   if (window < 0 || (window > 0 && !causal)) return FA_ERR_INVALID;
+  if (d_v != 64 && d_v != 128) return FA_ERR_UNSUPPORTED;
   bool empty = false;
   int rc = check_bwd(B, H, N, d, scale, {q, k, v, o, lse, dO, dq, dk, dv}, workspace, ws_bytes,
                      &empty);
   if (rc != FA_OK || empty) return rc;
   const cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
-  Problem p{q, k, v, B, H, N, d, causal, scale, window};
+  Problem p{q, k, v, B, H, N, d, causal, scale, window, d_v};
   rc = fa::launch_bwd_pre(p, o, lse, dO, workspace, st);
   if (rc == FA_OK) rc = fa::launch_bwd_main(p, dO, dk, dv, workspace, st);
   if (rc == FA_OK) rc = fa::launch_bwd_post(p, dq, workspace, st);
@@ -285,12 +286,12 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
 namespace {
 
 // Checks of the extended forward forms; sets *empty for B, H or Nq = 0.
-int check_fwd_ex(int B, int H, int Nq, int Nk, int d, int causal, int window, float scale,
+int check_fwd_ex(int B, int H, int Nq, int Nk, int d, int dv, int causal, int window, float scale,
                  std::initializer_list<const void*> ptrs, bool* empty) {
   *empty = false;
   if (B < 0 || H < 0 || Nq < 0 || Nk < 0 || window < 0) return FA_ERR_INVALID;
   if (!std::isfinite(scale) || scale < 0.f) return FA_ERR_INVALID;
-  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if ((d != 64 && d != 128) || (dv != 64 && dv != 128)) return FA_ERR_UNSUPPORTED;
   if (window > 0 && !causal) return FA_ERR_INVALID;
   if (B == 0 || H == 0 || Nq == 0) {
     *empty = true;
@@ -299,7 +300,8 @@ int check_fwd_ex(int B, int H, int Nq, int Nk, int d, int causal, int window, fl
   if (Nk == 0 || (causal && Nq > Nk)) return FA_ERR_INVALID;
   const long long bh = static_cast<long long>(B) * H;
   if (bh > (1LL << 31) - 1) return FA_ERR_INVALID;
-  if (bh * static_cast<long long>(Nq > Nk ? Nq : Nk) * d > (1LL << 46)) return FA_ERR_INVALID;
+  if (bh * static_cast<long long>(Nq > Nk ? Nq : Nk) * (d > dv ? d : dv) > (1LL << 46))
+    return FA_ERR_INVALID;
   for (const void* ptr : ptrs)
     if (!fa::aligned16(ptr)) return FA_ERR_INVALID;
   fa::DeviceState* st = nullptr;
@@ -316,40 +318,41 @@ int sm_count() {
 }  // namespace
 
 int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
-              int Nq, int Nk, int d, int causal, int window, float scale, void* cuda_stream) {
+              int Nq, int Nk, int d, int dv, int causal, int window, float scale,
+              void* cuda_stream) {
   bool empty = false;
-  int rc = check_fwd_ex(B, H, Nq, Nk, d, causal, window, scale, {q, k, v, o, lse}, &empty);
+  int rc = check_fwd_ex(B, H, Nq, Nk, d, dv, causal, window, scale, {q, k, v, o, lse}, &empty);
   if (rc != FA_OK || empty) return rc;
-  fa::FwdProblem p{q, k, v, B, H, Nq, Nk, d, causal, window, scale};
+  fa::FwdProblem p{q, k, v, B, H, Nq, Nk, d, dv, causal, window, scale};
   return fa::launch_fwd_general(p, o, lse, nullptr, nullptr, 1,
                                 static_cast<cudaStream_t>(cuda_stream));
 }
 
-int fa_decode_num_splits(int B, int H, int Nq, int Nk, int d, int n_splits) {
-  if (B <= 0 || H <= 0 || Nq <= 0 || Nk <= 0 || d <= 0) return 0;
-  fa::FwdProblem p{nullptr, nullptr, nullptr, B, H, Nq, Nk, d, 0, 0, 1.f};
+int fa_decode_num_splits(int B, int H, int Nq, int Nk, int n_splits) {
+  if (B <= 0 || H <= 0 || Nq <= 0 || Nk <= 0) return 0;
+  fa::FwdProblem p{nullptr, nullptr, nullptr, B, H, Nq, Nk, 64, 64, 0, 0, 1.f};
   return fa::fwd_split_count(p, n_splits, sm_count());
 }
 
-size_t fa_decode_workspace_bytes(int B, int H, int Nq, int Nk, int d, int n_splits) {
-  const int s = fa_decode_num_splits(B, H, Nq, Nk, d, n_splits);
-  if (s <= 0) return 0;
-  return static_cast<size_t>(s) * B * H * Nq * (static_cast<size_t>(d) + 1) * 4;
+size_t fa_decode_workspace_bytes(int B, int H, int Nq, int Nk, int dv, int n_splits) {
+  const int s = fa_decode_num_splits(B, H, Nq, Nk, n_splits);
+  if (s <= 0 || dv <= 0) return 0;
+  return static_cast<size_t>(s) * B * H * Nq * (static_cast<size_t>(dv) + 1) * 4;
 }
 
 int fa_decode_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B,
-                      int H, int Nq, int Nk, int d, int causal, int window, float scale,
+                      int H, int Nq, int Nk, int d, int dv, int causal, int window, float scale,
                       int n_splits, void* workspace, size_t ws_bytes, void* cuda_stream) {
   bool empty = false;
-  int rc = check_fwd_ex(B, H, Nq, Nk, d, causal, window, scale, {q, k, v, o, lse}, &empty);
+  int rc = check_fwd_ex(B, H, Nq, Nk, d, dv, causal, window, scale, {q, k, v, o, lse}, &empty);
   if (rc != FA_OK || empty) return rc;
-  const size_t need = fa_decode_workspace_bytes(B, H, Nq, Nk, d, n_splits);
+  const size_t need = fa_decode_workspace_bytes(B, H, Nq, Nk, dv, n_splits);
   if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || ws_bytes < need)
     return FA_ERR_WORKSPACE;
-  const int s = fa_decode_num_splits(B, H, Nq, Nk, d, n_splits);
-  fa::FwdProblem p{q, k, v, B, H, Nq, Nk, d, causal, window, scale};
+  const int s = fa_decode_num_splits(B, H, Nq, Nk, n_splits);
+  fa::FwdProblem p{q, k, v, B, H, Nq, Nk, d, dv, causal, window, scale};
   float* part_o = static_cast<float*>(workspace);
-  float* part_lse = part_o + static_cast<size_t>(s) * B * H * Nq * d;
+  float* part_lse = part_o + static_cast<size_t>(s) * B * H * Nq * dv;
   return fa::launch_fwd_general(p, o, lse, part_o, part_lse, s,
                                 static_cast<cudaStream_t>(cuda_stream));
 }

@@ -22,9 +22,9 @@
 //                  dK  += dS^T Q_i          (dS^T read from shared memory)
 //                  dQ_i = dS K_j            (same shared bytes, MN-major)
 //                dQ_i is added into the fp32 accumulator in global memory.
-//                Two variants: fa_bwd_main_d64 (pipelined across query
-//                blocks, dQ added by bulk reductions) and fa_bwd_main_d128
-//                (tensor memory too small to pipeline; see each kernel).
+//                Two variants: fa_bwd_main_d64 (d = d_v = 64: pipelined across
+//                query blocks, dQ added by bulk reductions) and fa_bwd_main_seq
+//                (other head sizes: tensor memory too small to pipeline).
 //   fa_bwd_post  dQ = bf16(accumulator)
 //
 // The dQ accumulator is fp32 [BH, Npad, d] in a blocked layout: each group
@@ -105,17 +105,18 @@ __host__ __device__ __forceinline__ size_t acc_index(long long bh, int n, int c,
 // For every row of the padded [BH, Npad] grid: -D = -sum_c dO[c] * O[c] and
 // -LSE * log2(e) (rows past N get 0 and -inf, so that their recomputed
 // probabilities are exactly 0). Stored negated so the main kernel's packed
-// FMAs take them as addends. Grid (row blocks, BH): one group of D/8 lanes
-// per row, each lane reading 8 bf16 (16 bytes) of both tensors; the CTAs of
-// a head also zero its Npad x D slice of the dQ accumulator.
-template <int D>
+// FMAs take them as addends. Grid (row blocks, BH): one group of DV/8 lanes
+// per row, each lane reading 8 bf16 (16 bytes) of both tensors (O and dO have
+// head size DV); the CTAs of a head also zero their rows of the head's
+// Npad x DQ slice of the dQ accumulator (DQ: head size of Q).
+template <int DV, int DQ>
 __global__ void __launch_bounds__(256) fa_bwd_pre(const __nv_bfloat16* __restrict__ o,
                                                   const __nv_bfloat16* __restrict__ dO,
                                                   const float* __restrict__ lse,
                                                   float* __restrict__ Dvec,
                                                   float* __restrict__ lse2, int N, int n_pad,
                                                   float* __restrict__ dq_acc, int BH) {
-  constexpr int kTpr = D / 8;               // lanes per row (8 or 16)
+  constexpr int kTpr = DV / 8;              // lanes per row (8 or 16)
   constexpr int kRowsPerCta = 256 / kTpr;
   for (int bh = blockIdx.y; bh < BH; bh += gridDim.y) {
   const int sub = threadIdx.x % kTpr;
@@ -125,8 +126,8 @@ __global__ void __launch_bounds__(256) fa_bwd_pre(const __nv_bfloat16* __restric
   float acc = 0.f;
   if (live) {
     const size_t row = head + n;
-    const uint4 a = *reinterpret_cast<const uint4*>(o + row * D + sub * 8);
-    const uint4 b = *reinterpret_cast<const uint4*>(dO + row * D + sub * 8);
+    const uint4 a = *reinterpret_cast<const uint4*>(o + row * DV + sub * 8);
+    const uint4 b = *reinterpret_cast<const uint4*>(dO + row * DV + sub * 8);
     const uint32_t aw[4] = {a.x, a.y, a.z, a.w};
     const uint32_t bw[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
@@ -146,9 +147,9 @@ __global__ void __launch_bounds__(256) fa_bwd_pre(const __nv_bfloat16* __restric
   }
   // zero rows [n0, n0 + kRowsPerCta) of this head's accumulator slice
   float4* z = reinterpret_cast<float4*>(dq_acc + (static_cast<size_t>(bh) * n_pad +
-                                                  static_cast<size_t>(blockIdx.x) * kRowsPerCta) * D);
+                                                  static_cast<size_t>(blockIdx.x) * kRowsPerCta) * DQ);
 #pragma unroll
-  for (int i = threadIdx.x; i < kRowsPerCta * D / 4; i += 256) z[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int i = threadIdx.x; i < kRowsPerCta * DQ / 4; i += 256) z[i] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
 }
 
@@ -172,8 +173,8 @@ __global__ void __launch_bounds__(256) fa_bwd_post(const float* __restrict__ acc
   }
 }
 
-// ---------------------------------------------------------------- B1, d = 128
-// With d = 128 the five accumulators (S^T, dP^T, dQ, dK, dV) need 640
+// ---------------------------------------------------------------- B1, other head sizes
+// With d = 128 (or d_v = 128) the five accumulators (S^T, dP^T, dQ, dK, dV) need 640
 // tensor-memory columns of the 512, so dQ shares the dP^T columns and each
 // query step runs in sequence: S^T / dP^T (one query half at a time), P/dS,
 // dV / dK, then dQ, whose read-out must finish before the next dP^T.
@@ -197,19 +198,22 @@ constexpr int kDqWarp0 = 8;
 constexpr int kMmaWarp = 12;
 constexpr int kLoadWarp = 13;
 
-template <int D>
+// D: head size of Q and K (and of dQ, dK); DV: head size of V and dO (and dV).
+template <int D, int DV>
 struct BwdCfg {
   static constexpr int kChunks = D / 64;
+  static constexpr int kChunksV = DV / 64;
   static constexpr int kChunkBytes = kBlk * 64 * 2;
-  static constexpr int kTileBytes = kChunks * kChunkBytes;
+  static constexpr int kTileBytes = kChunks * kChunkBytes;    // 128 rows x d (K, Q)
+  static constexpr int kVTileBytes = kChunksV * kChunkBytes;  // 128 rows x d_v (V, dO)
   static constexpr int kVecBytes = 2 * kBlk * 4;  // lse2[128], D[128] of one query block
-  static constexpr int kStages = (D == 64) ? 3 : 2;
+  static constexpr int kStages = (D == 64 && DV == 64) ? 3 : 2;
   static constexpr bool kDqAliasDp = (D == 128);
   static constexpr int kKOff = 0;
   static constexpr int kVOff = kKOff + kTileBytes;
-  static constexpr int kDSOff = kVOff + kTileBytes;             // 2 x 16 KiB
+  static constexpr int kDSOff = kVOff + kVTileBytes;            // 2 x 16 KiB
   static constexpr int kStageOff = kDSOff + 2 * kChunkBytes;
-  static constexpr int kStageBytes = 2 * kTileBytes + kVecBytes;  // Q, dO, vectors
+  static constexpr int kStageBytes = kTileBytes + kVTileBytes + kVecBytes;  // Q, dO, vectors
   static constexpr int kBarOff = kStageOff + kStages * kStageBytes;
   static constexpr int kBarKV = 0;
   static constexpr int kBarQFull = 1;
@@ -234,14 +238,15 @@ struct BwdCfg {
   static constexpr uint32_t kColDQ = kDqAliasDp ? 128 : 256;
   static constexpr uint32_t kColDK = kDqAliasDp ? 256 : 320;
   static constexpr uint32_t kColDV = kColDK + D;
+  static_assert(kColDV + DV <= kTmemCols, "backward accumulators exceed tensor memory");
 };
 
-template <int D>
+template <int D, int DV>
 __global__ void __launch_bounds__(kThreads, 1)
-    fa_bwd_main_d128(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+    fa_bwd_main_seq(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                 const BwdArgs args) {
-  using C = BwdCfg<D>;
+  using C = BwdCfg<D, DV>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_u32 = smem_u32(smem_raw);
   const uint32_t base = (raw_u32 + 1023u) & ~1023u;
@@ -296,11 +301,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_map(&tmK);
       tma_prefetch_map(&tmV);
       tma_prefetch_map(&tmDO);
-      mbar_arrive_expect_tx(bar(C::kBarKV), 2 * C::kTileBytes);
-      for (int c = 0; c < C::kChunks; ++c) {
+      mbar_arrive_expect_tx(bar(C::kBarKV), C::kTileBytes + C::kVTileBytes);
+      for (int c = 0; c < C::kChunks; ++c)
         tma_load_3d(base + C::kKOff + c * C::kChunkBytes, &tmK, bar(C::kBarKV), c * 64, jb * kBlk, bh);
+      for (int c = 0; c < C::kChunksV; ++c)
         tma_load_3d(base + C::kVOff + c * C::kChunkBytes, &tmV, bar(C::kBarKV), c * 64, jb * kBlk, bh);
-      }
       int issued = 0;
       bool ok = true;
       for (int it = 0; it < n_steps; ++it) {
@@ -312,13 +317,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t st = base + C::kStageOff + s * C::kStageBytes;
         const uint32_t fb = bar(C::kBarQFull + s);
         mbar_arrive_expect_tx(fb, C::kStageBytes);
-        for (int c = 0; c < C::kChunks; ++c) {
+        for (int c = 0; c < C::kChunks; ++c)
           tma_load_3d(st + c * C::kChunkBytes, &tmQ, fb, c * 64, row0, bh);
+        for (int c = 0; c < C::kChunksV; ++c)
           tma_load_3d(st + C::kTileBytes + c * C::kChunkBytes, &tmDO, fb, c * 64, row0, bh);
-        }
         const size_t voff = static_cast<size_t>(bh) * args.n_pad + row0;
-        bulk_load(st + 2 * C::kTileBytes, args.lse2 + voff, kBlk * 4, fb);
-        bulk_load(st + 2 * C::kTileBytes + kBlk * 4, args.Dvec + voff, kBlk * 4, fb);
+        bulk_load(st + C::kTileBytes + C::kVTileBytes, args.lse2 + voff, kBlk * 4, fb);
+        bulk_load(st + C::kTileBytes + C::kVTileBytes + kBlk * 4, args.Dvec + voff, kBlk * 4, fb);
         issued = it + 1;
       }
       if (*abort_flag) {
@@ -331,7 +336,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ MMA issue
     if (lane == 0) {
       constexpr uint32_t kIdT = idesc_bf16_f32(kBlk, kHalf, false, false); // S^T, dP^T halves
-      constexpr uint32_t kIdKV = idesc_bf16_f32(kBlk, D, false, true);     // dV, dK
+      constexpr uint32_t kIdV = idesc_bf16_f32(kBlk, DV, false, true);     // dV
+      constexpr uint32_t kIdK = idesc_bf16_f32(kBlk, D, false, true);      // dK
       constexpr uint32_t kIdQ = idesc_bf16_f32(kBlk, D, true, true);       // dQ
       const uint32_t kb = base + C::kKOff, vb = base + C::kVOff, dsb = base + C::kDSOff;
       bool ok = mbar_wait(bar(C::kBarKV), 0, abort_flag);
@@ -359,7 +365,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
           }
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {  // dP^T_h = V dO_h^T
+          for (int kk = 0; kk < DV / 16; ++kk) {  // dP^T_h = V dO_h^T
             const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
             mma_ss(tmem + C::kColDP + kHalf * h, sdesc_sw128(vb + off, 16, 1024),
                    sdesc_sw128(dob + off + h * 8192, 16, 1024), kIdT, kk > 0 ? 1u : 0u);
@@ -376,13 +382,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int kk = 0; kk < kHalf / 16; ++kk)
             mma_ts(tmem + C::kColDV, tmem + C::kColS + kHalf * h + kk * 8,
-                   sdesc_sw128(dob + (4 * h + kk) * 2048, C::kChunkBytes, 1024), kIdKV,
+                   sdesc_sw128(dob + (4 * h + kk) * 2048, C::kChunkBytes, 1024), kIdV,
                    (it > 0 || h > 0 || kk > 0) ? 1u : 0u);
           // dK += dS_h^T Q_h   (A = dS^T K-major in smem region h, B = Q MN-major)
 #pragma unroll
           for (int kk = 0; kk < kHalf / 16; ++kk)
             mma_ss(tmem + C::kColDK, sdesc_sw128(dsb + h * C::kChunkBytes + kk * 32, 16, 1024),
-                   sdesc_sw128(qb + (4 * h + kk) * 2048, C::kChunkBytes, 1024), kIdKV,
+                   sdesc_sw128(qb + (4 * h + kk) * 2048, C::kChunkBytes, 1024), kIdK,
                    (it > 0 || h > 0 || kk > 0) ? 1u : 0u);
         }
         if (!ok) break;
@@ -419,7 +425,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int it = 0; it < n_steps; ++it) {
       const float* nlse2_s =
           reinterpret_cast<const float*>(base_ptr + C::kStageOff + (it % C::kStages) * C::kStageBytes +
-                                         2 * C::kTileBytes) + kHalf * w;
+                                         C::kTileBytes + C::kVTileBytes) + kHalf * w;
       const float* nd_s = nlse2_s + kBlk;
       // the stage's vectors arrive with its Q/dO tiles; S^T, dP^T with the MMA commit
       ok = mbar_wait(bar(C::kBarQFull + it % C::kStages), (it / C::kStages) & 1, abort_flag);
@@ -505,14 +511,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const int key = jb * kBlk + r;
       const bool live = key < N;
-      const size_t off = (static_cast<size_t>(bh) * N + key) * D;
 #pragma unroll
       for (int which = 0; which < 2; ++which) {
         const uint32_t col = which == 0 ? C::kColDK : C::kColDV;
         const float mul = which == 0 ? scale : 1.f;
-        __nv_bfloat16* out = (which == 0 ? args.dk : args.dv) + off;
+        const int width = which == 0 ? D : DV;
+        __nv_bfloat16* out =
+            (which == 0 ? args.dk : args.dv) + (static_cast<size_t>(bh) * N + key) * width;
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
+        for (int c = 0; c < width / 32; ++c) {
           uint32_t g[32];
           tmem_ld32(tmem + lane_base + col + c * 32, g);
           tmem_ld_wait(g);
@@ -993,14 +1000,14 @@ Workspace carve(const Problem& p, void* workspace) {
   return w;
 }
 
-template <int D>
+template <int DV, int DQ>
 int launch_pre_d(const Problem& p, const void* o, const float* lse, const void* dO,
                  void* workspace, cudaStream_t stream) {
   const Workspace w = carve(p, workspace);
-  constexpr int kRowsPerCta = 256 / (D / 8);
+  constexpr int kRowsPerCta = 256 / (DV / 8);
   const int BH = p.B * p.H;
   const dim3 grid(w.n_pad / kRowsPerCta, BH < 65535 ? BH : 65535);
-  fa_bwd_pre<D><<<grid, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(o),
+  fa_bwd_pre<DV, DQ><<<grid, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(o),
                                            static_cast<const __nv_bfloat16*>(dO), lse, w.Dvec,
                                            w.lse2, p.N, w.n_pad, w.acc, BH);
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
@@ -1025,6 +1032,16 @@ BwdArgs make_args(const Problem& p, const Workspace& w, void* dk, void* dv, int*
   return a;
 }
 
+template <int D, int DV>
+bool launch_seq(long long grid, int slot, const CUtensorMap& mq, const CUtensorMap& mk,
+                const CUtensorMap& mv, const CUtensorMap& mdo, const BwdArgs& a, cudaStream_t stream) {
+  using C = wide::BwdCfg<D, DV>;
+  auto kern = wide::fa_bwd_main_seq<D, DV>;
+  if (!ensure_smem_attr(reinterpret_cast<const void*>(kern), C::kSmemBytes, slot)) return false;
+  kern<<<static_cast<unsigned>(grid), wide::kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, mdo, a);
+  return true;
+}
+
 int launch_main_any(const Problem& p, const void* dO, void* dk, void* dv, void* workspace,
                     cudaStream_t stream) {
   const Workspace w = carve(p, workspace);
@@ -1032,23 +1049,26 @@ int launch_main_any(const Problem& p, const void* dO, void* dk, void* dv, void* 
   int* status = device_status_word();
   if (!status) return FA_ERR_LAUNCH;
   CUtensorMap mq, mk, mv, mdo;
+  const int dvh = p.dv ? p.dv : p.d;
   if (!make_map_bhnd(&mq, p.q, BH, p.N, p.d) || !make_map_bhnd(&mk, p.k, BH, p.N, p.d) ||
-      !make_map_bhnd(&mv, p.v, BH, p.N, p.d) || !make_map_bhnd(&mdo, dO, BH, p.N, p.d))
+      !make_map_bhnd(&mv, p.v, BH, p.N, dvh) || !make_map_bhnd(&mdo, dO, BH, p.N, dvh))
     return FA_ERR_LAUNCH;
   const BwdArgs a = make_args(p, w, dk, dv, status);
   const long long grid = static_cast<long long>(a.n_blocks) * BH;
   if (grid > 0x7fffffffLL) return FA_ERR_INVALID;
-  if (p.d == 64) {
+  if (p.d == 64 && dvh == 64) {
     auto kern = pipe::fa_bwd_main_d64;
     if (!ensure_smem_attr(reinterpret_cast<const void*>(kern), pipe::kSmemBytes, 2))
       return FA_ERR_LAUNCH;
     kern<<<static_cast<unsigned>(grid), pipe::kThreads, pipe::kSmemBytes, stream>>>(mq, mk, mv, mdo, a);
+  } else if (p.d == 128 && dvh == 128) {
+    if (!launch_seq<128, 128>(grid, 3, mq, mk, mv, mdo, a, stream)) return FA_ERR_LAUNCH;
+  } else if (p.d == 128 && dvh == 64) {
+    if (!launch_seq<128, 64>(grid, 6, mq, mk, mv, mdo, a, stream)) return FA_ERR_LAUNCH;
+  } else if (p.d == 64 && dvh == 128) {
+    if (!launch_seq<64, 128>(grid, 7, mq, mk, mv, mdo, a, stream)) return FA_ERR_LAUNCH;
   } else {
-    using C = wide::BwdCfg<128>;
-    auto kern = wide::fa_bwd_main_d128<128>;
-    if (!ensure_smem_attr(reinterpret_cast<const void*>(kern), C::kSmemBytes, 3))
-      return FA_ERR_LAUNCH;
-    kern<<<static_cast<unsigned>(grid), wide::kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, mdo, a);
+    return FA_ERR_UNSUPPORTED;
   }
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
@@ -1062,14 +1082,18 @@ size_t bwd_workspace_bytes(long long B, long long H, long long N, long long d) {
 
 int launch_bwd_pre(const Problem& p, const void* o, const float* lse, const void* dO,
                    void* workspace, cudaStream_t stream) {
-  if (p.d == 64) return launch_pre_d<64>(p, o, lse, dO, workspace, stream);
-  if (p.d == 128) return launch_pre_d<128>(p, o, lse, dO, workspace, stream);
+  const int dv = p.dv ? p.dv : p.d;
+  if (p.d == 64 && dv == 64) return launch_pre_d<64, 64>(p, o, lse, dO, workspace, stream);
+  if (p.d == 128 && dv == 128) return launch_pre_d<128, 128>(p, o, lse, dO, workspace, stream);
+  if (p.d == 128 && dv == 64) return launch_pre_d<64, 128>(p, o, lse, dO, workspace, stream);
+  if (p.d == 64 && dv == 128) return launch_pre_d<128, 64>(p, o, lse, dO, workspace, stream);
   return FA_ERR_UNSUPPORTED;
 }
 
 int launch_bwd_main(const Problem& p, const void* dO, void* dk, void* dv, void* workspace,
                     cudaStream_t stream) {
-  if (p.d != 64 && p.d != 128) return FA_ERR_UNSUPPORTED;
+  const int dvh = p.dv ? p.dv : p.d;
+  if ((p.d != 64 && p.d != 128) || (dvh != 64 && dvh != 128)) return FA_ERR_UNSUPPORTED;
   return launch_main_any(p, dO, dk, dv, workspace, stream);
 }
 

@@ -57,16 +57,20 @@ constexpr int kThreads = kSoftmaxThreads + 64;   // + the MMA warp and the TMA w
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr float kLn2 = 0.6931471805599453f;
 
-template <int D>
+// D: head size of Q and K; DV: head size of V and O.
+template <int D, int DV>
 struct FwdCfg {
   static constexpr int kChunks = D / 64;
-  static constexpr int kChunkBytes = kBlockM * 64 * 2;      // 16 KiB
-  static constexpr int kTileBytes = kChunks * kChunkBytes;  // 128 rows x d
-  static constexpr int kStages = (D == 64) ? 4 : 2;
+  static constexpr int kChunksV = DV / 64;
+  static constexpr int kChunkBytes = kBlockM * 64 * 2;        // 16 KiB
+  static constexpr int kTileBytes = kChunks * kChunkBytes;    // 128 rows x d (Q, K)
+  static constexpr int kVTileBytes = kChunksV * kChunkBytes;  // 128 rows x d_v (V)
+  // K/V ring depth: as many stages as fit next to the two Q tiles
+  static constexpr int kStages = (D == 64 && DV == 64) ? 4 : (D + DV == 192 ? 3 : 2);
   static constexpr int kQOff = 0;
   static constexpr int kKOff = kQOff + kQTiles * kTileBytes;
   static constexpr int kVOff = kKOff + kStages * kTileBytes;
-  static constexpr int kBarOff = kVOff + kStages * kTileBytes;
+  static constexpr int kBarOff = kVOff + kStages * kVTileBytes;
   // barrier indices
   static constexpr int kBarQFull = 0;
   static constexpr int kBarKFull = 1;
@@ -84,12 +88,14 @@ struct FwdCfg {
   static constexpr int kSmemBytes = kMiscOff + 16 + 1024;  // + slack to align the base
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColO = 256;
-  // With d = 64 the two S tiles and two O accumulators take 384 columns, so
-  // each tile's P gets 64 columns of its own at kColP: the softmax releases
-  // S as soon as it has loaded it and the next tile's QK^T overlaps the
-  // exponentials. With d = 128 the columns are full and P overwrites S.
-  static constexpr bool kSepP = (D == 64);
-  static constexpr uint32_t kColP = 384;
+  // With d_v = 64 the two S tiles and two O accumulators take 384 columns,
+  // so each tile's P gets 64 columns of its own at kColP: the softmax
+  // releases S as soon as it has loaded it and the next tile's QK^T
+  // overlaps the exponentials. With d_v = 128 the columns are full and P
+  // overwrites S.
+  static constexpr bool kSepP = (DV == 64);
+  static constexpr uint32_t kColP = 256 + 2 * DV;
+  static_assert(kSmemBytes <= 232448, "forward tiles exceed shared memory");
 };
 
 struct FwdArgs {
@@ -109,11 +115,11 @@ struct FwdArgs {
   float scale_log2;    // scale * log2(e), > 0
 };
 
-template <int D>
+template <int D, int DV>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const FwdArgs args) {
-  using C = FwdCfg<D>;
+  using C = FwdCfg<D, DV>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_u32 = smem_u32(smem_raw);
   const uint32_t base = (raw_u32 + 1023u) & ~1023u;
@@ -231,9 +237,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           issued = 2 * jj + 1;
           break;
         }
-        mbar_arrive_expect_tx(bar(C::kBarVFull + s), C::kTileBytes);
-        for (int c = 0; c < C::kChunks; ++c)
-          tma_load_3d(base + C::kVOff + s * C::kTileBytes + c * C::kChunkBytes, &tmV,
+        mbar_arrive_expect_tx(bar(C::kBarVFull + s), C::kVTileBytes);
+        for (int c = 0; c < C::kChunksV; ++c)
+          tma_load_3d(base + C::kVOff + s * C::kVTileBytes + c * C::kChunkBytes, &tmV,
                       bar(C::kBarVFull + s), c * 64, key0, bh);
         issued = 2 * jj + 2;
       }
@@ -252,7 +258,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ MMA issue
     if (lane == 0) {
       constexpr uint32_t kIdS = idesc_bf16_f32(kBlockM, kBlockN, false, false);
-      constexpr uint32_t kIdO = idesc_bf16_f32(kBlockM, D, false, true);
+      constexpr uint32_t kIdO = idesc_bf16_f32(kBlockM, DV, false, true);
       bool ok = n_stream > 0 ? mbar_wait(bar(C::kBarQFull), 0, abort_flag) : false;
       tc_fence_after();
       int k_ready = -1;
@@ -277,11 +283,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       // O_t (+)= P_t V for stream step jj; P_t from its TMEM columns
       auto issue_pv = [&](int t, int jj, bool first) {
-        const uint32_t vb = base + C::kVOff + (jj % C::kStages) * C::kTileBytes;
+        const uint32_t vb = base + C::kVOff + (jj % C::kStages) * C::kVTileBytes;
         const uint32_t pcol = C::kSepP ? C::kColP + t * 64 : t * 128;
 #pragma unroll
         for (int kk = 0; kk < kBlockN / 16; ++kk)
-          mma_ts(tmem + C::kColO + t * D, tmem + pcol + kk * 8,
+          mma_ts(tmem + C::kColO + t * DV, tmem + pcol + kk * 8,
                  sdesc_sw128(vb + kk * 2048, C::kChunkBytes, 1024), kIdO,
                  (!first || kk > 0) ? 1u : 0u);
       };
@@ -436,7 +442,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row = tile_row0 + (threadIdx.x & 127);
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + lane_base + t * 128;
-    const uint32_t tO = tmem + lane_base + C::kColO + t * D;
+    const uint32_t tO = tmem + lane_base + C::kColO + t * DV;
     const uint32_t tP = tmem + lane_base + C::kColP + t * 64;  // separate-P layout only
     const float sl2 = args.scale_log2;
     // keys visible to this row: pos - window < key <= pos (pos = row + kv_off)
@@ -532,7 +538,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // P.V; with separate P, the previous P.V has completed (waited above).
       if (u > 0 && __any_sync(0xffffffffu, need)) {
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
+        for (int c = 0; c < DV / 32; ++c) {
           uint32_t o[32];
           tmem_ld32(tO + c * 32, o);
           tmem_ld_wait(o);
@@ -565,9 +571,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float lse_row = l > 0.f ? (m_use + log2f(l)) * kLn2 : -INFINITY;
         const float2 il2 = make_float2(inv_l, inv_l);
         if (args.split_mode) {
-          float* orow = args.part_o + prow * D;
+          float* orow = args.part_o + prow * DV;
 #pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
+          for (int c = 0; c < DV / 32; ++c) {
             uint32_t o[32];
             tmem_ld32(tO + c * 32, o);
             tmem_ld_wait(o);
@@ -583,9 +589,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (live) args.part_lse[prow] = lse_row;
         } else {
-          __nv_bfloat16* orow = args.o + (static_cast<size_t>(bh) * Nq + row) * D;
+          __nv_bfloat16* orow = args.o + (static_cast<size_t>(bh) * Nq + row) * DV;
 #pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
+          for (int c = 0; c < DV / 32; ++c) {
             uint32_t o[32];
             tmem_ld32(tO + c * 32, o);
             tmem_ld_wait(o);
@@ -608,9 +614,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     } else if (ok && n_mine == 0 && args.split_mode && live) {
       // no key of this split is visible to the tile: an empty partial state
-      float4* dst = reinterpret_cast<float4*>(args.part_o + prow * D);
+      float4* dst = reinterpret_cast<float4*>(args.part_o + prow * DV);
 #pragma unroll
-      for (int e = 0; e < D / 4; ++e) dst[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int e = 0; e < DV / 4; ++e) dst[e] = make_float4(0.f, 0.f, 0.f, 0.f);
       args.part_lse[prow] = -INFINITY;
     }
   }
@@ -671,19 +677,21 @@ __global__ void __launch_bounds__(256) fa_merge_splits(const float* __restrict__
   }
 }
 
-template <int D>
+template <int D, int DV>
 int launch_fwd_d(const FwdProblem& p, void* o, float* lse, float* part_o, float* part_lse,
                  int n_splits, cudaStream_t stream) {
-  using C = FwdCfg<D>;
+  using C = FwdCfg<D, DV>;
   const int BH = p.B * p.H;
   CUtensorMap mq, mk, mv;
   if (!make_map_bhnd(&mq, p.q, BH, p.Nq, D) || !make_map_bhnd(&mk, p.k, BH, p.Nk, D) ||
-      !make_map_bhnd(&mv, p.v, BH, p.Nk, D))
+      !make_map_bhnd(&mv, p.v, BH, p.Nk, DV))
     return -3;
   int* status = device_status_word();
   if (!status) return -3;
-  auto kern = fa_fwd_kernel<D>;
-  if (!ensure_smem_attr(reinterpret_cast<const void*>(kern), C::kSmemBytes, D == 64 ? 0 : 1))
+  auto kern = fa_fwd_kernel<D, DV>;
+  // attribute slots 0, 1, 4, 5 (the backward uses 2, 3, 6-8)
+  constexpr int kSlot = (D == 64 ? 0 : 1) + (DV == 64 ? 0 : 4);
+  if (!ensure_smem_attr(reinterpret_cast<const void*>(kern), C::kSmemBytes, kSlot))
     return -3;
   const int n_kv = (p.Nk + kBlockN - 1) / kBlockN;
   if (n_splits < 1) n_splits = 1;
@@ -715,9 +723,9 @@ int launch_fwd_d(const FwdProblem& p, void* o, float* lse, float* part_o, float*
   kern<<<grid, kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, a);
   if (cudaGetLastError() != cudaSuccess) return -3;
   if (a.split_mode) {
-    constexpr int kRowsPerCta = 256 / (D / 8);
+    constexpr int kRowsPerCta = 256 / (DV / 8);
     const dim3 mgrid((p.Nq + kRowsPerCta - 1) / kRowsPerCta, BH < 65535 ? BH : 65535);
-    fa_merge_splits<D><<<mgrid, 256, 0, stream>>>(part_o, part_lse, static_cast<__nv_bfloat16*>(o),
+    fa_merge_splits<DV><<<mgrid, 256, 0, stream>>>(part_o, part_lse, static_cast<__nv_bfloat16*>(o),
                                                    lse, p.Nq, BH, n_splits);
     if (cudaGetLastError() != cudaSuccess) return -3;
   }
@@ -759,13 +767,15 @@ int fwd_split_count(const FwdProblem& p, int n_splits, int sms) {
 
 int launch_fwd_general(const FwdProblem& p, void* o, float* lse, float* part_o, float* part_lse,
                        int n_splits, cudaStream_t stream) {
-  if (p.d == 64) return launch_fwd_d<64>(p, o, lse, part_o, part_lse, n_splits, stream);
-  if (p.d == 128) return launch_fwd_d<128>(p, o, lse, part_o, part_lse, n_splits, stream);
+  if (p.d == 64 && p.dv == 64) return launch_fwd_d<64, 64>(p, o, lse, part_o, part_lse, n_splits, stream);
+  if (p.d == 128 && p.dv == 128) return launch_fwd_d<128, 128>(p, o, lse, part_o, part_lse, n_splits, stream);
+  if (p.d == 128 && p.dv == 64) return launch_fwd_d<128, 64>(p, o, lse, part_o, part_lse, n_splits, stream);
+  if (p.d == 64 && p.dv == 128) return launch_fwd_d<64, 128>(p, o, lse, part_o, part_lse, n_splits, stream);
   return -2;
 }
 
 int launch_fwd(const Problem& p, void* o, float* lse, cudaStream_t stream) {
-  FwdProblem g{p.q, p.k, p.v, p.B, p.H, p.N, p.N, p.d, p.causal, 0, p.scale};
+  FwdProblem g{p.q, p.k, p.v, p.B, p.H, p.N, p.N, p.d, p.d, p.causal, 0, p.scale};
   return launch_fwd_general(g, o, lse, nullptr, nullptr, 1, stream);
 }
 

@@ -17,15 +17,17 @@ struct Problem {
   int causal;
   float scale;
   int window = 0;  // backward only: 0 = none, else a causal window of this many keys
+  int dv = 0;      // head size of V, O, dO and dV; 0 means d
 };
 
 // Forward problem with Nq queries over Nk keys (causal queries are the last
-// Nq positions) and an optional left window of `window` keys.
+// Nq positions), head sizes d (Q, K) and dv (V, O), and an optional left
+// window of `window` keys.
 struct FwdProblem {
   const void* q;
   const void* k;
   const void* v;
-  int B, H, Nq, Nk, d;
+  int B, H, Nq, Nk, d, dv;
   int causal;
   int window;
   float scale;

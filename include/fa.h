@@ -159,11 +159,17 @@ int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, c
 size_t fa_bwd_workspace_bytes(int B, int H, int N, int d);
 
 /*
- * Extended forward: Nq queries over Nk keys, optional sliding window.
+ * Extended forward: Nq queries over Nk keys, head sizes d (queries, keys)
+ * and dv (values, output), optional sliding window.
  *   q       : in,  bf16 [B,H,Nq,d]
- *   k, v    : in,  bf16 [B,H,Nk,d]   (e.g. a key/value cache)
- *   o       : out, bf16 [B,H,Nq,d]
+ *   k       : in,  bf16 [B,H,Nk,d]   (e.g. a key/value cache)
+ *   v       : in,  bf16 [B,H,Nk,dv]
+ *   o       : out, bf16 [B,H,Nq,dv]
  *   lse     : out, fp32 [B,H,Nq]     natural-log log-sum-exp of each row
+ * d and dv are each 64 or 128 (FA_ERR_UNSUPPORTED otherwise); the pages
+ * count the forward's work as O(N^2 (d + d_v)) ("Flash Attention: IO-Aware
+ * Exact Attention", section "Storage, arithmetic and IO are separate
+ * quantities"), with d_v = d as the square special case.
  * With causal != 0 the queries are the last Nq positions of the Nk keys:
  * query i sits at position p = i + Nk - Nq and sees keys j <= p (Nq <= Nk
  * required). window = W >= 1 (causal only) further keeps only the keys
@@ -178,18 +184,21 @@ size_t fa_bwd_workspace_bytes(int B, int H, int N, int d);
  * without causal, Nk = 0 with Nq > 0, or causal with Nq > Nk.
  */
 int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
-              int Nq, int Nk, int d, int causal, int window, float scale, void* cuda_stream);
+              int Nq, int Nk, int d, int dv, int causal, int window, float scale,
+              void* cuda_stream);
 
 /*
- * Backward of fa_fwd_ex for training (Nq = Nk = N) with an optional causal
- * sliding window of `window` keys (0 = none): arguments, workspace and
- * results as fa_bwd_stream. Key/value blocks skip the query blocks that
- * see none of their keys, and the boundary blocks are masked per element.
+ * Backward of fa_fwd_ex for training (Nq = Nk = N) with head sizes d (q, k,
+ * dq, dk: [B,H,N,d]) and d_v (v, o, dO, dv: [B,H,N,d_v]), each 64 or 128,
+ * and an optional causal sliding window of `window` keys (0 = none);
+ * workspace (fa_bwd_workspace_bytes(B,H,N,d)) and results as
+ * fa_bwd_stream. Key/value blocks skip the query blocks that see none of
+ * their keys, and the boundary blocks are masked per element.
  * FA_ERR_INVALID for window < 0 or a window without causal.
  */
 int fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const float* lse,
               const void* dO, void* dq, void* dk, void* dv, int B, int H, int N, int d,
-              int causal, int window, float scale, void* workspace, size_t ws_bytes,
+              int d_v, int causal, int window, float scale, void* workspace, size_t ws_bytes,
               void* cuda_stream);
 
 /*
@@ -207,14 +216,14 @@ int fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const 
  *               actually used).
  *   workspace : device memory of at least fa_decode_workspace_bytes(...)
  *               bytes, 256-byte aligned, owned by the caller (partial
- *               outputs [splits,B,H,Nq,d] fp32 then partial LSE
+ *               outputs [splits,B,H,Nq,dv] fp32 then partial LSE
  *               [splits,B,H,Nq] fp32); FA_ERR_WORKSPACE otherwise.
  */
 int fa_decode_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B,
-                      int H, int Nq, int Nk, int d, int causal, int window, float scale,
+                      int H, int Nq, int Nk, int d, int dv, int causal, int window, float scale,
                       int n_splits, void* workspace, size_t ws_bytes, void* cuda_stream);
-int fa_decode_num_splits(int B, int H, int Nq, int Nk, int d, int n_splits);
-size_t fa_decode_workspace_bytes(int B, int H, int Nq, int Nk, int d, int n_splits);
+int fa_decode_num_splits(int B, int H, int Nq, int Nk, int n_splits);
+size_t fa_decode_workspace_bytes(int B, int H, int Nq, int Nk, int dv, int n_splits);
 
 /* Static description of a return code. Never NULL. */
 const char* fa_strerror(int code);

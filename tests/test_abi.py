@@ -134,24 +134,25 @@ def test_flop_and_byte_counts():
 def test_extended_forward_rejects_bad_arguments_on_the_host(lib):
     p = ctypes.c_void_p(4096)  # never dereferenced: every call below fails its checks first
     z = ctypes.c_void_p(0)
-    assert lib.fa_fwd_ex(p, p, p, p, p, 1, 1, 8, 8, 64, 0, 4, 0.1, z) == fa.FA_ERR_INVALID  # window, not causal
-    assert lib.fa_fwd_ex(p, p, p, p, p, 1, 1, 8, 8, 64, 1, -2, 0.1, z) == fa.FA_ERR_INVALID
-    assert lib.fa_fwd_ex(p, p, p, p, p, 1, 1, 9, 8, 64, 1, 0, 0.1, z) == fa.FA_ERR_INVALID  # Nq > Nk, causal
-    assert lib.fa_fwd_ex(p, p, p, p, p, 1, 1, 8, 0, 64, 0, 0, 0.1, z) == fa.FA_ERR_INVALID  # no keys
-    assert lib.fa_fwd_ex(p, p, p, p, p, 1, 1, 8, 8, 96, 0, 0, 0.1, z) == fa.FA_ERR_UNSUPPORTED
-    assert lib.fa_fwd_ex(z, z, z, z, z, 0, 1, 8, 8, 64, 0, 0, 0.1, z) == fa.FA_OK  # empty
-    assert lib.fa_decode_splitkv(z, z, z, z, z, 1, 1, 0, 8, 64, 0, 0, 0.1, 2, z, 0, z) == fa.FA_OK
+    assert lib.fa_fwd_ex(p, p, p, p, p, 1, 1, 8, 8, 64, 64, 0, 4, 0.1, z) == fa.FA_ERR_INVALID  # window, not causal
+    assert lib.fa_fwd_ex(p, p, p, p, p, 1, 1, 8, 8, 64, 64, 1, -2, 0.1, z) == fa.FA_ERR_INVALID
+    assert lib.fa_fwd_ex(p, p, p, p, p, 1, 1, 9, 8, 64, 64, 1, 0, 0.1, z) == fa.FA_ERR_INVALID  # Nq > Nk, causal
+    assert lib.fa_fwd_ex(p, p, p, p, p, 1, 1, 8, 0, 64, 64, 0, 0, 0.1, z) == fa.FA_ERR_INVALID  # no keys
+    assert lib.fa_fwd_ex(p, p, p, p, p, 1, 1, 8, 8, 96, 64, 0, 0, 0.1, z) == fa.FA_ERR_UNSUPPORTED
+    assert lib.fa_fwd_ex(p, p, p, p, p, 1, 1, 8, 8, 64, 32, 0, 0, 0.1, z) == fa.FA_ERR_UNSUPPORTED
+    assert lib.fa_fwd_ex(z, z, z, z, z, 0, 1, 8, 8, 64, 64, 0, 0, 0.1, z) == fa.FA_OK  # empty
+    assert lib.fa_decode_splitkv(z, z, z, z, z, 1, 1, 0, 8, 64, 64, 0, 0, 0.1, 2, z, 0, z) == fa.FA_OK
 
 
 def test_decode_split_count_and_workspace(lib):
     # explicit counts: clamped to the key tiles and made free of empty trailing splits
-    assert lib.fa_decode_num_splits(1, 1, 1, 300, 64, 64) == 3      # 3 key tiles
-    assert lib.fa_decode_num_splits(1, 1, 1, 4096, 64, 5) == 5      # 32 tiles, 7 per split
-    assert lib.fa_decode_num_splits(1, 1, 1, 4096, 64, 6) == 6      # 6 per split
-    assert lib.fa_decode_num_splits(1, 1, 1, 4096, 64, 11) == 11    # 3 per split -> 11
-    assert lib.fa_decode_num_splits(1, 1, 1, 4096, 64, 12) == 11    # 3 per split -> 11
-    auto = lib.fa_decode_num_splits(2, 4, 1, 32768, 128, 0)
+    assert lib.fa_decode_num_splits(1, 1, 1, 300, 64) == 3      # 3 key tiles
+    assert lib.fa_decode_num_splits(1, 1, 1, 4096, 5) == 5      # 32 tiles, 7 per split
+    assert lib.fa_decode_num_splits(1, 1, 1, 4096, 6) == 6      # 6 per split
+    assert lib.fa_decode_num_splits(1, 1, 1, 4096, 11) == 11    # 3 per split -> 11
+    assert lib.fa_decode_num_splits(1, 1, 1, 4096, 12) == 11    # 3 per split -> 11
+    auto = lib.fa_decode_num_splits(2, 4, 1, 32768, 0)
     assert 1 <= auto <= 128
-    s = lib.fa_decode_num_splits(2, 3, 5, 1000, 128, 4)
+    s = lib.fa_decode_num_splits(2, 3, 5, 1000, 4)
     assert lib.fa_decode_workspace_bytes(2, 3, 5, 1000, 128, 4) == s * 2 * 3 * 5 * (128 + 1) * 4
     assert lib.fa_decode_workspace_bytes(0, 3, 5, 1000, 128, 4) == 0

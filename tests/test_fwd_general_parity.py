@@ -79,7 +79,7 @@ def test_fwd_ex_matches_oracle(B, H, Nq, Nk, d, causal, window):
 def test_decode_splitkv_matches_oracle(B, H, Nq, Nk, d, causal, window, splits):
     q, k, v = _inputs(B, H, Nq, Nk, d, seed=Nk + Nq + splits)
     scale = 1.0 / math.sqrt(d)
-    used = fa.fa_decode_num_splits(B, H, Nq, Nk, d, splits)
+    used = fa.fa_decode_num_splits(B, H, Nq, Nk, splits)
     assert 1 <= used <= -(-Nk // 128)
     o, lse = fa.fa_decode_splitkv(q.cuda(), k.cuda(), v.cuda(), causal=causal, window=window,
                                   scale=scale, n_splits=splits)
@@ -120,13 +120,13 @@ def test_invalid_extended_arguments_are_refused():
     p = __import__("ctypes").c_void_p(t.data_ptr())
     z = __import__("ctypes").c_void_p(0)
     # window without causal, negative window, causal with more queries than keys
-    assert lib.fa_fwd_ex(p, p, p, p, p, 1, 1, 8, 8, 64, 0, 4, 0.1, z) == fa.FA_ERR_INVALID
-    assert lib.fa_fwd_ex(p, p, p, p, p, 1, 1, 8, 8, 64, 1, -1, 0.1, z) == fa.FA_ERR_INVALID
-    assert lib.fa_fwd_ex(p, p, p, p, p, 1, 1, 9, 8, 64, 1, 0, 0.1, z) == fa.FA_ERR_INVALID
+    assert lib.fa_fwd_ex(p, p, p, p, p, 1, 1, 8, 8, 64, 64, 0, 4, 0.1, z) == fa.FA_ERR_INVALID
+    assert lib.fa_fwd_ex(p, p, p, p, p, 1, 1, 8, 8, 64, 64, 1, -1, 0.1, z) == fa.FA_ERR_INVALID
+    assert lib.fa_fwd_ex(p, p, p, p, p, 1, 1, 9, 8, 64, 64, 1, 0, 0.1, z) == fa.FA_ERR_INVALID
     # no keys for live queries
-    assert lib.fa_fwd_ex(p, p, p, p, p, 1, 1, 8, 0, 64, 0, 0, 0.1, z) == fa.FA_ERR_INVALID
+    assert lib.fa_fwd_ex(p, p, p, p, p, 1, 1, 8, 0, 64, 64, 0, 0, 0.1, z) == fa.FA_ERR_INVALID
     # empty query set: nothing to do
-    assert lib.fa_fwd_ex(z, z, z, z, z, 1, 1, 0, 8, 64, 0, 0, 0.1, z) == fa.FA_OK
+    assert lib.fa_fwd_ex(z, z, z, z, z, 1, 1, 0, 8, 64, 64, 0, 0, 0.1, z) == fa.FA_OK
     # split form without a large enough workspace
-    assert lib.fa_decode_splitkv(p, p, p, p, p, 1, 1, 1, 4096, 64, 1, 0, 0.1, 4, p, 16, z) == \
+    assert lib.fa_decode_splitkv(p, p, p, p, p, 1, 1, 1, 4096, 64, 64, 1, 0, 0.1, 4, p, 16, z) == \
         fa.FA_ERR_WORKSPACE
