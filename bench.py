@@ -135,6 +135,34 @@ def decode_leg(dev, stream, reps=20):
             "l2": "inputs (4.3 GB) larger than L2"}
 
 
+def headsize_leg(dev, stream, flush, reps=10):
+    """Queries/keys of head size 128 with values of head size 64 (causal,
+    B=4 H=16 N=4096): forward and full backward. FLOPs per visible pair:
+    2 (d + d_v) forward; 2 (3 d + 2 d_v) backward (S, dP, dV, dK, dQ)."""
+    import torch
+    import exact_io_aware_33_gb300 as fa
+    B, H, N, d, dv = 4, 16, 4096, 128, 64
+    g = torch.Generator(device="cpu").manual_seed(91)
+    q, k = (torch.randn(B, H, N, d, generator=g).to(torch.bfloat16).to(dev) for _ in range(2))
+    v, do = (torch.randn(B, H, N, dv, generator=g).to(torch.bfloat16).to(dev) for _ in range(2))
+    o = torch.empty(B, H, N, dv, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(B, H, N, dtype=torch.float32, device=dev)
+    dq, dk, dvv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(fa.fa_bwd_workspace_bytes(B, H, N, d), dtype=torch.uint8, device=dev)
+    with torch.cuda.stream(stream):
+        ms_f = time_calls(lambda: fa.fa_fwd_ex(q, k, v, causal=True, out=o, lse=lse, stream=stream),
+                          reps, 3, stream, flush)
+        ms_b = time_calls(lambda: fa.fa_bwd_ex(q, k, v, o, lse, do, causal=True, dq=dq, dk=dk,
+                                               dv=dvv, workspace=ws, stream=stream),
+                          reps, 3, stream, flush)
+    pairs = B * H * N * (N + 1) / 2
+    return {"workload": "headsize_causal_b4h16_n4096_d128_dv64", "fwd_ms": round(ms_f, 4),
+            "fwd_tflops": round(2.0 * (d + dv) * pairs / (ms_f * 1e-3) / 1e12, 1),
+            "bwd_ms": round(ms_b, 4),
+            "bwd_tflops": round(2.0 * (3 * d + 2 * dv) * pairs / (ms_b * 1e-3) / 1e12, 1),
+            "note": "backward = preprocess + main + finish"}
+
+
 def window_leg(dev, stream, flush, reps=10):
     """Causal sliding window W = 1024 on B=1 H=16 N=8192 d=128: forward and
     backward; FLOPs count visible pairs only (4 d per pair forward, 2.5x
@@ -347,34 +375,61 @@ def timed_loop(runner, steps, warmup, barrier, stream, soak_s=0.0):
     return t, wall
 
 
-def e2e_loop(runner, steps, warmup, stream):
-    """Same step through host buffers: H2D of the inputs, D2H of every output."""
-    torch = runner.torch
-    names_in = ["q", "k", "v"] + (["do"] if runner.w.backward else [])
-    h_in = {n: runner.host[n].pin_memory() for n in names_in}
-    outs = [runner.o, runner.lse] + ([runner.dq, runner.dk, runner.dv] if runner.w.backward else [])
-    h_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
+def e2e_loop(runners, steps, warmup, stream):
+    """The step through host buffers: every step copies its inputs from
+    pinned host memory and every output back. Two device buffer sets and
+    three streams (host-to-device copies, compute, device-to-host copies)
+    let step i+1's upload and step i-1's download overlap step i's
+    compute; the timed region runs from the first upload to the last
+    download."""
+    torch = runners[0].torch
+    w = runners[0].w
+    names_in = ["q", "k", "v"] + (["do"] if w.backward else [])
+    h_in = {n: runners[0].host[n].pin_memory() for n in names_in}
+
+    def outs(r):
+        return [r.o, r.lse] + ([r.dq, r.dk, r.dv] if w.backward else [])
+
+    h_out = [[torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs(r)] for r in runners]
     h2d = sum(t.numel() * t.element_size() for t in h_in.values())
-    d2h = sum(t.numel() * t.element_size() for t in h_out)
+    d2h = sum(t.numel() * t.element_size() for t in h_out[0])
+    s_up, s_down = torch.cuda.Stream(), torch.cuda.Stream()
+    mk = lambda: torch.cuda.Event(enable_timing=False)
+    ev_in = [mk(), mk()]
+    ev_comp = [mk(), mk()]
+    ev_out = [mk(), mk()]
+    used = [False, False]
 
-    def one():
-        for n in names_in:
-            runner.x[n].copy_(h_in[n], non_blocking=True)
-        runner.step(stream)
-        for d, h in zip(outs, h_out):
-            h.copy_(d, non_blocking=True)
+    def one(i):
+        b = i % 2
+        r = runners[b]
+        if used[b]:  # the buffer set's previous step has finished with its inputs and outputs
+            s_up.wait_event(ev_comp[b])
+            stream.wait_event(ev_out[b])
+        with torch.cuda.stream(s_up):
+            for n in names_in:
+                r.x[n].copy_(h_in[n], non_blocking=True)
+            ev_in[b].record(s_up)
+        stream.wait_event(ev_in[b])
+        r.step(stream)
+        ev_comp[b].record(stream)
+        s_down.wait_event(ev_comp[b])
+        with torch.cuda.stream(s_down):
+            for d, h in zip(outs(r), h_out[b]):
+                h.copy_(d, non_blocking=True)
+            ev_out[b].record(s_down)
+        used[b] = True
 
-    with torch.cuda.stream(stream):
-        for _ in range(warmup):
-            one()
-        torch.cuda.synchronize()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        for _ in range(steps):
-            one()
-        b.record(stream)
+    for i in range(warmup):
+        one(i)
     torch.cuda.synchronize()
-    return a.elapsed_time(b) / steps, h2d, d2h
+    a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(s_up)
+    for i in range(steps):
+        one(warmup + i)
+    z.record(s_down)
+    torch.cuda.synchronize()
+    return a.elapsed_time(z) / steps, h2d, d2h
 
 
 def traffic_from_profiles(kernel):
@@ -503,10 +558,13 @@ def run_ours(args):
         "wall_s": round(wall, 3),
     }
     if not args.no_extras:
-        e_ms, h2d, d2h = e2e_loop(runner, max(3, args.steps // 2), 2, stream)
+        runner2 = Runner(w, dev, seed_offset=rank_seed_offset(rank))
+        e_ms, h2d, d2h = e2e_loop([runner, runner2], max(3, args.steps // 2), 2, stream)
+        del runner2
         out["e2e"] = {"value": round(world * (f_fwd + f_bwd) / (e_ms * 1e-3) / 1e12, 2),
                       "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                      "ms_per_step": round(e_ms, 4)}
+                      "ms_per_step": round(e_ms, 4),
+                      "pipeline": "uploads, compute and downloads on three streams, two buffer sets"}
         # the long causal forward (B=1, H=16, N=8192, d=128), the head-size-128 target shape
         wl = si.WORKLOADS[3]
         rl = Runner(wl, dev)
@@ -518,6 +576,7 @@ def run_ours(args):
         del rl
         out["decode"] = decode_leg(dev, stream)
         out["window"] = window_leg(dev, stream, runner.flush_l2)
+        out["headsize"] = headsize_leg(dev, stream, runner.flush_l2)
         if world == 1:
             out["cpu_baseline"] = cpu_baseline(w)
     print(json.dumps(out), flush=True)
