@@ -149,3 +149,22 @@ def test_planted_mistakes_are_caught():
     # causal aligned to the top-left instead of the bottom-right
     bad2 = general.forward_head(q, k[:4], v[:4], True, 0.5, 3)
     assert np.abs(good[0] - bad2[0]).max() > 1e-3
+
+
+@pytest.mark.parametrize("nq,nk,d,dv,causal,window", [
+    (5, 5, 3, 5, True, 0), (4, 9, 5, 2, True, 0), (6, 6, 4, 7, True, 2), (3, 8, 2, 6, False, 0),
+])
+def test_value_head_size_differs_from_key_head_size(nq, nk, d, dv, causal, window):
+    q, k, v = _qkv(nq, nk, d, dv=dv, seed=nq * 13 + nk + dv)
+    o, lse = general.forward_head(q, k, v, causal, 0.55, window)
+    assert o.shape == (nq, dv)
+    ob, lb = _brute(q, k, v, causal, 0.55, window)
+    np.testing.assert_allclose(o, ob, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(lse, lb, rtol=1e-12, atol=1e-12)
+    if nq == nk:
+        do = np.random.default_rng(4).standard_normal((nq, dv))
+        g = general.backward_head(q, k, v, o, lse, do, causal, 0.55, window)
+        assert g[0].shape == (nq, d) and g[1].shape == (nk, d) and g[2].shape == (nk, dv)
+        n = finite_diff.gradients_general(q, k, v, do, causal, 0.55, window)
+        for a, b in zip(g, n):
+            np.testing.assert_allclose(a, b, rtol=1e-6, atol=1e-7)
