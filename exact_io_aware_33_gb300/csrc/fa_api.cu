@@ -26,6 +26,7 @@ constexpr int kSmemSlots = 16;
 struct DeviceState {
   bool probed = false;
   bool supported = false;
+  int sms = 0;
   int* status = nullptr;
   bool smem_set[kSmemSlots] = {};
 };
@@ -64,6 +65,8 @@ int current_device(DeviceState** st) {
         cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
       return FA_ERR_LAUNCH;
     s.supported = (major == 10 && minor == 3);
+    if (cudaDeviceGetAttribute(&s.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return FA_ERR_LAUNCH;
     void* addr = nullptr;
     if (s.supported) {
       if (cudaGetSymbolAddress(&addr, g_status_word) != cudaSuccess) return FA_ERR_LAUNCH;
@@ -122,6 +125,12 @@ int* device_status_word() {
   DeviceState* st = nullptr;
   if (current_device(&st) != FA_OK) return nullptr;
   return st->status;
+}
+
+int device_sm_count() {
+  DeviceState* st = nullptr;
+  if (current_device(&st) != FA_OK) return 0;
+  return st->sms;
 }
 
 bool ensure_smem_attr(const void* func, int bytes, int slot) {

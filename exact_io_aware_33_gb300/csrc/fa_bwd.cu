@@ -599,7 +599,8 @@ constexpr int kDqStageBytes = 32 * 32 * 4;          // one 32 x 32 fp32 block pe
 constexpr int kBarOff = kDqStageOff + 4 * kDqStageBytes;
 enum : int {
   kBarKV = 0,
-  kBarQFull = 1,
+  kBarKVFree,    // the item's last MMA has read K and V
+  kBarQFull,
   kBarQEmpty = kBarQFull + kStages,
   kBarSFull = kBarQEmpty + kStages,
   kBarSFree,
@@ -609,6 +610,7 @@ enum : int {
   kBarDQFull = kBarDSFree + 2,
   kBarDQEmpty,
   kBarDKDV,
+  kBarDKDVFree,  // the dQ warpgroup has read dK, dV out of tensor memory
   kBarDrain,
   kNumBars
 };
@@ -619,6 +621,17 @@ static_assert(kSmemBytes <= 232448, "backward tiles exceed shared memory");
 static_assert(kStageBytes % 1024 == 0 && kDqStageOff % 1024 == 0, "swizzle atoms need 1 KiB alignment");
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0, kColDP = 128, kColP = 256, kColDQ = 320, kColDK = 384, kColDV = 448;
+
+// The k-th work item of this CTA in a snake-ordered round robin over the
+// items (key block jb, batch-head bh) listed heaviest first: round k hands
+// item k*G + c to CTA c, reversed on odd rounds, so the per-CTA totals stay
+// balanced. Returns false when the CTA has no k-th item.
+__device__ __forceinline__ bool item_of(int k, int num_items, int* x) {
+  const int G = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
+  const int v = k * G + ((k & 1) ? (G - 1 - c) : c);
+  *x = v;
+  return v < num_items;
+}
 
 __global__ void __launch_bounds__(kThreads, 1)
     fa_bwd_main_d64(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -632,15 +645,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base_ptr + kMiscOff);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(base_ptr + kMiscOff + 4);
 
-  const int bh = blockIdx.x % args.BH;
-  const int jb = static_cast<int>(blockIdx.x / args.BH);  // key block (heaviest first)
-  const int i0 = args.causal ? jb : 0;
-  const int n_steps = bwd_query_blocks_end(args, jb) - i0;
+  const int num_items = args.n_blocks * args.BH;
+  // geometry of item x: key block, batch-head, first query block, query steps
+  auto geom = [&](int x, int& jb, int& bh, int& i0, int& n_steps) {
+    jb = x / args.BH;
+    bh = x - jb * args.BH;
+    i0 = args.causal ? jb : 0;
+    n_steps = bwd_query_blocks_end(args, jb) - i0;
+  };
   const int warp = warp_id();
   const int lane = lane_id();
 
   if (threadIdx.x == 0) {
     mbar_init(bar(kBarKV), 1);
+    mbar_init(bar(kBarKVFree), 1);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(bar(kBarQFull + s), 1);
       mbar_init(bar(kBarQEmpty + s), 1);
@@ -654,6 +672,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(kBarDQFull), 1);
     mbar_init(bar(kBarDQEmpty), 128);
     mbar_init(bar(kBarDKDV), 1);
+    mbar_init(bar(kBarDKDVFree), 128);
     mbar_init(bar(kBarDrain), 1);
     *abort_flag = 0;
     mbar_fence_init();
@@ -668,6 +687,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
   if (warp >= kDqWarp0) regs_decrease<kRegsOther>();
 
+  // Every role walks the same item sequence; g counts this CTA's query
+  // steps over all its items and drives every ring slot and barrier phase.
   if (warp == kLoadWarp) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
@@ -675,17 +696,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_map(&tmK);
       tma_prefetch_map(&tmV);
       tma_prefetch_map(&tmDO);
-      mbar_arrive_expect_tx(bar(kBarKV), 2 * kTileBytes);
-      tma_load_3d(base + kKOff, &tmK, bar(kBarKV), 0, jb * kBlk, bh);
-      tma_load_3d(base + kVOff, &tmV, bar(kBarKV), 0, jb * kBlk, bh);
-      int issued = 0;
+      int g = 0, n_kv = 0;
       bool ok = true;
-      for (int it = 0; it < n_steps; ++it) {
-        const int s = it % kStages;
-        if (it >= kStages)
-          ok = mbar_wait(bar(kBarQEmpty + s), ((it / kStages) + 1) & 1, abort_flag);
-        if (!ok) break;
-        const int row0 = (i0 + it) * kBlk;
+      auto load_q = [&](int bh, int row0) {  // query block of global step g
+        const int s = g % kStages;
+        if (g >= kStages) ok = mbar_wait(bar(kBarQEmpty + s), ((g / kStages) + 1) & 1, abort_flag);
+        if (!ok) return;
         const uint32_t st = base + kStageOff + s * kStageBytes;
         const uint32_t fb = bar(kBarQFull + s);
         mbar_arrive_expect_tx(fb, kStageBytes);
@@ -694,12 +710,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         const size_t voff = static_cast<size_t>(bh) * args.n_pad + row0;
         bulk_load(st + 2 * kTileBytes, args.lse2 + voff, kBlk * 4, fb);
         bulk_load(st + 2 * kTileBytes + kBlk * 4, args.Dvec + voff, kBlk * 4, fb);
-        issued = it + 1;
+        ++g;
+      };
+      for (int n = 0; ok; ++n) {
+        int x, jb, bh, i0, ns;
+        if (!item_of(n, num_items, &x)) break;
+        geom(x, jb, bh, i0, ns);
+        // the item's first query block goes into the ring before its K/V,
+        // which must wait for the previous item's last MMA
+        load_q(bh, i0 * kBlk);
+        if (!ok) break;
+        if (n > 0) ok = mbar_wait(bar(kBarKVFree), (n - 1) & 1, abort_flag);
+        if (!ok) break;
+        mbar_arrive_expect_tx(bar(kBarKV), 2 * kTileBytes);
+        tma_load_3d(base + kKOff, &tmK, bar(kBarKV), 0, jb * kBlk, bh);
+        tma_load_3d(base + kVOff, &tmV, bar(kBarKV), 0, jb * kBlk, bh);
+        ++n_kv;
+        for (int it = 1; it < ns && ok; ++it) load_q(bh, (i0 + it) * kBlk);
       }
       if (*abort_flag) {
-        mbar_wait(bar(kBarKV), 0, nullptr);
-        for (int it = issued - 1; it >= 0 && it >= issued - kStages; --it)
-          mbar_wait(bar(kBarQFull + it % kStages), (it / kStages) & 1, nullptr);
+        // Let every copy this thread started land before the CTA exits.
+        if (n_kv > 0) mbar_wait(bar(kBarKV), (n_kv - 1) & 1, nullptr);
+        for (int q = g - 1; q >= 0 && q >= g - kStages; --q)
+          mbar_wait(bar(kBarQFull + q % kStages), (q / kStages) & 1, nullptr);
       }
     }
   } else if (warp == kMmaWarp) {
@@ -720,9 +753,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t kDSmn0 = sdesc_sw128(base + kDSOff, kTileBytes, 1024);
       constexpr uint64_t kStageStep = kStageBytes >> 4, kTileStep = kTileBytes >> 4;
       constexpr uint64_t kDSStep = kDSBytes >> 4;
-      // S^T = K Q^T and dP^T = V dO^T of query block `it` (both K-major)
-      auto issue_sdp = [&](int it) {
-        const uint64_t q = kQ0 + (it % kStages) * kStageStep, o = q + kTileStep;
+      // S^T = K Q^T and dP^T = V dO^T of global step g (both K-major)
+      auto issue_sdp = [&](int g) {
+        const uint64_t q = kQ0 + (g % kStages) * kStageStep, o = q + kTileStep;
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk)
           mma_ss(tmem + kColS, kK + 2 * kk, q + 2 * kk, kIdS, kk > 0 ? 1u : 0u);
@@ -731,47 +764,62 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_ss(tmem + kColDP, kV + 2 * kk, o + 2 * kk, kIdS, kk > 0 ? 1u : 0u);
         mma_commit(bar(kBarSFull));
       };
-      bool ok = mbar_wait(bar(kBarKV), 0, abort_flag);
-      if (ok) ok = mbar_wait(bar(kBarQFull), 0, abort_flag);
-      tc_fence_after();
-      if (ok) issue_sdp(0);
-      for (int it = 0; it < n_steps && ok; ++it) {
-        if (it + 1 < n_steps) {
-          ok = mbar_wait(bar(kBarSFree), it & 1, abort_flag);
-          if (ok) ok = mbar_wait(bar(kBarQFull + (it + 1) % kStages), ((it + 1) / kStages) & 1, abort_flag);
-          if (!ok) break;
-          tc_fence_after();
-          issue_sdp(it + 1);
-        }
-        ok = mbar_wait(bar(kBarDSFull), it & 1, abort_flag);
+      bool ok = true;
+      int g = 0;
+      for (int n = 0; ok; ++n) {
+        int x, jb, bh, i0, ns;
+        if (!item_of(n, num_items, &x)) break;
+        geom(x, jb, bh, i0, ns);
+        ok = mbar_wait(bar(kBarKV), n & 1, abort_flag);
+        if (ok) ok = mbar_wait(bar(kBarQFull + g % kStages), (g / kStages) & 1, abort_flag);
         if (!ok) break;
         tc_fence_after();
-        const uint64_t qmn = kQmn0 + (it % kStages) * kStageStep, omn = qmn + kTileStep;
-        const uint64_t dsk = kDS0 + (it & 1) * kDSStep, dsmn = kDSmn0 + (it & 1) * kDSStep;
-        // dV += P^T dO   (A = P^T bf16 pairs in TMEM, B = dO MN-major, 16 rows per step)
-#pragma unroll
-        for (int kk = 0; kk < kBlk / 16; ++kk)
-          mma_ts(tmem + kColDV, tmem + kColP + kk * 8, omn + 128 * kk, kIdKV, (it > 0 || kk > 0) ? 1u : 0u);
-        // dK += dS^T Q   (A = dS^T K-major, query halves in two 16 KiB regions; B = Q MN-major)
-#pragma unroll
-        for (int kk = 0; kk < kBlk / 16; ++kk)
-          mma_ss(tmem + kColDK, dsk + (kk >> 2) * kTileStep + (kk & 3) * 2, qmn + 128 * kk, kIdKV,
-                 (it > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(bar(kBarPFree));
-        if (it > 0) {
-          ok = mbar_wait(bar(kBarDQEmpty), (it - 1) & 1, abort_flag);
+        issue_sdp(g);
+        for (int it = 0; it < ns && ok; ++it, ++g) {
+          if (it + 1 < ns) {
+            ok = mbar_wait(bar(kBarSFree), g & 1, abort_flag);
+            if (ok) ok = mbar_wait(bar(kBarQFull + (g + 1) % kStages), ((g + 1) / kStages) & 1, abort_flag);
+            if (!ok) break;
+            tc_fence_after();
+            issue_sdp(g + 1);
+          }
+          ok = mbar_wait(bar(kBarDSFull), g & 1, abort_flag);
           if (!ok) break;
           tc_fence_after();
-        }
-        // dQ = dS K      (A = dS MN-major: the same bytes, B = K MN-major)
+          if (it == 0 && n > 0) {  // the previous item's dK, dV have left tensor memory
+            ok = mbar_wait(bar(kBarDKDVFree), (n - 1) & 1, abort_flag);
+            if (!ok) break;
+            tc_fence_after();
+          }
+          const uint64_t qmn = kQmn0 + (g % kStages) * kStageStep, omn = qmn + kTileStep;
+          const uint64_t dsk = kDS0 + (g & 1) * kDSStep, dsmn = kDSmn0 + (g & 1) * kDSStep;
+          // dV += P^T dO   (A = P^T bf16 pairs in TMEM, B = dO MN-major, 16 rows per step)
 #pragma unroll
-        for (int kk = 0; kk < kBlk / 16; ++kk)
-          mma_ss(tmem + kColDQ, dsmn + 128 * kk, kKmn + 128 * kk, kIdQ, kk > 0 ? 1u : 0u);
-        mma_commit(bar(kBarDQFull));
-        mma_commit(bar(kBarQEmpty + it % kStages));
-        mma_commit(bar(kBarDSFree + (it & 1)));
+          for (int kk = 0; kk < kBlk / 16; ++kk)
+            mma_ts(tmem + kColDV, tmem + kColP + kk * 8, omn + 128 * kk, kIdKV, (it > 0 || kk > 0) ? 1u : 0u);
+          // dK += dS^T Q   (A = dS^T K-major, query halves in two 16 KiB regions; B = Q MN-major)
+#pragma unroll
+          for (int kk = 0; kk < kBlk / 16; ++kk)
+            mma_ss(tmem + kColDK, dsk + (kk >> 2) * kTileStep + (kk & 3) * 2, qmn + 128 * kk, kIdKV,
+                   (it > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(bar(kBarPFree));
+          if (g > 0) {
+            ok = mbar_wait(bar(kBarDQEmpty), (g - 1) & 1, abort_flag);
+            if (!ok) break;
+            tc_fence_after();
+          }
+          // dQ = dS K      (A = dS MN-major: the same bytes, B = K MN-major)
+#pragma unroll
+          for (int kk = 0; kk < kBlk / 16; ++kk)
+            mma_ss(tmem + kColDQ, dsmn + 128 * kk, kKmn + 128 * kk, kIdQ, kk > 0 ? 1u : 0u);
+          mma_commit(bar(kBarDQFull));
+          mma_commit(bar(kBarQEmpty + g % kStages));
+          mma_commit(bar(kBarDSFree + (g & 1)));
+        }
+        if (!ok) break;
+        mma_commit(bar(kBarDKDV));    // dK, dV of this item are complete
+        mma_commit(bar(kBarKVFree));  // and K, V may be replaced
       }
-      if (ok) mma_commit(bar(kBarDKDV));
       mma_commit(bar(kBarDrain));
       mbar_wait(bar(kBarDrain), 0, nullptr);
     }
@@ -788,14 +836,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float2 sl2x2 = make_float2(sl2, sl2);
     const int key_sw = key_row & 7;
     bool ok = true;
-    for (int it = 0; it < n_steps; ++it) {
-      const int s = it % kStages;
+    int g = 0;
+    for (int n = 0; ok; ++n) {
+      int xi, jb, bh, i0, ns;
+      if (!item_of(n, num_items, &xi)) break;
+      geom(xi, jb, bh, i0, ns);
+    for (int it = 0; it < ns; ++it, ++g) {
+      const int s = g % kStages;
       const float* nlse2_s =
           reinterpret_cast<const float*>(base_ptr + kStageOff + s * kStageBytes + 2 * kTileBytes) + 64 * w;
       const float* nd_s = nlse2_s + kBlk;
       // the stage's vectors arrive with its Q/dO tiles; S^T, dP^T with the MMA commit
-      ok = mbar_wait(bar(kBarQFull + s), (it / kStages) & 1, abort_flag);
-      if (ok) ok = mbar_wait(bar(kBarSFull), it & 1, abort_flag);
+      ok = mbar_wait(bar(kBarQFull + s), (g / kStages) & 1, abort_flag);
+      if (ok) ok = mbar_wait(bar(kBarSFull), g & 1, abort_flag);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
@@ -843,10 +896,10 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (qc + 2 * u < key_row) p.x = 0.f;
               if (qc + 2 * u + 1 < key_row) p.y = 0.f;
             }
-            const float2 g = __fmul2_rn(
+            const float2 gs = __fmul2_rn(
                 p, __fadd2_rn(make_float2(__uint_as_float(dr[x]), __uint_as_float(dr[x + 1])), nd2));
             pp[(ql >> 1) + u] = pack_bf16(p.x, p.y);
-            dd[(ql >> 1) + u] = pack_bf16(g.x, g.y);
+            dd[(ql >> 1) + u] = pack_bf16(gs.x, gs.y);
           }
         }
       };
@@ -862,21 +915,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
 
       // P^T into its own columns once the previous step's dV MMA has read them
-      if (it > 0) {
-        ok = mbar_wait(bar(kBarPFree), (it - 1) & 1, abort_flag);
+      if (g > 0) {
+        ok = mbar_wait(bar(kBarPFree), (g - 1) & 1, abort_flag);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         tc_fence_after();
       }
       tmem_st32(tP, pp);
-      // dS^T row of this key into dS buffer (it & 1), once step it-2's dK and
+      // dS^T row of this key into dS buffer (g & 1), once step g-2's dK and
       // dQ MMAs have read that buffer: 64 queries -> eight swizzled 16-byte chunks
-      if (it >= 2) {
-        ok = mbar_wait(bar(kBarDSFree + (it & 1)), ((it >> 1) - 1) & 1, abort_flag);
+      if (g >= 2) {
+        ok = mbar_wait(bar(kBarDSFree + (g & 1)), ((g >> 1) - 1) & 1, abort_flag);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
       }
-      uint8_t* ds_row = base_ptr + kDSOff + (it & 1) * kDSBytes + w * kTileBytes + key_row * 128;
+      uint8_t* ds_row = base_ptr + kDSOff + (g & 1) * kDSBytes + w * kTileBytes + key_row * 128;
 #pragma unroll
       for (int v = 0; v < 8; ++v)
         *reinterpret_cast<uint4*>(ds_row + ((v ^ key_sw) * 16)) =
@@ -885,6 +938,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       fence_async_smem();
       mbar_arrive(bar(kBarDSFull));
+    }
     }
   } else if (warp < kMmaWarp) {
     // ------------------------------------------------------------ dQ, dK, dV out
@@ -896,7 +950,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     bool pending = false;
     // one 32 x 32 block of dQ (this warp's rows, 32 columns) -> staging -> bulk add
-    auto put_block = [&](const uint32_t (&g)[32], float* dst) {
+    auto put_block = [&](const uint32_t (&gr)[32], float* dst) {
       if (pending) {
         if (lane == 0) bulk_wait_read<0>();
         __syncwarp();
@@ -904,8 +958,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int v = 0; v < 8; ++v)
         *reinterpret_cast<float4*>(stage_row + ((v ^ (lane & 7)) * 16)) =
-            make_float4(__uint_as_float(g[4 * v]) * scale, __uint_as_float(g[4 * v + 1]) * scale,
-                        __uint_as_float(g[4 * v + 2]) * scale, __uint_as_float(g[4 * v + 3]) * scale);
+            make_float4(__uint_as_float(gr[4 * v]) * scale, __uint_as_float(gr[4 * v + 1]) * scale,
+                        __uint_as_float(gr[4 * v + 2]) * scale, __uint_as_float(gr[4 * v + 3]) * scale);
       fence_async_smem();
       __syncwarp();
       if (lane == 0) {
@@ -914,30 +968,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       pending = true;
     };
-    for (int it = 0; it < n_steps; ++it) {
-      ok = mbar_wait(bar(kBarDQFull), it & 1, abort_flag);
+    int g = 0;
+    for (int n = 0; ok; ++n) {
+      int xi, jb, bh, i0, ns;
+      if (!item_of(n, num_items, &xi)) break;
+      geom(xi, jb, bh, i0, ns);
+      for (int it = 0; it < ns; ++it, ++g) {
+        ok = mbar_wait(bar(kBarDQFull), g & 1, abort_flag);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc_fence_after();
+        // rows [32 qw, 32 qw + 32) of query block i0 + it: two contiguous 4 KiB blocks
+        float* dst = args.dq_acc + (static_cast<size_t>(bh) * args.n_pad + (i0 + it) * kBlk + 32 * qw) * kD;
+        uint32_t gr[32];
+        tmem_ld32(tmem + lane_base + kColDQ, gr);
+        tmem_ld_wait(gr);
+        put_block(gr, dst);
+        tmem_ld32(tmem + lane_base + kColDQ + 32, gr);
+        tmem_ld_wait(gr);
+        tc_fence_before();
+        mbar_arrive(bar(kBarDQEmpty));
+        put_block(gr, dst + 1024);
+      }
+      if (!ok) break;
+      // dK (x scale) and dV of this item's keys (thread = key row); their TMEM
+      // columns go to the next item right after the last read
+      ok = mbar_wait(bar(kBarDKDV), n & 1, abort_flag);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
-      tc_fence_after();
-      // rows [32 qw, 32 qw + 32) of query block i0 + it: two contiguous 4 KiB blocks
-      float* dst = args.dq_acc + (static_cast<size_t>(bh) * args.n_pad + (i0 + it) * kBlk + 32 * qw) * kD;
-      uint32_t g[32];
-      tmem_ld32(tmem + lane_base + kColDQ, g);
-      tmem_ld_wait(g);
-      put_block(g, dst);
-      tmem_ld32(tmem + lane_base + kColDQ + 32, g);
-      tmem_ld_wait(g);
-      tc_fence_before();
-      mbar_arrive(bar(kBarDQEmpty));
-      put_block(g, dst + 1024);
-    }
-    if (lane == 0) bulk_wait<0>();
-    __syncwarp();
-    if (ok) {
-      ok = mbar_wait(bar(kBarDKDV), 0, abort_flag);
-      ok = __all_sync(0xffffffffu, ok);
-    }
-    if (ok) {
       tc_fence_after();
       const int key = jb * kBlk + qw * 32 + lane;
       const bool live = key < args.N;
@@ -949,13 +1007,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         __nv_bfloat16* out = (which == 0 ? args.dk : args.dv) + off;
 #pragma unroll
         for (int c = 0; c < kD / 32; ++c) {
-          uint32_t g[32];
-          tmem_ld32(tmem + lane_base + col + c * 32, g);
-          tmem_ld_wait(g);
+          uint32_t gr[32];
+          tmem_ld32(tmem + lane_base + col + c * 32, gr);
+          tmem_ld_wait(gr);
+          if (which == 1 && c == kD / 32 - 1) {
+            tc_fence_before();
+            mbar_arrive(bar(kBarDKDVFree));
+          }
           uint32_t pk[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e)
-            pk[e] = pack_bf16(__uint_as_float(g[2 * e]) * mul, __uint_as_float(g[2 * e + 1]) * mul);
+            pk[e] = pack_bf16(__uint_as_float(gr[2 * e]) * mul, __uint_as_float(gr[2 * e + 1]) * mul);
           if (live) {
             uint4* o4 = reinterpret_cast<uint4*>(out + c * 32);
 #pragma unroll
@@ -964,6 +1026,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
+    // the bulk reductions complete before the CTA exits
+    if (lane == 0) bulk_wait<0>();
+    __syncwarp();
   }
 
   tc_fence_before();
@@ -1057,10 +1122,14 @@ int launch_main_any(const Problem& p, const void* dO, void* dk, void* dv, void* 
   const long long grid = static_cast<long long>(a.n_blocks) * BH;
   if (grid > 0x7fffffffLL) return FA_ERR_INVALID;
   if (p.d == 64 && dvh == 64) {
+    // persistent: one CTA per SM walks its share of the (key block, batch-head) items
     auto kern = pipe::fa_bwd_main_d64;
     if (!ensure_smem_attr(reinterpret_cast<const void*>(kern), pipe::kSmemBytes, 2))
       return FA_ERR_LAUNCH;
-    kern<<<static_cast<unsigned>(grid), pipe::kThreads, pipe::kSmemBytes, stream>>>(mq, mk, mv, mdo, a);
+    const int sms = device_sm_count();
+    if (sms <= 0) return FA_ERR_LAUNCH;
+    const long long g = grid < sms ? grid : sms;
+    kern<<<static_cast<unsigned>(g), pipe::kThreads, pipe::kSmemBytes, stream>>>(mq, mk, mv, mdo, a);
   } else if (p.d == 128 && dvh == 128) {
     if (!launch_seq<128, 128>(grid, 3, mq, mk, mv, mdo, a, stream)) return FA_ERR_LAUNCH;
   } else if (p.d == 128 && dvh == 64) {

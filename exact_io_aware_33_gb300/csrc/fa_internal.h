@@ -43,6 +43,9 @@ int current_device_status();
 // Device pointer of the status word of the current device (nullptr on error).
 int* device_status_word();
 
+// Number of SMs of the current device (looked up once per device), or 0.
+int device_sm_count();
+
 // Sets the dynamic shared memory limit of `func` once per device.
 bool ensure_smem_attr(const void* func, int bytes, int slot);
 
