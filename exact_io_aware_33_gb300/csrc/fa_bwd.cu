@@ -562,6 +562,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 // per-warp 4 KiB shared staging tiles and bulk reductions (full 128-byte
 // lines, no per-thread atomics).
 //
+// Persistent: one CTA per SM walks its share of the (key block, batch-head)
+// items. The query ring and every barrier phase run on a step count over
+// all of the CTA's items, so the next item's first query block is already
+// in flight while the current one finishes; its K and V load once the last
+// MMA of the current item has read theirs, and its first dV/dK MMAs wait
+// only for the current item's dK and dV to be read out of tensor memory.
+//
 // CTA (512 threads):
 //   warps 0-7  two P/dS warpgroups: thread = key row = TMEM lane; warpgroup
 //              w handles query columns [64w, 64w+64) of every step
@@ -579,10 +586,14 @@ constexpr int kPdsThreads = 256;
 constexpr int kDqWarp0 = 8;
 constexpr int kMmaWarp = 12;
 constexpr int kLoadWarp = 13;
-// Register budgets after the split (launch: 128 per thread x 512 threads).
-constexpr uint32_t kRegsPds = 192;
-constexpr uint32_t kRegsOther = 64;
-static_assert(kRegsPds * kPdsThreads + kRegsOther * (kThreads - kPdsThreads) <= 128 * kThreads,
+// Register budgets after the split (launch: 128 per thread x 512 threads):
+// the P/dS warpgroups need more than the launch allocation, and the MMA
+// warp's issue loop must not spill (its queue of MMAs is short, so every
+// extra instruction between issues idles the tensor core).
+constexpr uint32_t kRegsPds = 168;
+constexpr uint32_t kRegsDq = 88;
+constexpr uint32_t kRegsMma = 88;
+static_assert(kRegsPds * kPdsThreads + kRegsDq * 128 + kRegsMma * 128 <= 128 * kThreads,
               "register split exceeds the launch allocation");
 
 constexpr int kTileBytes = kBlk * kD * 2;           // 16 KiB, one 128B-swizzled chunk
@@ -685,7 +696,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  if (warp >= kDqWarp0) regs_decrease<kRegsOther>();
+  if (warp >= kMmaWarp) regs_decrease<kRegsMma>();
+  else if (warp >= kDqWarp0) regs_decrease<kRegsDq>();
 
   // Every role walks the same item sequence; g counts this CTA's query
   // steps over all its items and drives every ring slot and barrier phase.
