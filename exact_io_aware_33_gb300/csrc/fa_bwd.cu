@@ -190,6 +190,8 @@ __global__ void __launch_bounds__(256) fa_bwd_post(const float* __restrict__ acc
 //   warp  13   TMA producer; warps 14-15 idle
 // TMEM columns: S^T/P^T [0,128), dP^T and dQ [128,256), dK [256,384),
 // dV [384,512).
+// Every wait sleeps in hardware (mbar_wait_sleep): with these longer steps,
+// polling warps take more issue slots than a later wake-up costs.
 namespace wide {
 
 constexpr int kHalf = 64;  // query columns per P/dS warpgroup
@@ -311,7 +313,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int it = 0; it < n_steps; ++it) {
         const int s = it % C::kStages;
         if (it >= C::kStages)
-          ok = mbar_wait(bar(C::kBarQEmpty + s), ((it / C::kStages) + 1) & 1, abort_flag);
+          ok = mbar_wait_sleep(bar(C::kBarQEmpty + s), ((it / C::kStages) + 1) & 1, abort_flag);
         if (!ok) break;
         const int row0 = (i0 + it) * kBlk;
         const uint32_t st = base + C::kStageOff + s * C::kStageBytes;
@@ -327,9 +329,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         issued = it + 1;
       }
       if (*abort_flag) {
-        mbar_wait(bar(C::kBarKV), 0, nullptr);
+        mbar_wait_sleep(bar(C::kBarKV), 0, nullptr);
         for (int it = issued - 1; it >= 0 && it >= issued - C::kStages; --it)
-          mbar_wait(bar(C::kBarQFull + it % C::kStages), (it / C::kStages) & 1, nullptr);
+          mbar_wait_sleep(bar(C::kBarQFull + it % C::kStages), (it / C::kStages) & 1, nullptr);
       }
     }
   } else if (warp == kMmaWarp) {
@@ -340,11 +342,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t kIdK = idesc_bf16_f32(kBlk, D, false, true);      // dK
       constexpr uint32_t kIdQ = idesc_bf16_f32(kBlk, D, true, true);       // dQ
       const uint32_t kb = base + C::kKOff, vb = base + C::kVOff, dsb = base + C::kDSOff;
-      bool ok = mbar_wait(bar(C::kBarKV), 0, abort_flag);
+      bool ok = mbar_wait_sleep(bar(C::kBarKV), 0, abort_flag);
       tc_fence_after();
       for (int it = 0; it < n_steps && ok; ++it) {
         const int s = it % C::kStages;
-        ok = mbar_wait(bar(C::kBarQFull + s), (it / C::kStages) & 1, abort_flag);
+        ok = mbar_wait_sleep(bar(C::kBarQFull + s), (it / C::kStages) & 1, abort_flag);
         if (!ok) break;
         tc_fence_after();
         const uint32_t qb = base + C::kStageOff + s * C::kStageBytes;
@@ -360,7 +362,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                    sdesc_sw128(qb + off + h * 8192, 16, 1024), kIdT, kk > 0 ? 1u : 0u);
           }
           if (C::kDqAliasDp && h == 0 && it > 0) {  // dQ of the last step shares dP's columns
-            ok = mbar_wait(bar(C::kBarDQEmpty), (it - 1) & 1, abort_flag);
+            ok = mbar_wait_sleep(bar(C::kBarDQEmpty), (it - 1) & 1, abort_flag);
             if (!ok) break;
             tc_fence_after();
           }
@@ -375,7 +377,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          ok = mbar_wait(bar(C::kBarDSFull + h), it & 1, abort_flag);
+          ok = mbar_wait_sleep(bar(C::kBarDSFull + h), it & 1, abort_flag);
           if (!ok) break;
           tc_fence_after();
           // dV += P_h^T dO_h   (A = P^T in TMEM, B = dO rows of half h, MN-major)
@@ -393,7 +395,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!ok) break;
         if (!C::kDqAliasDp && it > 0) {
-          ok = mbar_wait(bar(C::kBarDQEmpty), (it - 1) & 1, abort_flag);
+          ok = mbar_wait_sleep(bar(C::kBarDQEmpty), (it - 1) & 1, abort_flag);
           if (!ok) break;
           tc_fence_after();
         }
@@ -407,7 +409,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (ok) mma_commit(bar(C::kBarDKDV));
       mma_commit(bar(C::kBarDrain));
-      mbar_wait(bar(C::kBarDrain), 0, nullptr);
+      mbar_wait_sleep(bar(C::kBarDrain), 0, nullptr);
     }
   } else if (warp < kDqWarp0) {
     // ------------------------------------------------------------ P and dS
@@ -428,8 +430,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                          C::kTileBytes + C::kVTileBytes) + kHalf * w;
       const float* nd_s = nlse2_s + kBlk;
       // the stage's vectors arrive with its Q/dO tiles; S^T, dP^T with the MMA commit
-      ok = mbar_wait(bar(C::kBarQFull + it % C::kStages), (it / C::kStages) & 1, abort_flag);
-      if (ok) ok = mbar_wait(bar(C::kBarSFull + w), it & 1, abort_flag);
+      ok = mbar_wait_sleep(bar(C::kBarQFull + it % C::kStages), (it / C::kStages) & 1, abort_flag);
+      if (ok) ok = mbar_wait_sleep(bar(C::kBarSFull + w), it & 1, abort_flag);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
@@ -481,7 +483,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float scale = args.scale;
     bool ok = true;
     for (int it = 0; it < n_steps; ++it) {
-      ok = mbar_wait(bar(C::kBarDQFull), it & 1, abort_flag);
+      ok = mbar_wait_sleep(bar(C::kBarDQFull), it & 1, abort_flag);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
@@ -504,7 +506,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(bar(C::kBarDQEmpty));
     }
     if (ok) {
-      ok = mbar_wait(bar(C::kBarDKDV), 0, abort_flag);
+      ok = mbar_wait_sleep(bar(C::kBarDKDV), 0, abort_flag);
       ok = __all_sync(0xffffffffu, ok);
     }
     if (ok) {
@@ -553,7 +555,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 // Pipelined across query blocks. The P/dS warpgroups copy S^T_i and dP^T_i
 // from tensor memory into registers and release them at once, so the tensor
 // core computes S^T_{i+1} and dP^T_{i+1} while P_i and dS_i are formed; P^T
-// has tensor-memory columns of its own and dS two shared-memory buffers.
+// has tensor-memory columns of its own. dS has one shared-memory buffer: the
+// P/dS warpgroups write dS_{i+1} once the dK and dQ MMAs of step i have read
+// dS_i, which still comes before the tensor core needs dS_{i+1}.
 // Per query block the MMA warp issues, in this order:
 //   S^T_{i+1}, dP^T_{i+1}        (once the warpgroups hold S^T_i, dP^T_i)
 //   dV += P^T_i dO_i, dK += dS^T_i Q_i   (once P_i and dS_i are written)
@@ -565,9 +569,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 // Persistent: one CTA per SM walks its share of the (key block, batch-head)
 // items. The query ring and every barrier phase run on a step count over
 // all of the CTA's items, so the next item's first query block is already
-// in flight while the current one finishes; its K and V load once the last
-// MMA of the current item has read theirs, and its first dV/dK MMAs wait
-// only for the current item's dK and dV to be read out of tensor memory.
+// in flight while the current one finishes. K and V have two buffers (item
+// n uses buffer n & 1), so the next item's K and V load about two query
+// steps before they are needed rather than after the current item's last
+// MMA; the next item's first dV/dK MMAs wait only for the current item's dK
+// and dV to be read out of tensor memory.
 //
 // CTA (512 threads):
 //   warps 0-7  two P/dS warpgroups: thread = key row = TMEM lane; warpgroup
@@ -599,26 +605,27 @@ static_assert(kRegsPds * kPdsThreads + kRegsDq * 128 + kRegsMma * 128 <= 128 * k
 constexpr int kTileBytes = kBlk * kD * 2;           // 16 KiB, one 128B-swizzled chunk
 constexpr int kVecBytes = 2 * kBlk * 4;             // -lse2[128], -D[128] of a query block
 constexpr int kStages = 3;
-constexpr int kKOff = 0;
+constexpr int kKVBytes = 2 * kTileBytes;            // K then V of one item
+constexpr int kKOff = 0;                            // two K/V buffers
 constexpr int kVOff = kKOff + kTileBytes;
-constexpr int kDSOff = kVOff + kTileBytes;          // 2 buffers x (2 query halves x 16 KiB)
+constexpr int kDSOff = kKOff + 2 * kKVBytes;        // one buffer: 2 query halves x 16 KiB
 constexpr int kDSBytes = 2 * kTileBytes;
-constexpr int kStageOff = kDSOff + 2 * kDSBytes;
+constexpr int kStageOff = kDSOff + kDSBytes;
 constexpr int kStageBytes = 2 * kTileBytes + kVecBytes;  // Q, dO, vectors
 constexpr int kDqStageOff = kStageOff + kStages * kStageBytes;
 constexpr int kDqStageBytes = 32 * 32 * 4;          // one 32 x 32 fp32 block per dQ warp
 constexpr int kBarOff = kDqStageOff + 4 * kDqStageBytes;
 enum : int {
-  kBarKV = 0,
-  kBarKVFree,    // the item's last MMA has read K and V
-  kBarQFull,
+  kBarKV = 0,                // two, one per K/V buffer
+  kBarKVFree = kBarKV + 2,   // two: the last MMA of the buffer's item has read K and V
+  kBarQFull = kBarKVFree + 2,
   kBarQEmpty = kBarQFull + kStages,
   kBarSFull = kBarQEmpty + kStages,
   kBarSFree,
   kBarPFree,
   kBarDSFull,
-  kBarDSFree,  // two, one per dS buffer
-  kBarDQFull = kBarDSFree + 2,
+  kBarDSFree,  // the dK and dQ MMAs of the step have read dS
+  kBarDQFull,
   kBarDQEmpty,
   kBarDKDV,
   kBarDKDVFree,  // the dQ warpgroup has read dK, dV out of tensor memory
@@ -668,8 +675,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = lane_id();
 
   if (threadIdx.x == 0) {
-    mbar_init(bar(kBarKV), 1);
-    mbar_init(bar(kBarKVFree), 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar(kBarKV + b), 1);
+      mbar_init(bar(kBarKVFree + b), 1);
+    }
     for (int s = 0; s < kStages; ++s) {
       mbar_init(bar(kBarQFull + s), 1);
       mbar_init(bar(kBarQEmpty + s), 1);
@@ -678,8 +687,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(kBarSFree), kPdsThreads);
     mbar_init(bar(kBarPFree), 1);
     mbar_init(bar(kBarDSFull), kPdsThreads);
-    mbar_init(bar(kBarDSFree + 0), 1);
-    mbar_init(bar(kBarDSFree + 1), 1);
+    mbar_init(bar(kBarDSFree), 1);
     mbar_init(bar(kBarDQFull), 1);
     mbar_init(bar(kBarDQEmpty), 128);
     mbar_init(bar(kBarDKDV), 1);
@@ -728,21 +736,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         int x, jb, bh, i0, ns;
         if (!item_of(n, num_items, &x)) break;
         geom(x, jb, bh, i0, ns);
-        // the item's first query block goes into the ring before its K/V,
-        // which must wait for the previous item's last MMA
+        // the item's first query block goes into the ring before its K/V;
+        // K/V buffer n & 1 is free once item n - 2's last MMA has read it
         load_q(bh, i0 * kBlk);
         if (!ok) break;
-        if (n > 0) ok = mbar_wait(bar(kBarKVFree), (n - 1) & 1, abort_flag);
+        const int kv = n & 1;
+        if (n >= 2) ok = mbar_wait(bar(kBarKVFree + kv), ((n >> 1) - 1) & 1, abort_flag);
         if (!ok) break;
-        mbar_arrive_expect_tx(bar(kBarKV), 2 * kTileBytes);
-        tma_load_3d(base + kKOff, &tmK, bar(kBarKV), 0, jb * kBlk, bh);
-        tma_load_3d(base + kVOff, &tmV, bar(kBarKV), 0, jb * kBlk, bh);
+        mbar_arrive_expect_tx(bar(kBarKV + kv), 2 * kTileBytes);
+        tma_load_3d(base + kKOff + kv * kKVBytes, &tmK, bar(kBarKV + kv), 0, jb * kBlk, bh);
+        tma_load_3d(base + kVOff + kv * kKVBytes, &tmV, bar(kBarKV + kv), 0, jb * kBlk, bh);
         ++n_kv;
         for (int it = 1; it < ns && ok; ++it) load_q(bh, (i0 + it) * kBlk);
       }
       if (*abort_flag) {
         // Let every copy this thread started land before the CTA exits.
-        if (n_kv > 0) mbar_wait(bar(kBarKV), (n_kv - 1) & 1, nullptr);
+        for (int m = n_kv - 1; m >= 0 && m >= n_kv - 2; --m)
+          mbar_wait(bar(kBarKV + (m & 1)), (m >> 1) & 1, nullptr);
         for (int q = g - 1; q >= 0 && q >= g - kStages; --q)
           mbar_wait(bar(kBarQFull + q % kStages), (q / kStages) & 1, nullptr);
       }
@@ -753,20 +763,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t kIdS = idesc_bf16_f32(kBlk, kBlk, false, false);  // S^T, dP^T
       constexpr uint32_t kIdKV = idesc_bf16_f32(kBlk, kD, false, true);     // dV, dK
       constexpr uint32_t kIdQ = idesc_bf16_f32(kBlk, kD, true, true);       // dQ
-      // Shared-memory descriptors, built once. Advancing an operand by b
-      // bytes adds b / 16 to the descriptor's start-address field, which
-      // cannot carry out of its 14 bits below 256 KiB.
-      const uint64_t kK = sdesc_sw128(base + kKOff, 16, 1024);          // K, K-major
-      const uint64_t kV = sdesc_sw128(base + kVOff, 16, 1024);          // V, K-major
-      const uint64_t kKmn = sdesc_sw128(base + kKOff, kTileBytes, 1024);  // K as MN-major B
+      // Shared-memory descriptors, built once (K and V: once per item).
+      // Advancing an operand by b bytes adds b / 16 to the descriptor's
+      // start-address field, which cannot carry out of its 14 bits below
+      // 256 KiB.
       const uint64_t kQ0 = sdesc_sw128(base + kStageOff, 16, 1024);     // stage 0 Q, K-major
       const uint64_t kQmn0 = sdesc_sw128(base + kStageOff, kTileBytes, 1024);
       const uint64_t kDS0 = sdesc_sw128(base + kDSOff, 16, 1024);       // dS buffer 0, K-major
       const uint64_t kDSmn0 = sdesc_sw128(base + kDSOff, kTileBytes, 1024);
       constexpr uint64_t kStageStep = kStageBytes >> 4, kTileStep = kTileBytes >> 4;
-      constexpr uint64_t kDSStep = kDSBytes >> 4;
-      // S^T = K Q^T and dP^T = V dO^T of global step g (both K-major)
-      auto issue_sdp = [&](int g) {
+      // S^T = K Q^T and dP^T = V dO^T of global step g (both K-major), with
+      // the item's K and V descriptors
+      auto issue_sdp = [&](int g, uint64_t kK, uint64_t kV) {
         const uint64_t q = kQ0 + (g % kStages) * kStageStep, o = q + kTileStep;
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk)
@@ -782,18 +790,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         int x, jb, bh, i0, ns;
         if (!item_of(n, num_items, &x)) break;
         geom(x, jb, bh, i0, ns);
-        ok = mbar_wait(bar(kBarKV), n & 1, abort_flag);
+        const int kv = n & 1;
+        const uint32_t kvb = base + kv * kKVBytes;
+        const uint64_t kK = sdesc_sw128(kvb + kKOff, 16, 1024);            // K, K-major
+        const uint64_t kV = sdesc_sw128(kvb + kVOff, 16, 1024);            // V, K-major
+        const uint64_t kKmn = sdesc_sw128(kvb + kKOff, kTileBytes, 1024);  // K as MN-major B
+        ok = mbar_wait(bar(kBarKV + kv), (n >> 1) & 1, abort_flag);
         if (ok) ok = mbar_wait(bar(kBarQFull + g % kStages), (g / kStages) & 1, abort_flag);
         if (!ok) break;
         tc_fence_after();
-        issue_sdp(g);
+        issue_sdp(g, kK, kV);
         for (int it = 0; it < ns && ok; ++it, ++g) {
           if (it + 1 < ns) {
             ok = mbar_wait(bar(kBarSFree), g & 1, abort_flag);
             if (ok) ok = mbar_wait(bar(kBarQFull + (g + 1) % kStages), ((g + 1) / kStages) & 1, abort_flag);
             if (!ok) break;
             tc_fence_after();
-            issue_sdp(g + 1);
+            issue_sdp(g + 1, kK, kV);
           }
           ok = mbar_wait(bar(kBarDSFull), g & 1, abort_flag);
           if (!ok) break;
@@ -804,7 +817,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
           }
           const uint64_t qmn = kQmn0 + (g % kStages) * kStageStep, omn = qmn + kTileStep;
-          const uint64_t dsk = kDS0 + (g & 1) * kDSStep, dsmn = kDSmn0 + (g & 1) * kDSStep;
+          const uint64_t dsk = kDS0, dsmn = kDSmn0;
           // dV += P^T dO   (A = P^T bf16 pairs in TMEM, B = dO MN-major, 16 rows per step)
 #pragma unroll
           for (int kk = 0; kk < kBlk / 16; ++kk)
@@ -826,11 +839,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_ss(tmem + kColDQ, dsmn + 128 * kk, kKmn + 128 * kk, kIdQ, kk > 0 ? 1u : 0u);
           mma_commit(bar(kBarDQFull));
           mma_commit(bar(kBarQEmpty + g % kStages));
-          mma_commit(bar(kBarDSFree + (g & 1)));
+          mma_commit(bar(kBarDSFree));
         }
         if (!ok) break;
         mma_commit(bar(kBarDKDV));    // dK, dV of this item are complete
-        mma_commit(bar(kBarKVFree));  // and K, V may be replaced
+        mma_commit(bar(kBarKVFree + kv));  // and this K/V buffer may be refilled
       }
       mma_commit(bar(kBarDrain));
       mbar_wait(bar(kBarDrain), 0, nullptr);
@@ -934,14 +947,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
       }
       tmem_st32(tP, pp);
-      // dS^T row of this key into dS buffer (g & 1), once step g-2's dK and
-      // dQ MMAs have read that buffer: 64 queries -> eight swizzled 16-byte chunks
-      if (g >= 2) {
-        ok = mbar_wait(bar(kBarDSFree + (g & 1)), ((g >> 1) - 1) & 1, abort_flag);
+      // dS^T row of this key into the dS buffer once step g-1's dK and dQ
+      // MMAs have read it: 64 queries -> eight swizzled 16-byte chunks
+      if (g >= 1) {
+        ok = mbar_wait(bar(kBarDSFree), (g - 1) & 1, abort_flag);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
       }
-      uint8_t* ds_row = base_ptr + kDSOff + (g & 1) * kDSBytes + w * kTileBytes + key_row * 128;
+      uint8_t* ds_row = base_ptr + kDSOff + w * kTileBytes + key_row * 128;
 #pragma unroll
       for (int v = 0; v < 8; ++v)
         *reinterpret_cast<uint4*>(ds_row + ((v ^ key_sw) * 16)) =
@@ -1004,19 +1017,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) break;
       // dK (x scale) and dV of this item's keys (thread = key row); their TMEM
-      // columns go to the next item right after the last read
+      // columns go to the next item right after the last read. A thread's
+      // row is one 128-byte line, so storing rows straight from registers
+      // would touch 32 lines per warp instruction and crowd the shared-memory
+      // data path the tensor core reads its operands through; each warp
+      // instead swizzles its 32 rows into its 4 KiB staging block and writes
+      // them back four whole lines per instruction.
       ok = mbar_wait(bar(kBarDKDV), n & 1, abort_flag);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
-      const int key = jb * kBlk + qw * 32 + lane;
-      const bool live = key < args.N;
-      const size_t off = (static_cast<size_t>(bh) * args.N + key) * kD;
-#pragma unroll
+      if (pending) {  // the last dQ reduction has finished reading the staging block
+        if (lane == 0) bulk_wait_read<0>();
+        __syncwarp();
+        pending = false;
+      }
+      const int key0 = jb * kBlk + qw * 32;  // this warp's first key row
+      const uint8_t* stage_blk = base_ptr + kDqStageOff + qw * kDqStageBytes;
+#pragma unroll 1
       for (int which = 0; which < 2; ++which) {
         const uint32_t col = which == 0 ? kColDK : kColDV;
         const float mul = which == 0 ? scale : 1.f;
-        __nv_bfloat16* out = (which == 0 ? args.dk : args.dv) + off;
 #pragma unroll
         for (int c = 0; c < kD / 32; ++c) {
           uint32_t gr[32];
@@ -1030,12 +1051,23 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int e = 0; e < 16; ++e)
             pk[e] = pack_bf16(__uint_as_float(gr[2 * e]) * mul, __uint_as_float(gr[2 * e + 1]) * mul);
-          if (live) {
-            uint4* o4 = reinterpret_cast<uint4*>(out + c * 32);
+          // 16-byte chunks 4c..4c+3 of row `lane`, chunk v in slot v ^ (lane & 7)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) o4[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
-          }
+          for (int e = 0; e < 4; ++e)
+            *reinterpret_cast<uint4*>(stage_row + (((4 * c + e) ^ (lane & 7)) * 16)) =
+                make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
         }
+        __syncwarp();
+        // instruction j: lanes 8r'..8r'+7 write the eight chunks of row 4j + r'
+        __nv_bfloat16* out = (which == 0 ? args.dk : args.dv) + static_cast<size_t>(bh) * args.N * kD;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int r = 4 * j + (lane >> 3), v = lane & 7;
+          const uint4 val = *reinterpret_cast<const uint4*>(stage_blk + r * 128 + ((v ^ (r & 7)) * 16));
+          if (key0 + r < args.N)
+            *reinterpret_cast<uint4*>(out + static_cast<size_t>(key0 + r) * kD + v * 8) = val;
+        }
+        __syncwarp();  // the block is read back before it is written again
       }
     }
     // the bulk reductions complete before the CTA exits

@@ -269,26 +269,31 @@ __global__ void __launch_bounds__(kThreads, 1)
           k_ready = jj;
         }
       };
+      // Shared-memory descriptors, built once: advancing an operand by b
+      // bytes adds b / 16 to the start-address field (no carry below
+      // 256 KiB). The MMA thread shares its scheduler with busy softmax
+      // warps, so every instruction it saves between MMAs counts.
+      const uint64_t dQ0 = sdesc_sw128(base + C::kQOff, 16, 1024);
+      const uint64_t dK0 = sdesc_sw128(base + C::kKOff, 16, 1024);
+      const uint64_t dV0 = sdesc_sw128(base + C::kVOff, C::kChunkBytes, 1024);
       // S_t = Q_t K^T for stream step jj
       auto issue_s = [&](int t, int jj) {
-        const uint32_t qb = base + C::kQOff + t * C::kTileBytes;
-        const uint32_t kb = base + C::kKOff + (jj % C::kStages) * C::kTileBytes;
+        const uint64_t q = dQ0 + static_cast<uint64_t>(t * C::kTileBytes >> 4);
+        const uint64_t k = dK0 + static_cast<uint64_t>((jj % C::kStages) * (C::kTileBytes >> 4));
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
-          mma_ss(tmem + t * 128, sdesc_sw128(qb + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024),
-                 kIdS, kk > 0 ? 1u : 0u);
+          const uint64_t off = static_cast<uint64_t>(((kk >> 2) * C::kChunkBytes + (kk & 3) * 32) >> 4);
+          mma_ss(tmem + t * 128, q + off, k + off, kIdS, kk > 0 ? 1u : 0u);
         }
         mma_commit(bar(C::kBarSFull + t));
       };
       // O_t (+)= P_t V for stream step jj; P_t from its TMEM columns
       auto issue_pv = [&](int t, int jj, bool first) {
-        const uint32_t vb = base + C::kVOff + (jj % C::kStages) * C::kVTileBytes;
+        const uint64_t v = dV0 + static_cast<uint64_t>((jj % C::kStages) * (C::kVTileBytes >> 4));
         const uint32_t pcol = C::kSepP ? C::kColP + t * 64 : t * 128;
 #pragma unroll
         for (int kk = 0; kk < kBlockN / 16; ++kk)
-          mma_ts(tmem + C::kColO + t * DV, tmem + pcol + kk * 8,
-                 sdesc_sw128(vb + kk * 2048, C::kChunkBytes, 1024), kIdO,
+          mma_ts(tmem + C::kColO + t * DV, tmem + pcol + kk * 8, v + 128 * kk, kIdO,
                  (!first || kk > 0) ? 1u : 0u);
       };
       auto step_of = [&](int t, int jj) -> int {  // tile-local step, or -1
@@ -589,25 +594,45 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (live) args.part_lse[prow] = lse_row;
         } else {
-          __nv_bfloat16* orow = args.o + (static_cast<size_t>(bh) * Nq + row) * DV;
+          // A thread's O row is 128-byte lines of its own; written straight
+          // from registers, one warp instruction would touch 32 lines. Each
+          // warp instead swizzles its 32 rows, 64 columns at a time, into 4 KiB
+          // of this tile's Q buffer (free: every QK^T of the tile has
+          // completed) and writes them back as four whole lines per instruction.
+          __nv_bfloat16* obase = args.o + static_cast<size_t>(bh) * Nq * DV;
+          uint8_t* stage_blk = base_ptr + C::kQOff + t * C::kTileBytes + (warp & 3) * 4096;
+          uint8_t* stage_row = stage_blk + lane * 128;
+          const int row0 = row - lane;  // first row of this warp
 #pragma unroll
-          for (int c = 0; c < DV / 32; ++c) {
-            uint32_t o[32];
-            tmem_ld32(tO + c * 32, o);
-            tmem_ld_wait(o);
-            uint32_t pko[16];
+          for (int h = 0; h < DV / 64; ++h) {
 #pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              const float2 v =
-                  __fmul2_rn(make_float2(__uint_as_float(o[2 * e]), __uint_as_float(o[2 * e + 1])), il2);
-              pko[e] = pack_bf16(v.x, v.y);
-            }
-            if (live) {
-              uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+            for (int c = 0; c < 2; ++c) {
+              uint32_t o[32];
+              tmem_ld32(tO + h * 64 + c * 32, o);
+              tmem_ld_wait(o);
+              uint32_t pko[16];
+#pragma unroll
+              for (int e = 0; e < 16; ++e) {
+                const float2 v =
+                    __fmul2_rn(make_float2(__uint_as_float(o[2 * e]), __uint_as_float(o[2 * e + 1])), il2);
+                pko[e] = pack_bf16(v.x, v.y);
+              }
+              // 16-byte chunks 4c..4c+3 of row `lane`, chunk v in slot v ^ (lane & 7)
 #pragma unroll
               for (int e = 0; e < 4; ++e)
-                dst[e] = make_uint4(pko[4 * e], pko[4 * e + 1], pko[4 * e + 2], pko[4 * e + 3]);
+                *reinterpret_cast<uint4*>(stage_row + (((4 * c + e) ^ (lane & 7)) * 16)) =
+                    make_uint4(pko[4 * e], pko[4 * e + 1], pko[4 * e + 2], pko[4 * e + 3]);
             }
+            __syncwarp();
+            // instruction j: lanes 8r'..8r'+7 write the eight chunks of row 4j + r'
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const int r = 4 * j + (lane >> 3), v = lane & 7;
+              const uint4 val = *reinterpret_cast<const uint4*>(stage_blk + r * 128 + ((v ^ (r & 7)) * 16));
+              if (row0 + r < Nq)
+                *reinterpret_cast<uint4*>(obase + static_cast<size_t>(row0 + r) * DV + h * 64 + v * 8) = val;
+            }
+            __syncwarp();  // the block is read back before it is written again
           }
           if (live) args.lse[static_cast<size_t>(bh) * Nq + row] = lse_row;
         }
