@@ -566,6 +566,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 // per-warp 4 KiB shared staging tiles and bulk reductions (full 128-byte
 // lines, no per-thread atomics).
 //
+// The MMA thread waits on two barriers per query block: every wait costs the
+// issuing thread a shared-memory round trip, during which the tensor core's
+// short instruction queue runs dry. So the other roles fold their conditions
+// into those two: the P/dS warpgroups release S^T_i only once Q_{i+1} and
+// dO_{i+1} have landed, and the dQ warpgroup joins the "dS_i written"
+// barrier once it has read dQ_{i-1} (and, at an item's first query block,
+// the previous item's dK and dV) out of tensor memory.
+//
 // Persistent: one CTA per SM walks its share of the (key block, batch-head)
 // items. The query ring and every barrier phase run on a step count over
 // all of the CTA's items, so the next item's first query block is already
@@ -621,14 +629,11 @@ enum : int {
   kBarQFull = kBarKVFree + 2,
   kBarQEmpty = kBarQFull + kStages,
   kBarSFull = kBarQEmpty + kStages,
-  kBarSFree,
+  kBarSFree,     // S^T, dP^T are in registers and the next Q/dO have landed
   kBarPFree,
-  kBarDSFull,
-  kBarDSFree,  // the dK and dQ MMAs of the step have read dS
+  kBarDSFull,    // P^T and dS written; dQ (and at an item start dK, dV) read out
   kBarDQFull,
-  kBarDQEmpty,
   kBarDKDV,
-  kBarDKDVFree,  // the dQ warpgroup has read dK, dV out of tensor memory
   kBarDrain,
   kNumBars
 };
@@ -686,12 +691,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(kBarSFull), 1);
     mbar_init(bar(kBarSFree), kPdsThreads);
     mbar_init(bar(kBarPFree), 1);
-    mbar_init(bar(kBarDSFull), kPdsThreads);
-    mbar_init(bar(kBarDSFree), 1);
+    mbar_init(bar(kBarDSFull), kPdsThreads + 128);
     mbar_init(bar(kBarDQFull), 1);
-    mbar_init(bar(kBarDQEmpty), 128);
     mbar_init(bar(kBarDKDV), 1);
-    mbar_init(bar(kBarDKDVFree), 128);
     mbar_init(bar(kBarDrain), 1);
     *abort_flag = 0;
     mbar_fence_init();
@@ -802,20 +804,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         issue_sdp(g, kK, kV);
         for (int it = 0; it < ns && ok; ++it, ++g) {
           if (it + 1 < ns) {
-            ok = mbar_wait(bar(kBarSFree), g & 1, abort_flag);
-            if (ok) ok = mbar_wait(bar(kBarQFull + (g + 1) % kStages), ((g + 1) / kStages) & 1, abort_flag);
+            ok = mbar_wait(bar(kBarSFree), g & 1, abort_flag);  // (Q/dO of g+1 have landed too)
             if (!ok) break;
             tc_fence_after();
             issue_sdp(g + 1, kK, kV);
           }
+          // P^T and dS of step g written, dQ of step g-1 (and at an item's
+          // first step the previous item's dK, dV) read out of tensor memory
           ok = mbar_wait(bar(kBarDSFull), g & 1, abort_flag);
           if (!ok) break;
           tc_fence_after();
-          if (it == 0 && n > 0) {  // the previous item's dK, dV have left tensor memory
-            ok = mbar_wait(bar(kBarDKDVFree), (n - 1) & 1, abort_flag);
-            if (!ok) break;
-            tc_fence_after();
-          }
           const uint64_t qmn = kQmn0 + (g % kStages) * kStageStep, omn = qmn + kTileStep;
           const uint64_t dsk = kDS0, dsmn = kDSmn0;
           // dV += P^T dO   (A = P^T bf16 pairs in TMEM, B = dO MN-major, 16 rows per step)
@@ -828,18 +826,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_ss(tmem + kColDK, dsk + (kk >> 2) * kTileStep + (kk & 3) * 2, qmn + 128 * kk, kIdKV,
                    (it > 0 || kk > 0) ? 1u : 0u);
           mma_commit(bar(kBarPFree));
-          if (g > 0) {
-            ok = mbar_wait(bar(kBarDQEmpty), (g - 1) & 1, abort_flag);
-            if (!ok) break;
-            tc_fence_after();
-          }
           // dQ = dS K      (A = dS MN-major: the same bytes, B = K MN-major)
 #pragma unroll
           for (int kk = 0; kk < kBlk / 16; ++kk)
             mma_ss(tmem + kColDQ, dsmn + 128 * kk, kKmn + 128 * kk, kIdQ, kk > 0 ? 1u : 0u);
-          mma_commit(bar(kBarDQFull));
+          mma_commit(bar(kBarDQFull));  // (dS may be overwritten too)
           mma_commit(bar(kBarQEmpty + g % kStages));
-          mma_commit(bar(kBarDSFree));
         }
         if (!ok) break;
         mma_commit(bar(kBarDKDV));    // dK, dV of this item are complete
@@ -871,8 +863,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float* nlse2_s =
           reinterpret_cast<const float*>(base_ptr + kStageOff + s * kStageBytes + 2 * kTileBytes) + 64 * w;
       const float* nd_s = nlse2_s + kBlk;
-      // the stage's vectors arrive with its Q/dO tiles; S^T, dP^T with the MMA commit
+      // the stage's vectors arrive with its Q/dO tiles; S^T, dP^T with the MMA
+      // commit. The next step's Q and dO are checked here too, so that the
+      // release of S^T below also tells the MMA thread they have landed and
+      // it has one wait less.
       ok = mbar_wait(bar(kBarQFull + s), (g / kStages) & 1, abort_flag);
+      if (ok && it + 1 < ns)
+        ok = mbar_wait(bar(kBarQFull + (g + 1) % kStages), ((g + 1) / kStages) & 1, abort_flag);
       if (ok) ok = mbar_wait(bar(kBarSFull), g & 1, abort_flag);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
@@ -887,7 +884,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld_wait(d0);
       tmem_ld_wait(d1);
       // S^T and dP^T of this step are in registers: the next step's MMAs may
-      // overwrite their columns.
+      // overwrite their columns (its Q and dO have landed, checked above).
       tc_fence_before();
       mbar_arrive(bar(kBarSFree));
 
@@ -948,9 +945,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tmem_st32(tP, pp);
       // dS^T row of this key into the dS buffer once step g-1's dK and dQ
-      // MMAs have read it: 64 queries -> eight swizzled 16-byte chunks
+      // MMAs have read it (dQ complete): 64 queries -> eight swizzled 16-byte chunks
       if (g >= 1) {
-        ok = mbar_wait(bar(kBarDSFree), (g - 1) & 1, abort_flag);
+        ok = mbar_wait(bar(kBarDQFull), (g - 1) & 1, abort_flag);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
       }
@@ -994,6 +991,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       pending = true;
     };
     int g = 0;
+    mbar_arrive(bar(kBarDSFull));  // the first step has no dQ to read out
     for (int n = 0; ok; ++n) {
       int xi, jb, bh, i0, ns;
       if (!item_of(n, num_items, &xi)) break;
@@ -1012,7 +1010,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld32(tmem + lane_base + kColDQ + 32, gr);
         tmem_ld_wait(gr);
         tc_fence_before();
-        mbar_arrive(bar(kBarDQEmpty));
+        if (it + 1 < ns) mbar_arrive(bar(kBarDSFull));  // dQ columns free for step g+1
         put_block(gr, dst + 1024);
       }
       if (!ok) break;
@@ -1043,9 +1041,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t gr[32];
           tmem_ld32(tmem + lane_base + col + c * 32, gr);
           tmem_ld_wait(gr);
-          if (which == 1 && c == kD / 32 - 1) {
+          if (which == 1 && c == kD / 32 - 1) {  // dQ, dK, dV columns free for the next item
             tc_fence_before();
-            mbar_arrive(bar(kBarDKDVFree));
+            mbar_arrive(bar(kBarDSFull));
           }
           uint32_t pk[16];
 #pragma unroll
