@@ -558,21 +558,24 @@ __global__ void __launch_bounds__(kThreads, 1)
 // has tensor-memory columns of its own. dS has one shared-memory buffer: the
 // P/dS warpgroups write dS_{i+1} once the dK and dQ MMAs of step i have read
 // dS_i, which still comes before the tensor core needs dS_{i+1}.
-// Per query block the MMA warp issues, in this order:
-//   S^T_{i+1}, dP^T_{i+1}        (once the warpgroups hold S^T_i, dP^T_i)
-//   dV += P^T_i dO_i, dK += dS^T_i Q_i   (once P_i and dS_i are written)
-//   dQ_i = dS_i K                (once dQ_{i-1} has been read out)
+// Two threads issue tensor-core work, each waiting on one barrier per
+// query block:
+//   warp 14: S^T_{i+1}, dP^T_{i+1}   (once the warpgroups hold S^T_i, dP^T_i)
+//   warp 12: dV += P^T_i dO_i, dK += dS^T_i Q_i, then dQ_i = dS_i K
+//            (once P_i and dS_i are written and dQ_{i-1} has been read out)
 // dQ_i is added to the fp32 accumulator by the dQ warpgroup through
 // per-warp 4 KiB shared staging tiles and bulk reductions (full 128-byte
 // lines, no per-thread atomics).
 //
-// The MMA thread waits on two barriers per query block: every wait costs the
-// issuing thread a shared-memory round trip, during which the tensor core's
-// short instruction queue runs dry. So the other roles fold their conditions
-// into those two: the P/dS warpgroups release S^T_i only once Q_{i+1} and
-// dO_{i+1} have landed, and the dQ warpgroup joins the "dS_i written"
+// Every wait costs the issuing thread a shared-memory round trip, during
+// which the tensor core's short instruction queue runs dry, so each issuer
+// waits on one barrier per query block and the other roles fold their
+// conditions into it: the P/dS warpgroups release S^T_i only once Q_{i+1}
+// and dO_{i+1} have landed, and the dQ warpgroup joins the "dS_i written"
 // barrier once it has read dQ_{i-1} (and, at an item's first query block,
-// the previous item's dK and dV) out of tensor memory.
+// the previous item's dK and dV) out of tensor memory. With the S^T/dP^T
+// MMAs on a thread of their own, neither issuer's wait holds up the other's
+// instructions.
 //
 // Persistent: one CTA per SM walks its share of the (key block, batch-head)
 // items. The query ring and every barrier phase run on a step count over
@@ -588,8 +591,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 //              w handles query columns [64w, 64w+64) of every step
 //   warps 8-11 dQ warpgroup: thread = query row of dQ_i; at the end writes
 //              dK and dV (thread = key row)
-//   warp  12   tcgen05 MMA issue and TMEM allocation
-//   warp  13   TMA producer; warps 14-15 idle
+//   warp  12   tcgen05 MMA issue (dV, dK, dQ) and TMEM allocation
+//   warp  13   TMA producer
+//   warp  14   tcgen05 MMA issue (S^T, dP^T); warp 15 idle
 // TMEM columns: S^T [0,128), dP^T [128,256), P^T (bf16 pairs) [256,320),
 // dQ [320,384), dK [384,448), dV [448,512).
 namespace pipe {
@@ -600,6 +604,7 @@ constexpr int kPdsThreads = 256;
 constexpr int kDqWarp0 = 8;
 constexpr int kMmaWarp = 12;
 constexpr int kLoadWarp = 13;
+constexpr int kSWarp = 14;
 // Register budgets after the split (launch: 128 per thread x 512 threads):
 // the P/dS warpgroups need more than the launch allocation, and the MMA
 // warp's issue loop must not spill (its queue of MMAs is short, so every
@@ -634,8 +639,8 @@ enum : int {
   kBarDSFull,    // P^T and dS written; dQ (and at an item start dK, dV) read out
   kBarDQFull,
   kBarDKDV,
-  kBarDrain,
-  kNumBars
+  kBarDrain,     // two: one per issuing thread
+  kNumBars = kBarDrain + 2
 };
 constexpr int kMiscOff = kBarOff + kNumBars * 8;
 constexpr int kLayoutBytes = kMiscOff + 16;
@@ -695,6 +700,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(kBarDQFull), 1);
     mbar_init(bar(kBarDKDV), 1);
     mbar_init(bar(kBarDrain), 1);
+    mbar_init(bar(kBarDrain + 1), 1);
     *abort_flag = 0;
     mbar_fence_init();
   }
@@ -762,30 +768,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issue
     if (lane == 0) {
-      constexpr uint32_t kIdS = idesc_bf16_f32(kBlk, kBlk, false, false);  // S^T, dP^T
       constexpr uint32_t kIdKV = idesc_bf16_f32(kBlk, kD, false, true);     // dV, dK
       constexpr uint32_t kIdQ = idesc_bf16_f32(kBlk, kD, true, true);       // dQ
       // Shared-memory descriptors, built once (K and V: once per item).
       // Advancing an operand by b bytes adds b / 16 to the descriptor's
       // start-address field, which cannot carry out of its 14 bits below
       // 256 KiB.
-      const uint64_t kQ0 = sdesc_sw128(base + kStageOff, 16, 1024);     // stage 0 Q, K-major
       const uint64_t kQmn0 = sdesc_sw128(base + kStageOff, kTileBytes, 1024);
       const uint64_t kDS0 = sdesc_sw128(base + kDSOff, 16, 1024);       // dS buffer 0, K-major
       const uint64_t kDSmn0 = sdesc_sw128(base + kDSOff, kTileBytes, 1024);
       constexpr uint64_t kStageStep = kStageBytes >> 4, kTileStep = kTileBytes >> 4;
-      // S^T = K Q^T and dP^T = V dO^T of global step g (both K-major), with
-      // the item's K and V descriptors
-      auto issue_sdp = [&](int g, uint64_t kK, uint64_t kV) {
-        const uint64_t q = kQ0 + (g % kStages) * kStageStep, o = q + kTileStep;
-#pragma unroll
-        for (int kk = 0; kk < kD / 16; ++kk)
-          mma_ss(tmem + kColS, kK + 2 * kk, q + 2 * kk, kIdS, kk > 0 ? 1u : 0u);
-#pragma unroll
-        for (int kk = 0; kk < kD / 16; ++kk)
-          mma_ss(tmem + kColDP, kV + 2 * kk, o + 2 * kk, kIdS, kk > 0 ? 1u : 0u);
-        mma_commit(bar(kBarSFull));
-      };
       bool ok = true;
       int g = 0;
       for (int n = 0; ok; ++n) {
@@ -794,21 +786,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         geom(x, jb, bh, i0, ns);
         const int kv = n & 1;
         const uint32_t kvb = base + kv * kKVBytes;
-        const uint64_t kK = sdesc_sw128(kvb + kKOff, 16, 1024);            // K, K-major
-        const uint64_t kV = sdesc_sw128(kvb + kVOff, 16, 1024);            // V, K-major
+        // K has landed: the S^T MMAs that read it completed before this
+        // step's P and dS were formed
         const uint64_t kKmn = sdesc_sw128(kvb + kKOff, kTileBytes, 1024);  // K as MN-major B
-        ok = mbar_wait(bar(kBarKV + kv), (n >> 1) & 1, abort_flag);
-        if (ok) ok = mbar_wait(bar(kBarQFull + g % kStages), (g / kStages) & 1, abort_flag);
-        if (!ok) break;
-        tc_fence_after();
-        issue_sdp(g, kK, kV);
         for (int it = 0; it < ns && ok; ++it, ++g) {
-          if (it + 1 < ns) {
-            ok = mbar_wait(bar(kBarSFree), g & 1, abort_flag);  // (Q/dO of g+1 have landed too)
-            if (!ok) break;
-            tc_fence_after();
-            issue_sdp(g + 1, kK, kV);
-          }
           // P^T and dS of step g written, dQ of step g-1 (and at an item's
           // first step the previous item's dK, dV) read out of tensor memory
           ok = mbar_wait(bar(kBarDSFull), g & 1, abort_flag);
@@ -835,10 +816,59 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!ok) break;
         mma_commit(bar(kBarDKDV));    // dK, dV of this item are complete
-        mma_commit(bar(kBarKVFree + kv));  // and this K/V buffer may be refilled
+        // and this K/V buffer may be refilled (the item's S^T/dP^T MMAs on
+        // the other issuer completed before its last P and dS were formed)
+        mma_commit(bar(kBarKVFree + kv));
       }
       mma_commit(bar(kBarDrain));
       mbar_wait(bar(kBarDrain), 0, nullptr);
+    }
+  } else if (warp == kSWarp) {
+    // ------------------------------------------------------------ S^T / dP^T issue
+    if (lane == 0) {
+      constexpr uint32_t kIdS = idesc_bf16_f32(kBlk, kBlk, false, false);
+      const uint64_t kQ0 = sdesc_sw128(base + kStageOff, 16, 1024);  // stage 0 Q, K-major
+      constexpr uint64_t kStageStep = kStageBytes >> 4, kTileStep = kTileBytes >> 4;
+      // S^T = K Q^T and dP^T = V dO^T of global step g (both K-major)
+      auto issue_sdp = [&](int g, uint64_t kK, uint64_t kV) {
+        const uint64_t q = kQ0 + (g % kStages) * kStageStep, o = q + kTileStep;
+#pragma unroll
+        for (int kk = 0; kk < kD / 16; ++kk)
+          mma_ss(tmem + kColS, kK + 2 * kk, q + 2 * kk, kIdS, kk > 0 ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < kD / 16; ++kk)
+          mma_ss(tmem + kColDP, kV + 2 * kk, o + 2 * kk, kIdS, kk > 0 ? 1u : 0u);
+        mma_commit(bar(kBarSFull));
+      };
+      bool ok = true;
+      int g = 0;
+      for (int n = 0; ok; ++n) {
+        int x, jb, bh, i0, ns;
+        if (!item_of(n, num_items, &x)) break;
+        geom(x, jb, bh, i0, ns);
+        const int kv = n & 1;
+        const uint32_t kvb = base + kv * kKVBytes;
+        const uint64_t kK = sdesc_sw128(kvb + kKOff, 16, 1024);
+        const uint64_t kV = sdesc_sw128(kvb + kVOff, 16, 1024);
+        ok = mbar_wait(bar(kBarKV + kv), (n >> 1) & 1, abort_flag);
+        if (ok) ok = mbar_wait(bar(kBarQFull + g % kStages), (g / kStages) & 1, abort_flag);
+        if (!ok) break;
+        tc_fence_after();
+        issue_sdp(g, kK, kV);
+        // S^T of every step is released before the next S^T is issued (the
+        // next item's first one included)
+        for (int it = 0; it < ns && ok; ++it, ++g) {
+          ok = mbar_wait(bar(kBarSFree), g & 1, abort_flag);
+          if (!ok) break;
+          if (it + 1 < ns) {
+            tc_fence_after();
+            issue_sdp(g + 1, kK, kV);
+          }
+        }
+      }
+      // Let every MMA this thread issued finish before TMEM is released.
+      mma_commit(bar(kBarDrain + 1));
+      mbar_wait(bar(kBarDrain + 1), 0, nullptr);
     }
   } else if (warp < kDqWarp0) {
     // ------------------------------------------------------------ P and dS
