@@ -11,8 +11,8 @@
 //
 // Three kernels:
 //   fa_bwd_pre   D = rowsum(dO * O) in fp32, and zero the fp32 dQ accumulator
-//   fa_bwd_main  one CTA per (key/value block of 128 keys, batch-head): K_j
-//                and V_j stay in shared memory and dK_j, dV_j accumulate in
+//   fa_bwd_main  per (key/value block of 128 keys, batch-head) item: K_j and
+//                V_j stay in shared memory and dK_j, dV_j accumulate in
 //                tensor memory while the query blocks i stream past; per i
 //                five tcgen05 MMAs:
 //                  S^T  = K_j Q_i^T         (TMEM)
@@ -22,9 +22,11 @@
 //                  dK  += dS^T Q_i          (dS^T read from shared memory)
 //                  dQ_i = dS K_j            (same shared bytes, MN-major)
 //                dQ_i is added into the fp32 accumulator in global memory.
-//                Two variants: fa_bwd_main_d64 (d = d_v = 64: pipelined across
+//                Two variants: fa_bwd_main_d64 (d = d_v = 64: persistent, one
+//                CTA per SM walking its share of the items, pipelined across
 //                query blocks, dQ added by bulk reductions) and fa_bwd_main_seq
-//                (other head sizes: tensor memory too small to pipeline).
+//                (other head sizes, one CTA per item: tensor memory too small
+//                to pipeline).
 //   fa_bwd_post  dQ = bf16(accumulator)
 //
 // The dQ accumulator is fp32 [BH, Npad, d] in a blocked layout: each group
