@@ -29,11 +29,14 @@
 //                to pipeline).
 //   fa_bwd_post  dQ = bf16(accumulator)
 //
-// The dQ accumulator is fp32 [BH, Npad, d] in a blocked layout: each group
-// of 32 rows is stored as d/32 blocks of 32 rows x 32 columns (4 KiB,
-// contiguous), and inside a block the eight 16-byte chunks of a row are
-// rotated by XOR with (row mod 8). A block is then one contiguous bulk
-// reduction from a bank-conflict-free shared staging tile.
+// The dQ accumulator is fp32 [BH, Npad, d] in a blocked layout, per group of
+// 32 rows. With d = 64 (added by bulk reductions) the group is d/32 blocks of
+// 32 rows x 32 columns (4 KiB, contiguous) and inside a block the eight
+// 16-byte chunks of a row are rotated by XOR with (row mod 8): a block is one
+// contiguous bulk reduction from a bank-conflict-free shared staging tile.
+// With d = 128 (added by per-thread 16-byte reductions, thread = row) the
+// group is d/4 runs of 32 rows x one 16-byte chunk, so one warp instruction
+// adds 512 contiguous bytes.
 
 #include <cuda_bf16.h>
 #include <type_traits>
@@ -99,8 +102,12 @@ __device__ __forceinline__ RowMask bwd_row_mask(const BwdArgs& a, int i, int jb,
 // a multiple of 4 when the caller accesses 16 bytes.
 template <int D>
 __host__ __device__ __forceinline__ size_t acc_index(long long bh, int n, int c, int n_pad) {
-  return (static_cast<size_t>(bh) * n_pad + (n & ~31)) * D + static_cast<size_t>(c >> 5) * 1024 +
-         (n & 31) * 32 + (((((c & 31) >> 2) ^ (n & 7))) << 2) + (c & 3);
+  const size_t group = (static_cast<size_t>(bh) * n_pad + (n & ~31)) * D;
+  if constexpr (D == 128)
+    return group + static_cast<size_t>(c >> 2) * 128 + (n & 31) * 4 + (c & 3);
+  else
+    return group + static_cast<size_t>(c >> 5) * 1024 + (n & 31) * 32 +
+           (((((c & 31) >> 2) ^ (n & 7))) << 2) + (c & 3);
 }
 
 // ---------------------------------------------------------------- B0
@@ -495,6 +502,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t g[32];
         tmem_ld32(tmem + lane_base + C::kColDQ + c * 32, g);
         tmem_ld_wait(g);
+        if (c == D / 32 - 1) {  // dQ has left tensor memory: its columns are free
+          tc_fence_before();
+          mbar_arrive(bar(C::kBarDQEmpty));
+        }
         if (q < N) {
 #pragma unroll
           for (int e = 0; e < 32; e += 4)
@@ -504,38 +515,53 @@ __global__ void __launch_bounds__(kThreads, 1)
                        __uint_as_float(g[e + 3]) * scale);
         }
       }
-      tc_fence_before();
-      mbar_arrive(bar(C::kBarDQEmpty));
     }
     if (ok) {
       ok = mbar_wait_sleep(bar(C::kBarDKDV), 0, abort_flag);
       ok = __all_sync(0xffffffffu, ok);
     }
     if (ok) {
+      // dK (x scale) and dV (thread = key row). Each warp swizzles its 32 rows,
+      // 64 columns at a time, into 4 KiB of the query stage 0 buffer (idle:
+      // every MMA has completed) and writes them back four whole 128-byte
+      // lines per store instruction rather than 32 partial lines.
       tc_fence_after();
-      const int key = jb * kBlk + r;
-      const bool live = key < N;
-#pragma unroll
+      const int lw = warp & 3;
+      uint8_t* stage_blk = base_ptr + C::kStageOff + lw * 4096;
+      uint8_t* stage_row = stage_blk + lane * 128;
+      const int key0 = jb * kBlk + lw * 32;  // this warp's first key row
+#pragma unroll 1
       for (int which = 0; which < 2; ++which) {
         const uint32_t col = which == 0 ? C::kColDK : C::kColDV;
         const float mul = which == 0 ? scale : 1.f;
         const int width = which == 0 ? D : DV;
-        __nv_bfloat16* out =
-            (which == 0 ? args.dk : args.dv) + (static_cast<size_t>(bh) * N + key) * width;
+        __nv_bfloat16* out = (which == 0 ? args.dk : args.dv) + static_cast<size_t>(bh) * N * width;
+        for (int h = 0; h < width / 64; ++h) {
 #pragma unroll
-        for (int c = 0; c < width / 32; ++c) {
-          uint32_t g[32];
-          tmem_ld32(tmem + lane_base + col + c * 32, g);
-          tmem_ld_wait(g);
-          uint32_t pk[16];
+          for (int c = 0; c < 2; ++c) {
+            uint32_t g[32];
+            tmem_ld32(tmem + lane_base + col + h * 64 + c * 32, g);
+            tmem_ld_wait(g);
+            uint32_t pk[16];
 #pragma unroll
-          for (int e = 0; e < 16; ++e)
-            pk[e] = pack_bf16(__uint_as_float(g[2 * e]) * mul, __uint_as_float(g[2 * e + 1]) * mul);
-          if (live) {
-            uint4* o4 = reinterpret_cast<uint4*>(out + c * 32);
+            for (int e = 0; e < 16; ++e)
+              pk[e] = pack_bf16(__uint_as_float(g[2 * e]) * mul, __uint_as_float(g[2 * e + 1]) * mul);
+            // 16-byte chunks 4c..4c+3 of row `lane`, chunk v in slot v ^ (lane & 7)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) o4[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+            for (int e = 0; e < 4; ++e)
+              *reinterpret_cast<uint4*>(stage_row + (((4 * c + e) ^ (lane & 7)) * 16)) =
+                  make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
           }
+          __syncwarp();
+          // instruction j: lanes 8r'..8r'+7 write the eight chunks of row 4j + r'
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const int rr = 4 * j + (lane >> 3), v = lane & 7;
+            const uint4 val = *reinterpret_cast<const uint4*>(stage_blk + rr * 128 + ((v ^ (rr & 7)) * 16));
+            if (key0 + rr < N)
+              *reinterpret_cast<uint4*>(out + static_cast<size_t>(key0 + rr) * width + h * 64 + v * 8) = val;
+          }
+          __syncwarp();  // the block is read back before it is written again
         }
       }
     }
