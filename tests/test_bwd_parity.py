@@ -96,6 +96,20 @@ def test_fwdbwd_workload_full_size():
     assert float(vsum.abs().max()) <= 2e-2 * float(dv.abs().sum(dim=2).max())
 
 
+@pytest.mark.parametrize("causal", [True, False])
+def test_many_items_per_cta(causal):
+    # 4 x 64 heads x 3 key blocks = 768 (key block, head) items, about five per
+    # CTA of the persistent d = 64 kernel: exercises the alternating K/V
+    # buffers, the hand-offs between items and the guarded write-back of a
+    # ragged last block (N = 333), compared in full.
+    x = si.make_small(4, 64, 333, 64, seed=77 + int(causal), with_grad=True)
+    scale = 0.125
+    grads = _run(x, causal, scale)
+    o_ref, lse_ref = dense.forward(x["q"], x["k"], x["v"], causal, scale)
+    refs = dense.backward(x["q"], x["k"], x["v"], o_ref, lse_ref, x["do"], causal, scale)
+    _check(grads, refs)
+
+
 def test_larger_scale_and_ragged():
     x = si.make_small(1, 2, 777, 64, seed=31, k_mult=3.0, with_grad=True)
     for causal in (False, True):

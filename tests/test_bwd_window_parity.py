@@ -50,6 +50,26 @@ def test_windowed_backward_matches_oracle(B, H, N, d, window):
         assert rel <= REL, (name, rel)
 
 
+def test_windowed_backward_many_items_per_cta():
+    # 4 x 24 heads x 5 key blocks = 480 items, about three per CTA of the
+    # persistent d = 64 kernel, each stopping at the last query block its
+    # window reaches; ragged last block; compared on every head.
+    B, H, N, d, window = 4, 24, 600, 64, 150
+    x = si.make_small(B, H, N, d, seed=91, with_grad=True)
+    g = {k: t.cuda() for k, t in x.items()}
+    scale = 0.125
+    o, lse = fa.fa_fwd_ex(g["q"], g["k"], g["v"], causal=True, window=window, scale=scale)
+    dq, dk, dv = fa.fa_bwd_ex(g["q"], g["k"], g["v"], o, lse, g["do"], causal=True, window=window,
+                              scale=scale)
+    torch.cuda.synchronize()
+    assert fa.fa_get_last_device_status() == fa.FA_OK
+    o_ref, lse_ref = general.forward(x["q"], x["k"], x["v"], True, scale, window)
+    ref = general.backward(x["q"], x["k"], x["v"], o_ref, lse_ref, x["do"], True, scale, window)
+    for name, got, r in zip(("dq", "dk", "dv"), (dq, dk, dv), ref):
+        rel = np.abs(got.float().cpu().double().numpy() - r).max() / np.abs(r).max()
+        assert rel <= REL, (name, rel)
+
+
 def test_wide_window_backward_equals_causal_backward():
     x = si.make_small(1, 2, 600, 64, seed=3, with_grad=True)
     g = {k: t.cuda() for k, t in x.items()}
