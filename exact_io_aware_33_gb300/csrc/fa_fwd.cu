@@ -49,24 +49,30 @@ namespace {
 
 constexpr int kBlockM = 128;
 constexpr int kBlockN = 128;
-constexpr int kQTiles = 2;
-constexpr int kSoftmaxThreads = 128 * kQTiles;
-constexpr int kMmaWarp = kSoftmaxThreads / 32;
-constexpr int kLoadWarp = kMmaWarp + 1;
-constexpr int kThreads = kSoftmaxThreads + 64;   // + the MMA warp and the TMA warp
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr float kLn2 = 0.6931471805599453f;
 
-// D: head size of Q and K; DV: head size of V and O.
-template <int D, int DV>
+// D: head size of Q and K; DV: head size of V and O; QT: 128-row query tiles
+// per CTA. QT = 2 shares each K/V tile between two query tiles; QT = 1 (used
+// at d = d_v = 64) needs half the tensor memory and shared memory, so two
+// CTAs share an SM and one's start-up and write-back overlap the other's
+// key loop.
+template <int D, int DV, int QT = 2>
 struct FwdCfg {
+  static constexpr int kQTiles = QT;
+  static constexpr int kSoftmaxThreads = 128 * QT;
+  static constexpr int kMmaWarp = kSoftmaxThreads / 32;
+  static constexpr int kLoadWarp = kMmaWarp + 1;
+  static constexpr int kThreads = kSoftmaxThreads + 64;  // + the MMA warp and the TMA warp
+  static constexpr int kCtasPerSm = QT == 1 ? 2 : 1;
   static constexpr int kChunks = D / 64;
   static constexpr int kChunksV = DV / 64;
   static constexpr int kChunkBytes = kBlockM * 64 * 2;        // 16 KiB
   static constexpr int kTileBytes = kChunks * kChunkBytes;    // 128 rows x d (Q, K)
   static constexpr int kVTileBytes = kChunksV * kChunkBytes;  // 128 rows x d_v (V)
-  // K/V ring depth: as many stages as fit next to the two Q tiles
-  static constexpr int kStages = (D == 64 && DV == 64) ? 4 : (D + DV == 192 ? 3 : 2);
+  // K/V ring depth: as many stages as fit next to the Q tiles (QT = 1: two
+  // CTAs per SM)
+  static constexpr int kStages = QT == 1 ? 2 : (D == 64 && DV == 64) ? 4 : (D + DV == 192 ? 3 : 2);
   static constexpr int kQOff = 0;
   static constexpr int kKOff = kQOff + kQTiles * kTileBytes;
   static constexpr int kVOff = kKOff + kStages * kTileBytes;
@@ -86,15 +92,15 @@ struct FwdCfg {
   static constexpr int kNumBars = kBarDrain + 1;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kSmemBytes = kMiscOff + 16 + 1024;  // + slack to align the base
-  static constexpr uint32_t kTmemCols = 512;
-  static constexpr uint32_t kColO = 256;
+  static constexpr uint32_t kTmemCols = 256 * QT;
+  static constexpr uint32_t kColO = 128 * QT;
   // With d_v = 64 the two S tiles and two O accumulators take 384 columns,
   // so each tile's P gets 64 columns of its own at kColP: the softmax
   // releases S as soon as it has loaded it and the next tile's QK^T
   // overlaps the exponentials. With d_v = 128 the columns are full and P
   // overwrites S.
   static constexpr bool kSepP = (DV == 64);
-  static constexpr uint32_t kColP = 256 + 2 * DV;
+  static constexpr uint32_t kColP = kColO + QT * DV;
   static_assert(kSmemBytes <= 232448, "forward tiles exceed shared memory");
 };
 
@@ -115,11 +121,14 @@ struct FwdArgs {
   float scale_log2;    // scale * log2(e), > 0
 };
 
-template <int D, int DV>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int D, int DV, int QT>
+__global__ void __launch_bounds__(FwdCfg<D, DV, QT>::kThreads, FwdCfg<D, DV, QT>::kCtasPerSm)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const FwdArgs args) {
-  using C = FwdCfg<D, DV>;
+  using C = FwdCfg<D, DV, QT>;
+  constexpr int kQTiles = C::kQTiles;
+  constexpr int kMmaWarp = C::kMmaWarp;
+  constexpr int kLoadWarp = C::kLoadWarp;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_u32 = smem_u32(smem_raw);
   const uint32_t base = (raw_u32 + 1023u) & ~1023u;
@@ -169,7 +178,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_stream = j_end - j_first;
   // stream steps [a_t, b_t) of each query tile (empty when n_t = 0)
   const int a0 = lo_t[0] - j_first, b0 = a0 + n_t[0];
-  const int a1 = lo_t[1] - j_first, b1 = a1 + n_t[1];
+  // (one query tile: tile "1" is empty)
+  const int a1 = kQTiles > 1 ? lo_t[kQTiles - 1] - j_first : 0;
+  const int b1 = kQTiles > 1 ? a1 + n_t[kQTiles - 1] : 0;
 
   const int warp = warp_id();
   const int lane = lane_id();
@@ -441,8 +452,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp < kMmaWarp) {
     // ------------------------------------------------------------ softmax
     const int t = warp / 4;
-    const int n_mine = t == 0 ? n_t[0] : n_t[1];
-    const int tile_row0 = t == 0 ? q_row0[0] : q_row0[1];
+    const int n_mine = t == 0 ? n_t[0] : n_t[kQTiles - 1];
+    const int tile_row0 = t == 0 ? q_row0[0] : q_row0[kQTiles - 1];
     const int key_tile0 = j_first + (t == 0 ? a0 : a1);  // first key tile of this query tile
     const int row = tile_row0 + (threadIdx.x & 127);
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
@@ -702,10 +713,10 @@ __global__ void __launch_bounds__(256) fa_merge_splits(const float* __restrict__
   }
 }
 
-template <int D, int DV>
+template <int D, int DV, int QT>
 int launch_fwd_d(const FwdProblem& p, void* o, float* lse, float* part_o, float* part_lse,
                  int n_splits, cudaStream_t stream) {
-  using C = FwdCfg<D, DV>;
+  using C = FwdCfg<D, DV, QT>;
   const int BH = p.B * p.H;
   CUtensorMap mq, mk, mv;
   if (!make_map_bhnd(&mq, p.q, BH, p.Nq, D) || !make_map_bhnd(&mk, p.k, BH, p.Nk, D) ||
@@ -713,9 +724,9 @@ int launch_fwd_d(const FwdProblem& p, void* o, float* lse, float* part_o, float*
     return -3;
   int* status = device_status_word();
   if (!status) return -3;
-  auto kern = fa_fwd_kernel<D, DV>;
-  // attribute slots 0, 1, 4, 5 (the backward uses 2, 3, 6-8)
-  constexpr int kSlot = (D == 64 ? 0 : 1) + (DV == 64 ? 0 : 4);
+  auto kern = fa_fwd_kernel<D, DV, QT>;
+  // attribute slots 0, 1, 4, 5 and 9 (the backward uses 2, 3, 6-8)
+  constexpr int kSlot = QT == 1 ? 9 : (D == 64 ? 0 : 1) + (DV == 64 ? 0 : 4);
   if (!ensure_smem_attr(reinterpret_cast<const void*>(kern), C::kSmemBytes, kSlot))
     return -3;
   const int n_kv = (p.Nk + kBlockN - 1) / kBlockN;
@@ -735,7 +746,7 @@ int launch_fwd_d(const FwdProblem& p, void* o, float* lse, float* part_o, float*
   a.window = p.window;
   a.BH = BH;
   a.causal = p.causal ? 1 : 0;
-  a.num_pairs = (p.Nq + kBlockM * kQTiles - 1) / (kBlockM * kQTiles);
+  a.num_pairs = (p.Nq + kBlockM * QT - 1) / (kBlockM * QT);
   a.split_tiles = split_tiles;
   a.split_mode = part_o != nullptr ? 1 : 0;
   // scale 0 (uniform weights) runs as a tiny positive scale: exp2 of a
@@ -745,7 +756,7 @@ int launch_fwd_d(const FwdProblem& p, void* o, float* lse, float* part_o, float*
   const long long gx = static_cast<long long>(a.num_pairs) * BH;
   if (gx > 0x7fffffffLL || n_splits > 65535) return -1;
   const dim3 grid(static_cast<unsigned>(gx), a.split_mode ? n_splits : 1);
-  kern<<<grid, kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, a);
+  kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, a);
   if (cudaGetLastError() != cudaSuccess) return -3;
   if (a.split_mode) {
     constexpr int kRowsPerCta = 256 / (DV / 8);
@@ -792,10 +803,14 @@ int fwd_split_count(const FwdProblem& p, int n_splits, int sms) {
 
 int launch_fwd_general(const FwdProblem& p, void* o, float* lse, float* part_o, float* part_lse,
                        int n_splits, cudaStream_t stream) {
-  if (p.d == 64 && p.dv == 64) return launch_fwd_d<64, 64>(p, o, lse, part_o, part_lse, n_splits, stream);
-  if (p.d == 128 && p.dv == 128) return launch_fwd_d<128, 128>(p, o, lse, part_o, part_lse, n_splits, stream);
-  if (p.d == 128 && p.dv == 64) return launch_fwd_d<128, 64>(p, o, lse, part_o, part_lse, n_splits, stream);
-  if (p.d == 64 && p.dv == 128) return launch_fwd_d<64, 128>(p, o, lse, part_o, part_lse, n_splits, stream);
+  if (p.d == 64 && p.dv == 64) {
+    if (part_o == nullptr)  // one query tile per CTA, two CTAs per SM
+      return launch_fwd_d<64, 64, 1>(p, o, lse, part_o, part_lse, n_splits, stream);
+    return launch_fwd_d<64, 64, 2>(p, o, lse, part_o, part_lse, n_splits, stream);
+  }
+  if (p.d == 128 && p.dv == 128) return launch_fwd_d<128, 128, 2>(p, o, lse, part_o, part_lse, n_splits, stream);
+  if (p.d == 128 && p.dv == 64) return launch_fwd_d<128, 64, 2>(p, o, lse, part_o, part_lse, n_splits, stream);
+  if (p.d == 64 && p.dv == 128) return launch_fwd_d<64, 128, 2>(p, o, lse, part_o, part_lse, n_splits, stream);
   return -2;
 }
 
