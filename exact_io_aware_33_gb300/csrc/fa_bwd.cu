@@ -589,8 +589,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 // Two threads issue tensor-core work, each waiting on one barrier per
 // query block:
 //   warp 14: S^T_{i+1}, dP^T_{i+1}   (once the warpgroups hold S^T_i, dP^T_i)
-//   warp 12: dV += P^T_i dO_i, dK += dS^T_i Q_i, then dQ_i = dS_i K
-//            (once P_i and dS_i are written and dQ_{i-1} has been read out)
+//   warp 12: dQ_i = dS_i K, then dV += P^T_i dO_i, dK += dS^T_i Q_i
+//            (once P_i and dS_i are written and dQ_{i-1} has been read out;
+//            dQ first, so that its read-out, which gates the next query
+//            block's dV/dK/dQ, starts as early as possible)
 // dQ_i is added to the fp32 accumulator by the dQ warpgroup through
 // per-warp 4 KiB shared staging tiles and bulk reductions (full 128-byte
 // lines, no per-thread atomics).
@@ -825,6 +827,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           const uint64_t qmn = kQmn0 + (g % kStages) * kStageStep, omn = qmn + kTileStep;
           const uint64_t dsk = kDS0, dsmn = kDSmn0;
+          // dQ = dS K first, so the dQ warpgroup starts reading it out sooner
+          // (A = dS MN-major: the same bytes as dS^T, B = K MN-major)
+#pragma unroll
+          for (int kk = 0; kk < kBlk / 16; ++kk)
+            mma_ss(tmem + kColDQ, dsmn + 128 * kk, kKmn + 128 * kk, kIdQ, kk > 0 ? 1u : 0u);
+          mma_commit(bar(kBarDQFull));
           // dV += P^T dO   (A = P^T bf16 pairs in TMEM, B = dO MN-major, 16 rows per step)
 #pragma unroll
           for (int kk = 0; kk < kBlk / 16; ++kk)
@@ -835,11 +843,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_ss(tmem + kColDK, dsk + (kk >> 2) * kTileStep + (kk & 3) * 2, qmn + 128 * kk, kIdKV,
                    (it > 0 || kk > 0) ? 1u : 0u);
           mma_commit(bar(kBarPFree));
-          // dQ = dS K      (A = dS MN-major: the same bytes, B = K MN-major)
-#pragma unroll
-          for (int kk = 0; kk < kBlk / 16; ++kk)
-            mma_ss(tmem + kColDQ, dsmn + 128 * kk, kKmn + 128 * kk, kIdQ, kk > 0 ? 1u : 0u);
-          mma_commit(bar(kBarDQFull));  // (dS may be overwritten too)
           mma_commit(bar(kBarQEmpty + g % kStages));
         }
         if (!ok) break;
@@ -1002,10 +1005,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
       }
       tmem_st32(tP, pp);
-      // dS^T row of this key into the dS buffer once step g-1's dK and dQ
-      // MMAs have read it (dQ complete): 64 queries -> eight swizzled 16-byte chunks
+      // dS^T row of this key into the dS buffer once step g-1's dQ and dK
+      // MMAs have read it: 64 queries -> eight swizzled 16-byte chunks
       if (g >= 1) {
-        ok = mbar_wait(bar(kBarDQFull), (g - 1) & 1, abort_flag);
+        ok = mbar_wait(bar(kBarDQFull), (g - 1) & 1, abort_flag);  // dK read it before PFree (above)
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
       }
