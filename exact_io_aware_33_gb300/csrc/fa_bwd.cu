@@ -186,7 +186,8 @@ __global__ void __launch_bounds__(256) fa_bwd_post(const float* __restrict__ acc
 // With d = 128 (or d_v = 128) the five accumulators (S^T, dP^T, dQ, dK, dV) need 640
 // tensor-memory columns of the 512, so dQ shares the dP^T columns and each
 // query step runs in sequence: S^T / dP^T (one query half at a time), P/dS,
-// dV / dK, then dQ, whose read-out must finish before the next dP^T.
+// dV / dK of the first half, dQ (as soon as both dS halves are written),
+// dV / dK of the second half; dQ's read-out must finish before the next dP^T.
 //
 // CTA (512 threads):
 //   warps 0-7  two P/dS warpgroups: thread = key row = TMEM lane; warpgroup
@@ -389,6 +390,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = mbar_wait_sleep(bar(C::kBarDSFull + h), it & 1, abort_flag);
           if (!ok) break;
           tc_fence_after();
+          if (h == 1) {
+            // dQ as soon as both dS halves are written: its read-out gates the
+            // next step (dQ shares the dP^T columns at d = 128)
+            if (!C::kDqAliasDp && it > 0) {
+              ok = mbar_wait_sleep(bar(C::kBarDQEmpty), (it - 1) & 1, abort_flag);
+              if (!ok) break;
+              tc_fence_after();
+            }
+            // dQ = dS K          (A = dS MN-major in smem, B = K MN-major)
+#pragma unroll
+            for (int kk = 0; kk < kBlk / 16; ++kk)
+              mma_ss(tmem + C::kColDQ, sdesc_sw128(dsb + kk * 2048, C::kChunkBytes, 1024),
+                     sdesc_sw128(kb + kk * 2048, C::kChunkBytes, 1024), kIdQ, kk > 0 ? 1u : 0u);
+            mma_commit(bar(C::kBarDQFull));
+          }
           // dV += P_h^T dO_h   (A = P^T in TMEM, B = dO rows of half h, MN-major)
 #pragma unroll
           for (int kk = 0; kk < kHalf / 16; ++kk)
@@ -403,17 +419,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                    (it > 0 || h > 0 || kk > 0) ? 1u : 0u);
         }
         if (!ok) break;
-        if (!C::kDqAliasDp && it > 0) {
-          ok = mbar_wait_sleep(bar(C::kBarDQEmpty), (it - 1) & 1, abort_flag);
-          if (!ok) break;
-          tc_fence_after();
-        }
-        // dQ = dS K          (A = dS MN-major in smem, B = K MN-major)
-#pragma unroll
-        for (int kk = 0; kk < kBlk / 16; ++kk)
-          mma_ss(tmem + C::kColDQ, sdesc_sw128(dsb + kk * 2048, C::kChunkBytes, 1024),
-                 sdesc_sw128(kb + kk * 2048, C::kChunkBytes, 1024), kIdQ, kk > 0 ? 1u : 0u);
-        mma_commit(bar(C::kBarDQFull));
         mma_commit(bar(C::kBarQEmpty + s));
       }
       if (ok) mma_commit(bar(C::kBarDKDV));
