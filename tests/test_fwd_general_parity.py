@@ -93,6 +93,20 @@ def test_decode_splitkv_matches_oracle(B, H, Nq, Nk, d, causal, window, splits):
     assert (lse - lse1).abs().max().item() <= 1e-3
 
 
+@pytest.mark.parametrize("causal,window", [(True, 0), (True, 200), (False, 0)])
+def test_fwd_ex_many_ctas_per_sm(causal, window):
+    # d = 64 runs one query tile per CTA, two CTAs per SM: 4 x 32 heads x 3
+    # query tiles = 384 CTAs of different key ranges (offset diagonal, window,
+    # ragged tails) share the SMs; every head compared.
+    B, H, Nq, Nk, d = 4, 32, 333, 800, 64
+    q, k, v = _inputs(B, H, Nq, Nk, d, seed=901 + window + int(causal))
+    scale = 0.125
+    o, lse = fa.fa_fwd_ex(q.cuda(), k.cuda(), v.cuda(), causal=causal, window=window, scale=scale)
+    torch.cuda.synchronize()
+    assert fa.fa_get_last_device_status() == fa.FA_OK
+    _check(o, lse, q, k, v, causal, window, scale)
+
+
 def test_fwd_ex_square_equals_fa_fwd():
     q, k, v = _inputs(2, 3, 777, 777, 64, seed=5)
     a = fa.fa_fwd(q.cuda(), k.cuda(), v.cuda(), causal=True)
