@@ -47,6 +47,7 @@ _P = ctypes.c_void_p
 _I = ctypes.c_int
 _F = ctypes.c_float
 _S = ctypes.c_size_t
+_U64 = ctypes.c_ulonglong
 SIGNATURES = {
     "fa_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F]),
     "fa_fwd_stream": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P]),
@@ -62,6 +63,9 @@ SIGNATURES = {
     "fa_decode_splitkv": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P, _S, _P]),
     "fa_decode_num_splits": (_I, [_I, _I, _I, _I, _I]),
     "fa_decode_workspace_bytes": (_S, [_I, _I, _I, _I, _I, _I]),
+    "fa_fwd_dropout": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _F, _U64, _U64, _P]),
+    "fa_bwd_dropout": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _F, _U64, _U64,
+                            _P, _S, _P]),
     "fa_strerror": (ctypes.c_char_p, [_I]),
     "fa_get_last_device_status": (_I, []),
     "fa_version": (_I, []),
@@ -329,4 +333,63 @@ def fa_bwd_ex(q, k, v, o, lse, do, causal: bool = False, window: int = 0,
                            float(scale), _ptr(workspace), ctypes.c_size_t(workspace.numel()),
                            _stream_handle(stream, q.device))
     _check(rc, "fa_bwd_ex")
+    return dq, dk, dv
+
+
+def fa_fwd_dropout(q, k, v, dropout_p: float, seed: int, offset: int = 0, causal: bool = False,
+                   scale: float | None = None, out=None, lse=None, stream=None):
+    """Forward with dropout on the probabilities; returns (o, lse). The mask
+    is a function of (seed, offset, batch-head, query, key) only."""
+    import torch
+    if q.dim() != 4:
+        raise ValueError("q must be [B, H, N, d]")
+    B, H, N, d = q.shape
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _check_tensor(t, name, (B, H, N, d), torch.bfloat16)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    out = torch.empty_like(q) if out is None else out
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    _check_tensor(out, "out", (B, H, N, d), torch.bfloat16)
+    _check_tensor(lse, "lse", (B, H, N), torch.float32)
+    lib = load_library()
+    with torch.cuda.device(q.device):
+        rc = lib.fa_fwd_dropout(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, N, d,
+                                int(bool(causal)), float(scale), float(dropout_p), int(seed),
+                                int(offset), _stream_handle(stream, q.device))
+    _check(rc, "fa_fwd_dropout")
+    return out, lse
+
+
+def fa_bwd_dropout(q, k, v, o, lse, do, dropout_p: float, seed: int, offset: int = 0,
+                   causal: bool = False, scale: float | None = None, dq=None, dk=None, dv=None,
+                   workspace=None, stream=None):
+    """Backward of fa_fwd_dropout for the same (dropout_p, seed, offset); returns (dq, dk, dv)."""
+    import torch
+    if q.dim() != 4:
+        raise ValueError("q must be [B, H, N, d]")
+    B, H, N, d = q.shape
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("do", do)):
+        _check_tensor(t, name, (B, H, N, d), torch.bfloat16)
+    _check_tensor(lse, "lse", (B, H, N), torch.float32)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
+        _check_tensor(t, name, (B, H, N, d), torch.bfloat16)
+    lib = load_library()
+    need = lib.fa_bwd_workspace_bytes(B, H, N, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    if workspace.numel() < need:
+        raise ValueError(f"workspace needs {need} bytes")
+    with torch.cuda.device(q.device):
+        rc = lib.fa_bwd_dropout(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do), _ptr(dq),
+                                _ptr(dk), _ptr(dv), B, H, N, d, int(bool(causal)), float(scale),
+                                float(dropout_p), int(seed), int(offset), _ptr(workspace),
+                                ctypes.c_size_t(workspace.numel()), _stream_handle(stream, q.device))
+    _check(rc, "fa_bwd_dropout")
     return dq, dk, dv

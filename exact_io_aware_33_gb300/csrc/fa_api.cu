@@ -271,6 +271,62 @@ int fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const 
   return rc;
 }
 
+namespace {
+
+// Dropout parameters after checks: FA_ERR_INVALID unless 0 <= p < 1.
+int make_dropout(float p, unsigned long long seed, unsigned long long offset, fa::Dropout* out) {
+  if (!(p >= 0.f && p < 1.f)) return FA_ERR_INVALID;
+  long t = lrintf(256.f * p);
+  if (t > 255) t = 255;
+  out->t = static_cast<uint32_t>(t);
+  out->inv_keep = 256.f / static_cast<float>(256 - t);
+  out->seed_lo = static_cast<uint32_t>(seed & 0xffffffffull);
+  out->seed_hi = static_cast<uint32_t>(seed >> 32);
+  out->offset = static_cast<uint32_t>(offset & 0xffffffffull);
+  return FA_OK;
+}
+
+}  // namespace
+
+int fa_fwd_dropout(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                   int N, int d, int causal, float scale, float dropout_p, unsigned long long seed,
+                   unsigned long long offset, void* cuda_stream) {
+  fa::Dropout drop;
+  int rc = make_dropout(dropout_p, seed, offset, &drop);
+  if (rc != FA_OK) return rc;
+  bool empty = false;
+  rc = fa::check_problem(B, H, N, d, scale, &empty);
+  if (rc != FA_OK || empty) return rc;
+  if (!fa::aligned16(q) || !fa::aligned16(k) || !fa::aligned16(v) || !fa::aligned16(o) ||
+      !fa::aligned16(lse))
+    return FA_ERR_INVALID;
+  fa::DeviceState* st = nullptr;
+  rc = fa::current_device(&st);
+  if (rc != FA_OK) return rc;
+  Problem p{q, k, v, B, H, N, d, causal, scale};
+  p.drop = drop;
+  return fa::launch_fwd(p, o, lse, static_cast<cudaStream_t>(cuda_stream));
+}
+
+int fa_bwd_dropout(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                   const void* dO, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+                   int causal, float scale, float dropout_p, unsigned long long seed,
+                   unsigned long long offset, void* workspace, size_t ws_bytes, void* cuda_stream) {
+  fa::Dropout drop;
+  int rc = make_dropout(dropout_p, seed, offset, &drop);
+  if (rc != FA_OK) return rc;
+  bool empty = false;
+  rc = check_bwd(B, H, N, d, scale, {q, k, v, o, lse, dO, dq, dk, dv}, workspace, ws_bytes, &empty);
+  if (rc != FA_OK || empty) return rc;
+  const cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+  Problem p{q, k, v, B, H, N, d, causal, scale};
+  p.drop = drop;
+  rc = fa::launch_bwd_pre(p, o, lse, dO, workspace, st);
+  if (rc == FA_OK) rc = fa::launch_bwd_main(p, dO, dk, dv, workspace, st);
+  if (rc == FA_OK) rc = fa::launch_bwd_post(p, dq, workspace, st);
+  return rc;
+}
+
 int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
            const void* dO, void* dq, void* dk, void* dv, int B, int H, int N, int d, int causal,
            float scale) {

@@ -67,6 +67,7 @@ struct BwdArgs {
   int n_blocks;
   float scale;
   float scale_log2;
+  Dropout drop;        // kDrop kernels only (drop.inv_keep also scales dV)
 };
 
 // One past the last query block that sees a key of key block jb: with a
@@ -253,7 +254,9 @@ struct BwdCfg {
   static_assert(kColDV + DV <= kTmemCols, "backward accumulators exceed tensor memory");
 };
 
-template <int D, int DV>
+// kDrop: dropout on the probabilities (see Dropout): dV and dS use the kept
+// probabilities, dS the kept and rescaled dP.
+template <int D, int DV, bool kDrop>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_bwd_main_seq(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
@@ -458,10 +461,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld_wait(sr);
         tmem_ld_wait(dr);
         uint32_t pp[16], dd[16];
+        uint32_t kb[4];  // dropout: keep bytes of this key for the current 16 queries
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
           const int ql = c * 32 + e;            // query column within this half
           const int qc = kHalf * w + ql;        // ... within the block
+          if constexpr (kDrop) {
+            if ((e & 15) == 0)
+              keep_bytes_quad<false>(static_cast<uint32_t>((jb * kBlk + key_row) >> 2),
+                                     static_cast<uint32_t>(((i0 + it) * kBlk + qc) >> 2),
+                                     static_cast<uint32_t>(bh), args.drop.offset, args.drop.seed_lo,
+                                     args.drop.seed_hi, kb);
+          }
           const float2 nl = *reinterpret_cast<const float2*>(nlse2_s + ql);
           const float2 nd = *reinterpret_cast<const float2*>(nd_s + ql);
           const float2 a = __ffma2_rn(make_float2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])),
@@ -471,9 +482,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (qc < rm.qc_lo || qc >= rm.qc_hi) p.x = 0.f;
             if (qc + 1 < rm.qc_lo || qc + 1 >= rm.qc_hi) p.y = 0.f;
           }
-          const float2 g = __fmul2_rn(
-              p, __fadd2_rn(make_float2(__uint_as_float(dr[e]), __uint_as_float(dr[e + 1])), nd));
-          pp[e >> 1] = pack_bf16(p.x, p.y);
+          float2 dpv = make_float2(__uint_as_float(dr[e]), __uint_as_float(dr[e + 1]));
+          float2 pk = p;
+          if constexpr (kDrop) {  // queries e, e + 1: bytes (e & 3), (e & 3) + 1 of group (e >> 2) & 3
+            const uint32_t word = kb[(e >> 2) & 3] >> ((e & 3) * 8);
+            const float ik = args.drop.inv_keep;
+            if ((word & 0xffu) < args.drop.t) { pk.x = 0.f; dpv.x = 0.f; } else { dpv.x *= ik; }
+            if (((word >> 8) & 0xffu) < args.drop.t) { pk.y = 0.f; dpv.y = 0.f; } else { dpv.y *= ik; }
+          }
+          const float2 g = __fmul2_rn(p, __fadd2_rn(dpv, nd));
+          pp[e >> 1] = pack_bf16(pk.x, pk.y);
           dd[e >> 1] = pack_bf16(g.x, g.y);
         }
         tmem_st16(tS + c * 16, pp);
@@ -538,7 +556,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
       for (int which = 0; which < 2; ++which) {
         const uint32_t col = which == 0 ? C::kColDK : C::kColDV;
-        const float mul = which == 0 ? scale : 1.f;
+        const float mul = which == 0 ? scale : args.drop.inv_keep;
         const int width = which == 0 ? D : DV;
         __nv_bfloat16* out = (which == 0 ? args.dk : args.dv) + static_cast<size_t>(bh) * N * width;
         for (int h = 0; h < width / 64; ++h) {
@@ -696,6 +714,7 @@ __device__ __forceinline__ bool item_of(int k, int num_items, int* x) {
   return v < num_items;
 }
 
+template <bool kDrop>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_bwd_main_d64(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
@@ -962,10 +981,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       // A compile-time kind keeps the unmasked blocks free of per-element tests.
       auto half = [&](auto kind, const uint32_t (&sr)[32], const uint32_t (&dr)[32], int c) {
         constexpr int kKind = decltype(kind)::value;
+        uint32_t kb[4];  // dropout: keep bytes of this key for the current 16 queries
 #pragma unroll
         for (int e = 0; e < 32; e += 4) {
           const int ql = c * 32 + e;     // query column within this warpgroup's half
           const int qc = 64 * w + ql;    // ... within the query block
+          if constexpr (kDrop) {
+            if ((e & 15) == 0)
+              keep_bytes_quad<false>(static_cast<uint32_t>((jb * kBlk + key_row) >> 2),
+                                     static_cast<uint32_t>(((i0 + it) * kBlk + qc) >> 2),
+                                     static_cast<uint32_t>(bh), args.drop.offset, args.drop.seed_lo,
+                                     args.drop.seed_hi, kb);
+          }
           const float4 nl = *reinterpret_cast<const float4*>(nlse2_s + ql);
           const float4 nd = *reinterpret_cast<const float4*>(nd_s + ql);
 #pragma unroll
@@ -984,9 +1011,16 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (qc + 2 * u < key_row) p.x = 0.f;
               if (qc + 2 * u + 1 < key_row) p.y = 0.f;
             }
-            const float2 gs = __fmul2_rn(
-                p, __fadd2_rn(make_float2(__uint_as_float(dr[x]), __uint_as_float(dr[x + 1])), nd2));
-            pp[(ql >> 1) + u] = pack_bf16(p.x, p.y);
+            float2 dpv = make_float2(__uint_as_float(dr[x]), __uint_as_float(dr[x + 1]));
+            float2 pk = p;
+            if constexpr (kDrop) {  // queries x, x + 1: bytes 2u, 2u + 1 of group (e >> 2) & 3
+              const uint32_t word = kb[(e >> 2) & 3] >> (16 * u);
+              const float ik = args.drop.inv_keep;
+              if ((word & 0xffu) < args.drop.t) { pk.x = 0.f; dpv.x = 0.f; } else { dpv.x *= ik; }
+              if (((word >> 8) & 0xffu) < args.drop.t) { pk.y = 0.f; dpv.y = 0.f; } else { dpv.y *= ik; }
+            }
+            const float2 gs = __fmul2_rn(p, __fadd2_rn(dpv, nd2));
+            pp[(ql >> 1) + u] = pack_bf16(pk.x, pk.y);
             dd[(ql >> 1) + u] = pack_bf16(gs.x, gs.y);
           }
         }
@@ -1101,7 +1135,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
       for (int which = 0; which < 2; ++which) {
         const uint32_t col = which == 0 ? kColDK : kColDV;
-        const float mul = which == 0 ? scale : 1.f;
+        const float mul = which == 0 ? scale : args.drop.inv_keep;
 #pragma unroll
         for (int c = 0; c < kD / 32; ++c) {
           uint32_t gr[32];
@@ -1202,14 +1236,15 @@ BwdArgs make_args(const Problem& p, const Workspace& w, void* dk, void* dv, int*
   a.n_blocks = w.n_pad / kBlk;
   a.scale = p.scale;
   a.scale_log2 = p.scale * kLog2e;
+  a.drop = p.drop;
   return a;
 }
 
-template <int D, int DV>
+template <int D, int DV, bool kDrop = false>
 bool launch_seq(long long grid, int slot, const CUtensorMap& mq, const CUtensorMap& mk,
                 const CUtensorMap& mv, const CUtensorMap& mdo, const BwdArgs& a, cudaStream_t stream) {
   using C = wide::BwdCfg<D, DV>;
-  auto kern = wide::fa_bwd_main_seq<D, DV>;
+  auto kern = wide::fa_bwd_main_seq<D, DV, kDrop>;
   if (!ensure_smem_attr(reinterpret_cast<const void*>(kern), C::kSmemBytes, slot)) return false;
   kern<<<static_cast<unsigned>(grid), wide::kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, mdo, a);
   return true;
@@ -1229,17 +1264,20 @@ int launch_main_any(const Problem& p, const void* dO, void* dk, void* dv, void* 
   const BwdArgs a = make_args(p, w, dk, dv, status);
   const long long grid = static_cast<long long>(a.n_blocks) * BH;
   if (grid > 0x7fffffffLL) return FA_ERR_INVALID;
+  if (p.drop.t > 0 && !(p.d == dvh && p.window == 0)) return FA_ERR_UNSUPPORTED;
   if (p.d == 64 && dvh == 64) {
     // persistent: one CTA per SM walks its share of the (key block, batch-head) items
-    auto kern = pipe::fa_bwd_main_d64;
-    if (!ensure_smem_attr(reinterpret_cast<const void*>(kern), pipe::kSmemBytes, 2))
+    auto kern = p.drop.t > 0 ? pipe::fa_bwd_main_d64<true> : pipe::fa_bwd_main_d64<false>;
+    if (!ensure_smem_attr(reinterpret_cast<const void*>(kern), pipe::kSmemBytes, p.drop.t > 0 ? 12 : 2))
       return FA_ERR_LAUNCH;
     const int sms = device_sm_count();
     if (sms <= 0) return FA_ERR_LAUNCH;
     const long long g = grid < sms ? grid : sms;
     kern<<<static_cast<unsigned>(g), pipe::kThreads, pipe::kSmemBytes, stream>>>(mq, mk, mv, mdo, a);
   } else if (p.d == 128 && dvh == 128) {
-    if (!launch_seq<128, 128>(grid, 3, mq, mk, mv, mdo, a, stream)) return FA_ERR_LAUNCH;
+    const bool ok = p.drop.t > 0 ? launch_seq<128, 128, true>(grid, 13, mq, mk, mv, mdo, a, stream)
+                                 : launch_seq<128, 128>(grid, 3, mq, mk, mv, mdo, a, stream);
+    if (!ok) return FA_ERR_LAUNCH;
   } else if (p.d == 128 && dvh == 64) {
     if (!launch_seq<128, 64>(grid, 6, mq, mk, mv, mdo, a, stream)) return FA_ERR_LAUNCH;
   } else if (p.d == 64 && dvh == 128) {

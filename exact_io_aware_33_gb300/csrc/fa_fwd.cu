@@ -119,9 +119,12 @@ struct FwdArgs {
   int split_tiles;     // key tiles per split (all of them when not split)
   int split_mode;      // 1: write fp32 partial states instead of O / LSE
   float scale_log2;    // scale * log2(e), > 0
+  Dropout drop;        // kDrop kernels only
 };
 
-template <int D, int DV, int QT>
+// kDrop: dropout on the probabilities that multiply V (see Dropout); the
+// row sums and the LSE are those of the softmax itself.
+template <int D, int DV, int QT, bool kDrop>
 __global__ void __launch_bounds__(FwdCfg<D, DV, QT>::kThreads, FwdCfg<D, DV, QT>::kCtasPerSm)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const FwdArgs args) {
@@ -517,13 +520,25 @@ __global__ void __launch_bounds__(FwdCfg<D, DV, QT>::kThreads, FwdCfg<D, DV, QT>
       const float2 negm = make_float2(-m_use, -m_use);
       float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
       auto exp_half = [&](int h, uint32_t (&pk)[32]) {
+        uint32_t kb[4];  // dropout: keep bytes of this row for the current 16 keys
 #pragma unroll
         for (int c = 0; c < 32; ++c) {
           const int e = 64 * h + 2 * c;
+          if constexpr (kDrop) {
+            if ((c & 7) == 0)
+              keep_bytes_quad<true>(static_cast<uint32_t>(row >> 2), static_cast<uint32_t>((key0 + e) >> 2),
+                                    static_cast<uint32_t>(bh), args.drop.offset, args.drop.seed_lo,
+                                    args.drop.seed_hi, kb);
+          }
           const float2 a = __ffma2_rn(make_float2(x[e], x[e + 1]), sl2x2, negm);
-          const float2 pr = make_float2(ex2(a.x), ex2(a.y));
+          float2 pr = make_float2(ex2(a.x), ex2(a.y));
           if (c & 1) acc1 = __fadd2_rn(acc1, pr);
           else acc0 = __fadd2_rn(acc0, pr);
+          if constexpr (kDrop) {  // keys e, e + 1: bytes 2 (c & 1), 2 (c & 1) + 1 of group (c >> 1) & 3
+            const uint32_t word = kb[(c >> 1) & 3] >> ((c & 1) * 16);
+            if ((word & 0xffu) < args.drop.t) pr.x = 0.f;
+            if (((word >> 8) & 0xffu) < args.drop.t) pr.y = 0.f;
+          }
           pk[c] = pack_bf16(pr.x, pr.y);
         }
       };
@@ -582,7 +597,7 @@ __global__ void __launch_bounds__(FwdCfg<D, DV, QT>::kThreads, FwdCfg<D, DV, QT>
       ok = __all_sync(0xffffffffu, ok);
       if (ok) {
         tc_fence_after();
-        const float inv_l = l > 0.f ? 1.0f / l : 0.f;
+        const float inv_l = l > 0.f ? (kDrop ? args.drop.inv_keep : 1.0f) / l : 0.f;
         const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
         const float lse_row = l > 0.f ? (m_use + log2f(l)) * kLn2 : -INFINITY;
         const float2 il2 = make_float2(inv_l, inv_l);
@@ -713,7 +728,7 @@ __global__ void __launch_bounds__(256) fa_merge_splits(const float* __restrict__
   }
 }
 
-template <int D, int DV, int QT>
+template <int D, int DV, int QT, bool kDrop = false>
 int launch_fwd_d(const FwdProblem& p, void* o, float* lse, float* part_o, float* part_lse,
                  int n_splits, cudaStream_t stream) {
   using C = FwdCfg<D, DV, QT>;
@@ -724,9 +739,9 @@ int launch_fwd_d(const FwdProblem& p, void* o, float* lse, float* part_o, float*
     return -3;
   int* status = device_status_word();
   if (!status) return -3;
-  auto kern = fa_fwd_kernel<D, DV, QT>;
-  // attribute slots 0, 1, 4, 5 and 9 (the backward uses 2, 3, 6-8)
-  constexpr int kSlot = QT == 1 ? 9 : (D == 64 ? 0 : 1) + (DV == 64 ? 0 : 4);
+  auto kern = fa_fwd_kernel<D, DV, QT, kDrop>;
+  // attribute slots 0, 1, 4, 5, 9 and with dropout 10, 11 (the backward uses 2, 3, 6-8, 12, 13)
+  constexpr int kSlot = kDrop ? (QT == 1 ? 10 : 11) : QT == 1 ? 9 : (D == 64 ? 0 : 1) + (DV == 64 ? 0 : 4);
   if (!ensure_smem_attr(reinterpret_cast<const void*>(kern), C::kSmemBytes, kSlot))
     return -3;
   const int n_kv = (p.Nk + kBlockN - 1) / kBlockN;
@@ -753,6 +768,7 @@ int launch_fwd_d(const FwdProblem& p, void* o, float* lse, float* part_o, float*
   // |value| below 2^-25 rounds to exactly 1 in fp32.
   const float sl2 = p.scale * 1.4426950408889634f;
   a.scale_log2 = sl2 > 1e-30f ? sl2 : 1e-30f;
+  a.drop = p.drop;
   const long long gx = static_cast<long long>(a.num_pairs) * BH;
   if (gx > 0x7fffffffLL || n_splits > 65535) return -1;
   const dim3 grid(static_cast<unsigned>(gx), a.split_mode ? n_splits : 1);
@@ -803,6 +819,14 @@ int fwd_split_count(const FwdProblem& p, int n_splits, int sms) {
 
 int launch_fwd_general(const FwdProblem& p, void* o, float* lse, float* part_o, float* part_lse,
                        int n_splits, cudaStream_t stream) {
+  if (p.drop.t > 0) {  // dropout: whole key range, d = d_v in {64, 128}
+    if (part_o != nullptr) return -2;
+    if (p.d == 64 && p.dv == 64)
+      return launch_fwd_d<64, 64, 1, true>(p, o, lse, part_o, part_lse, n_splits, stream);
+    if (p.d == 128 && p.dv == 128)
+      return launch_fwd_d<128, 128, 2, true>(p, o, lse, part_o, part_lse, n_splits, stream);
+    return -2;
+  }
   if (p.d == 64 && p.dv == 64) {
     if (part_o == nullptr)  // one query tile per CTA, two CTAs per SM
       return launch_fwd_d<64, 64, 1>(p, o, lse, part_o, part_lse, n_splits, stream);
@@ -815,7 +839,7 @@ int launch_fwd_general(const FwdProblem& p, void* o, float* lse, float* part_o, 
 }
 
 int launch_fwd(const Problem& p, void* o, float* lse, cudaStream_t stream) {
-  FwdProblem g{p.q, p.k, p.v, p.B, p.H, p.N, p.N, p.d, p.d, p.causal, 0, p.scale};
+  FwdProblem g{p.q, p.k, p.v, p.B, p.H, p.N, p.N, p.d, p.d, p.causal, 0, p.scale, p.drop};
   return launch_fwd_general(g, o, lse, nullptr, nullptr, 1, stream);
 }
 

@@ -8,6 +8,16 @@
 
 namespace fa {
 
+// Dropout on the attention probabilities (inactive when t = 0): an element
+// is kept when its generator byte is >= t; kept values are scaled by
+// inv_keep = 256 / (256 - t).
+struct Dropout {
+  uint32_t t = 0;
+  float inv_keep = 1.0f;
+  uint32_t seed_lo = 0, seed_hi = 0;
+  uint32_t offset = 0;
+};
+
 // Problem description after argument checks.
 struct Problem {
   const void* q;
@@ -18,6 +28,7 @@ struct Problem {
   float scale;
   int window = 0;  // backward only: 0 = none, else a causal window of this many keys
   int dv = 0;      // head size of V, O, dO and dV; 0 means d
+  Dropout drop{};
 };
 
 // Forward problem with Nq queries over Nk keys (causal queries are the last
@@ -31,6 +42,7 @@ struct FwdProblem {
   int causal;
   int window;
   float scale;
+  Dropout drop{};
 };
 
 // Encodes a 3-D tiled TMA map over a bf16 [BH, N, d] tensor with boxes of

@@ -375,4 +375,77 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return r;
 }
 
+// ---------------------------------------------------------------- dropout keep bytes
+// Philox4x32-10 (Salmon, Moraes, Dror and Shaw, "Parallel random numbers: as
+// easy as 1, 2, 3", SC 2011): ten rounds, each forming the 64-bit products
+// of counter words 0 and 2 with two fixed odd multipliers and replacing the
+// counter by (hi2 ^ c1 ^ k0, lo2, hi0 ^ c3 ^ k1, lo0); the key grows by two
+// Weyl increments before every round after the first.
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    if (r > 0) {
+      k0 += 0x9E3779B9u;
+      k1 += 0xBB67AE85u;
+    }
+    const uint32_t lo0 = c.x * 0xD2511F53u, hi0 = __umulhi(c.x, 0xD2511F53u);
+    const uint32_t lo1 = c.z * 0xCD9E8D57u, hi1 = __umulhi(c.z, 0xCD9E8D57u);
+    c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+  }
+  return c;
+}
+
+// Word idx (0..3, run-time) of four registers.
+__device__ __forceinline__ uint32_t pick4(uint32_t a, uint32_t b, uint32_t c, uint32_t d, uint32_t idx) {
+  const uint32_t lo = (idx & 1u) ? b : a, hi = (idx & 1u) ? d : c;
+  return (idx & 2u) ? hi : lo;
+}
+
+// Dropout keep bytes. One generator call covers a 4 x 4 block of (query,
+// key) pairs: counter (key >> 2, query >> 2, batch-head, offset), output
+// word (query & 3), byte (key & 3). Lanes 4m..4m+3 of a warp own four
+// consecutive rows of one kind (queries in the forward, keys in the
+// backward, lane & 3 = row & 3) and need the same 16 columns of the other
+// kind: lane r makes the call for column group r and the four words are
+// rotated among the quad in four shuffles. On return out[g] holds this
+// lane's four bytes of column group g (byte c = column 4g + c).
+//   row_major = true:  calls are indexed (column group, row group): the
+//                      forward (rows = queries, columns = keys)
+//   row_major = false: (row group, column group) and each word is
+//                      transposed first: the backward (rows = keys,
+//                      columns = queries)
+template <bool kRowsAreQueries>
+__device__ __forceinline__ void keep_bytes_quad(uint32_t row_group, uint32_t col_group0, uint32_t bh,
+                                                uint32_t offset, uint32_t seed_lo, uint32_t seed_hi,
+                                                uint32_t (&out)[4]) {
+  const uint32_t r = threadIdx.x & 3u;
+  const uint32_t col_group = col_group0 + r;
+  const uint4 w = kRowsAreQueries
+                      ? philox4x32_10(make_uint4(col_group, row_group, bh, offset), seed_lo, seed_hi)
+                      : philox4x32_10(make_uint4(row_group, col_group, bh, offset), seed_lo, seed_hi);
+  uint32_t t0, t1, t2, t3;  // t_j: what lane j of the quad needs from this call
+  if constexpr (kRowsAreQueries) {
+    t0 = w.x; t1 = w.y; t2 = w.z; t3 = w.w;  // word q: query q's four keys
+  } else {
+    // key k of the block needs byte k of each query word: 4 x 4 byte transpose
+    const uint32_t lo01 = __byte_perm(w.x, w.y, 0x5140), hi01 = __byte_perm(w.x, w.y, 0x7362);
+    const uint32_t lo23 = __byte_perm(w.z, w.w, 0x5140), hi23 = __byte_perm(w.z, w.w, 0x7362);
+    t0 = __byte_perm(lo01, lo23, 0x5410);
+    t1 = __byte_perm(lo01, lo23, 0x7632);
+    t2 = __byte_perm(hi01, hi23, 0x5410);
+    t3 = __byte_perm(hi01, hi23, 0x7632);
+  }
+  const int quad = static_cast<int>(threadIdx.x & 31u) & ~3;
+  uint32_t rot[4];
+#pragma unroll
+  for (int s = 0; s < 4; ++s) {
+    // round s: lane r receives, from lane (r + s) & 3, that lane's call's part for lane r
+    const uint32_t send = pick4(t0, t1, t2, t3, (r - static_cast<uint32_t>(s)) & 3u);
+    rot[s] = __shfl_sync(0xffffffffu, send, quad | static_cast<int>((r + s) & 3u));
+  }
+  // rot[s] belongs to column group (r + s) & 3
+#pragma unroll
+  for (int g = 0; g < 4; ++g) out[g] = pick4(rot[0], rot[1], rot[2], rot[3], (static_cast<uint32_t>(g) - r) & 3u);
+}
+
 }  // namespace fa

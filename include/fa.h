@@ -225,6 +225,37 @@ int fa_decode_splitkv(const void* q, const void* k, const void* v, void* o, floa
 int fa_decode_num_splits(int B, int H, int Nq, int Nk, int n_splits);
 size_t fa_decode_workspace_bytes(int B, int H, int Nq, int Nk, int dv, int n_splits);
 
+/*
+ * Forward and backward with dropout on the attention probabilities. The
+ * pages name dropout only as a setting to hold equal between implementations
+ * ("Flash Attention: IO-Aware Exact Attention", section "What changes in
+ * FlashAttention-2"); the form here is inverted dropout on P:
+ *     O = (P * M) V / keep,   LSE as without dropout (the softmax statistic)
+ * and the backward is the exact gradient of that O for the same mask M:
+ *     dV = (P*M/keep)^T dO, dP = (dO V^T) * M / keep, dS = P * (dP - D),
+ *     D = rowsum(dO * O), dQ = scale dS K, dK = scale dS^T Q.
+ *   dropout_p : 0 <= p < 1 (else FA_ERR_INVALID), applied as the byte
+ *               threshold t = round(256 p) (at most 255): an element is kept
+ *               when its generator byte is >= t, so keep = (256 - t) / 256
+ *               and p = 0 is exactly attention without dropout.
+ *   seed, offset : the mask of batch-head bh, query i, key j is byte (j & 3)
+ *               of word (i & 3) of Philox4x32-10 (Salmon, Moraes, Dror and
+ *               Shaw, SC 2011) with counter (j >> 2, i >> 2, bh,
+ *               offset mod 2^32) and key (seed mod 2^32, seed >> 32). The
+ *               backward must get the forward's seed and offset; a new
+ *               offset per call gives a new mask.
+ * d must be 64 or 128 (FA_ERR_UNSUPPORTED otherwise); other arguments,
+ * layouts, the workspace and errors as fa_fwd_stream and fa_bwd_stream.
+ */
+int fa_fwd_dropout(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                   int N, int d, int causal, float scale, float dropout_p, unsigned long long seed,
+                   unsigned long long offset, void* cuda_stream);
+int fa_bwd_dropout(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                   const void* dO, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+                   int causal, float scale, float dropout_p, unsigned long long seed,
+                   unsigned long long offset, void* workspace, size_t ws_bytes,
+                   void* cuda_stream);
+
 /* Static description of a return code. Never NULL. */
 const char* fa_strerror(int code);
 

@@ -105,6 +105,23 @@ def test_bwd_rejects_bad_arguments(lib):
                              ctypes.c_void_p(0x100010), ws_need, n) == fa.FA_ERR_WORKSPACE
 
 
+def test_dropout_entry_points_check_arguments_on_the_host(lib):
+    p, n = ALIGNED, NULL
+    for bad in (-0.1, 1.0, 1.5, float("nan")):
+        assert lib.fa_fwd_dropout(p, p, p, p, p, 1, 1, 8, 64, 0, 0.125, bad, 1, 0, n) == fa.FA_ERR_INVALID
+        assert lib.fa_bwd_dropout(p, p, p, p, p, p, p, p, p, 1, 1, 8, 64, 0, 0.125, bad, 1, 0, p, 1 << 20,
+                                  n) == fa.FA_ERR_INVALID
+    # empty problems are no-ops; bad sizes and pointers as without dropout
+    assert lib.fa_fwd_dropout(n, n, n, n, n, 0, 4, 128, 64, 0, 0.125, 0.1, 1, 0, n) == fa.FA_OK
+    assert lib.fa_fwd_dropout(p, p, p, p, p, 1, 1, 8, 96, 0, 0.125, 0.1, 1, 0, n) == fa.FA_ERR_UNSUPPORTED
+    assert lib.fa_fwd_dropout(n, p, p, p, p, 1, 1, 8, 64, 0, 0.125, 0.1, 1, 0, n) == fa.FA_ERR_INVALID
+    ws_need = lib.fa_bwd_workspace_bytes(1, 1, 8, 64)
+    assert lib.fa_bwd_dropout(p, p, p, p, p, p, p, p, p, 1, 1, 8, 64, 0, 0.125, 0.1, 1, 0, p, ws_need - 4,
+                              n) == fa.FA_ERR_WORKSPACE
+    assert lib.fa_bwd_dropout(n, n, n, n, n, n, n, n, n, 1, 0, 64, 64, 0, 0.125, 0.1, 1, 0, n, 0,
+                              n) == fa.FA_OK
+
+
 def test_binding_refuses_cpu_tensors():
     import torch
     x = torch.zeros(1, 1, 8, 64, dtype=torch.bfloat16)
