@@ -189,6 +189,35 @@ def window_leg(dev, stream, flush, reps=10):
             "note": "backward = preprocess + main + finish"}
 
 
+def dropout_leg(dev, stream, flush, reps=10):
+    """Dropout p = 0.1 on the forward+backward workload's shape (causal,
+    B=8 H=12 N=2048 d=64): forward and full backward with the keep mask
+    regenerated in both; FLOPs as without dropout (4 B H N^2 d / 2 forward,
+    2.5x that backward), the generator's integer work not counted."""
+    import torch
+    import exact_io_aware_33_gb300 as fa
+    w = si.workload("causal_fwdbwd_b8h12_n2048_d64")
+    x = si.make_inputs(w, with_grad=True)
+    q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "do"))
+    o = torch.empty_like(q)
+    lse = torch.empty(w.B, w.H, w.N, dtype=torch.float32, device=dev)
+    dq, dk, dv = (torch.empty_like(q) for _ in range(3))
+    ws = torch.empty(fa.fa_bwd_workspace_bytes(w.B, w.H, w.N, w.d), dtype=torch.uint8, device=dev)
+    p, seed = 0.1, 2024
+    with torch.cuda.stream(stream):
+        ms_f = time_calls(lambda: fa.fa_fwd_dropout(q, k, v, p, seed, 1, causal=True, scale=w.scale,
+                                                    out=o, lse=lse, stream=stream), reps, 3, stream, flush)
+        ms_b = time_calls(lambda: fa.fa_bwd_dropout(q, k, v, o, lse, do, p, seed, 1, causal=True,
+                                                    scale=w.scale, dq=dq, dk=dk, dv=dv, workspace=ws,
+                                                    stream=stream), reps, 3, stream, flush)
+    f_fwd, f_bwd = step_flops(w)
+    return {"workload": "dropout_p0.1_" + w.name, "fwd_ms": round(ms_f, 4),
+            "fwd_tflops": round(f_fwd / (ms_f * 1e-3) / 1e12, 1), "bwd_ms": round(ms_b, 4),
+            "bwd_tflops": round(f_bwd / (ms_b * 1e-3) / 1e12, 1),
+            "step_tflops": round((f_fwd + f_bwd) / ((ms_f + ms_b) * 1e-3) / 1e12, 1),
+            "note": "backward = preprocess + main + finish; keep mask from Philox4x32-10 in both"}
+
+
 def max_over_ranks(values, device, world):
     """Element-wise maximum of per-rank floats (the slowest rank's times)."""
     if world <= 1:
@@ -577,6 +606,7 @@ def run_ours(args):
         out["decode"] = decode_leg(dev, stream)
         out["window"] = window_leg(dev, stream, runner.flush_l2)
         out["headsize"] = headsize_leg(dev, stream, runner.flush_l2)
+        out["dropout"] = dropout_leg(dev, stream, runner.flush_l2)
         if world == 1:
             out["cpu_baseline"] = cpu_baseline(w)
     print(json.dumps(out), flush=True)
