@@ -446,6 +446,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           reinterpret_cast<const float*>(base_ptr + C::kStageOff + (it % C::kStages) * C::kStageBytes +
                                          C::kTileBytes + C::kVTileBytes) + kHalf * w;
       const float* nd_s = nlse2_s + kBlk;
+      // dropout: this key's keep bytes for the step's 64 query columns, made
+      // before the waits (the generator needs no operand)
+      uint32_t kball[16];
+      if constexpr (kDrop) {
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) {
+          uint32_t kb[4];
+          keep_bytes_quad<false>(static_cast<uint32_t>((jb * kBlk + key_row) >> 2),
+                                 static_cast<uint32_t>(((i0 + it) * kBlk + kHalf * w + 16 * ch) >> 2),
+                                 static_cast<uint32_t>(bh), args.drop.offset, args.drop.seed_lo,
+                                 args.drop.seed_hi, kb);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) kball[4 * ch + q] = kb[q];
+        }
+      }
       // the stage's vectors arrive with its Q/dO tiles; S^T, dP^T with the MMA commit
       ok = mbar_wait_sleep(bar(C::kBarQFull + it % C::kStages), (it / C::kStages) & 1, abort_flag);
       if (ok) ok = mbar_wait_sleep(bar(C::kBarSFull + w), it & 1, abort_flag);
@@ -461,18 +476,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld_wait(sr);
         tmem_ld_wait(dr);
         uint32_t pp[16], dd[16];
-        uint32_t kb[4];  // dropout: keep bytes of this key for the current 16 queries
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
           const int ql = c * 32 + e;            // query column within this half
           const int qc = kHalf * w + ql;        // ... within the block
-          if constexpr (kDrop) {
-            if ((e & 15) == 0)
-              keep_bytes_quad<false>(static_cast<uint32_t>((jb * kBlk + key_row) >> 2),
-                                     static_cast<uint32_t>(((i0 + it) * kBlk + qc) >> 2),
-                                     static_cast<uint32_t>(bh), args.drop.offset, args.drop.seed_lo,
-                                     args.drop.seed_hi, kb);
-          }
           const float2 nl = *reinterpret_cast<const float2*>(nlse2_s + ql);
           const float2 nd = *reinterpret_cast<const float2*>(nd_s + ql);
           const float2 a = __ffma2_rn(make_float2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])),
@@ -485,7 +492,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           float2 dpv = make_float2(__uint_as_float(dr[e]), __uint_as_float(dr[e + 1]));
           float2 pk = p;
           if constexpr (kDrop) {  // queries e, e + 1: bytes (e & 3), (e & 3) + 1 of group (e >> 2) & 3
-            const uint32_t word = kb[(e >> 2) & 3] >> ((e & 3) * 8);
+            const uint32_t word = kball[ql >> 2] >> ((e & 3) * 8);
             const float ik = args.drop.inv_keep;
             if ((word & 0xffu) < args.drop.t) { pk.x = 0.f; dpv.x = 0.f; } else { dpv.x *= ik; }
             if (((word >> 8) & 0xffu) < args.drop.t) { pk.y = 0.f; dpv.y = 0.f; } else { dpv.y *= ik; }
@@ -948,6 +955,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float* nlse2_s =
           reinterpret_cast<const float*>(base_ptr + kStageOff + s * kStageBytes + 2 * kTileBytes) + 64 * w;
       const float* nd_s = nlse2_s + kBlk;
+      // dropout: this key's keep bytes for the step's 64 query columns, made
+      // before the waits below (the generator needs no operand) so that they
+      // cost no time on the step's chain and hold no registers next to S, dP
+      uint32_t kball[16];
+      if constexpr (kDrop) {
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) {
+          uint32_t kb[4];
+          keep_bytes_quad<false>(static_cast<uint32_t>((jb * kBlk + key_row) >> 2),
+                                 static_cast<uint32_t>(((i0 + it) * kBlk + 64 * w + 16 * ch) >> 2),
+                                 static_cast<uint32_t>(bh), args.drop.offset, args.drop.seed_lo,
+                                 args.drop.seed_hi, kb);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) kball[4 * ch + q] = kb[q];
+        }
+      }
       // the stage's vectors arrive with its Q/dO tiles; S^T, dP^T with the MMA
       // commit. The next step's Q and dO are checked here too, so that the
       // release of S^T below also tells the MMA thread they have landed and
@@ -981,18 +1004,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       // A compile-time kind keeps the unmasked blocks free of per-element tests.
       auto half = [&](auto kind, const uint32_t (&sr)[32], const uint32_t (&dr)[32], int c) {
         constexpr int kKind = decltype(kind)::value;
-        uint32_t kb[4];  // dropout: keep bytes of this key for the current 16 queries
 #pragma unroll
         for (int e = 0; e < 32; e += 4) {
           const int ql = c * 32 + e;     // query column within this warpgroup's half
           const int qc = 64 * w + ql;    // ... within the query block
-          if constexpr (kDrop) {
-            if ((e & 15) == 0)
-              keep_bytes_quad<false>(static_cast<uint32_t>((jb * kBlk + key_row) >> 2),
-                                     static_cast<uint32_t>(((i0 + it) * kBlk + qc) >> 2),
-                                     static_cast<uint32_t>(bh), args.drop.offset, args.drop.seed_lo,
-                                     args.drop.seed_hi, kb);
-          }
           const float4 nl = *reinterpret_cast<const float4*>(nlse2_s + ql);
           const float4 nd = *reinterpret_cast<const float4*>(nd_s + ql);
 #pragma unroll
@@ -1014,7 +1029,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             float2 dpv = make_float2(__uint_as_float(dr[x]), __uint_as_float(dr[x + 1]));
             float2 pk = p;
             if constexpr (kDrop) {  // queries x, x + 1: bytes 2u, 2u + 1 of group (e >> 2) & 3
-              const uint32_t word = kb[(e >> 2) & 3] >> (16 * u);
+              const uint32_t word = kball[ql >> 2] >> (16 * u);
               const float ik = args.drop.inv_keep;
               if ((word & 0xffu) < args.drop.t) { pk.x = 0.f; dpv.x = 0.f; } else { dpv.x *= ik; }
               if (((word >> 8) & 0xffu) < args.drop.t) { pk.y = 0.f; dpv.y = 0.f; } else { dpv.y *= ik; }

@@ -474,6 +474,20 @@ __global__ void __launch_bounds__(FwdCfg<D, DV, QT>::kThreads, FwdCfg<D, DV, QT>
     bool ok = true;
     for (int u = 0; u < n_mine; ++u) {
       const int key0 = (key_tile0 + u) * kBlockN;
+      // dropout: this row's keep bytes for the tile's first 64 keys, made
+      // before the wait (the generator needs no operand)
+      uint32_t kpre[16];
+      if constexpr (kDrop) {
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) {
+          uint32_t kb[4];
+          keep_bytes_quad<true>(static_cast<uint32_t>(row >> 2), static_cast<uint32_t>((key0 + 16 * ch) >> 2),
+                                static_cast<uint32_t>(bh), args.drop.offset, args.drop.seed_lo,
+                                args.drop.seed_hi, kb);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) kpre[4 * ch + q] = kb[q];
+        }
+      }
       ok = mbar_wait(bar(C::kBarSFull + t), u & 1, abort_flag);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
@@ -525,7 +539,7 @@ __global__ void __launch_bounds__(FwdCfg<D, DV, QT>::kThreads, FwdCfg<D, DV, QT>
         for (int c = 0; c < 32; ++c) {
           const int e = 64 * h + 2 * c;
           if constexpr (kDrop) {
-            if ((c & 7) == 0)
+            if (h == 1 && (c & 7) == 0)
               keep_bytes_quad<true>(static_cast<uint32_t>(row >> 2), static_cast<uint32_t>((key0 + e) >> 2),
                                     static_cast<uint32_t>(bh), args.drop.offset, args.drop.seed_lo,
                                     args.drop.seed_hi, kb);
@@ -535,7 +549,7 @@ __global__ void __launch_bounds__(FwdCfg<D, DV, QT>::kThreads, FwdCfg<D, DV, QT>
           if (c & 1) acc1 = __fadd2_rn(acc1, pr);
           else acc0 = __fadd2_rn(acc0, pr);
           if constexpr (kDrop) {  // keys e, e + 1: bytes 2 (c & 1), 2 (c & 1) + 1 of group (c >> 1) & 3
-            const uint32_t word = kb[(c >> 1) & 3] >> ((c & 1) * 16);
+            const uint32_t word = (h == 0 ? kpre[c >> 1] : kb[(c >> 1) & 3]) >> ((c & 1) * 16);
             if ((word & 0xffu) < args.drop.t) pr.x = 0.f;
             if (((word >> 8) & 0xffu) < args.drop.t) pr.y = 0.f;
           }
