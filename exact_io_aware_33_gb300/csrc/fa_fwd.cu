@@ -534,7 +534,7 @@ __global__ void __launch_bounds__(FwdCfg<D, DV, QT>::kThreads, FwdCfg<D, DV, QT>
       const float2 negm = make_float2(-m_use, -m_use);
       float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
       auto exp_half = [&](int h, uint32_t (&pk)[32]) {
-        uint32_t kb[4];  // dropout: keep bytes of this row for the current 16 keys
+        uint32_t kb[4];  // dropout, second half: keep bytes of this row for the current 16 keys
 #pragma unroll
         for (int c = 0; c < 32; ++c) {
           const int e = 64 * h + 2 * c;
@@ -548,7 +548,7 @@ __global__ void __launch_bounds__(FwdCfg<D, DV, QT>::kThreads, FwdCfg<D, DV, QT>
           float2 pr = make_float2(ex2(a.x), ex2(a.y));
           if (c & 1) acc1 = __fadd2_rn(acc1, pr);
           else acc0 = __fadd2_rn(acc0, pr);
-          if constexpr (kDrop) {  // keys e, e + 1: bytes 2 (c & 1), 2 (c & 1) + 1 of group (c >> 1) & 3
+          if constexpr (kDrop) {  // keys e, e + 1: bytes 2 (c & 1), 2 (c & 1) + 1 of key group e >> 2
             const uint32_t word = (h == 0 ? kpre[c >> 1] : kb[(c >> 1) & 3]) >> ((c & 1) * 16);
             if ((word & 0xffu) < args.drop.t) pr.x = 0.f;
             if (((word >> 8) & 0xffu) < args.drop.t) pr.y = 0.f;
