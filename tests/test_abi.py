@@ -127,6 +127,11 @@ def test_binding_refuses_cpu_tensors():
     x = torch.zeros(1, 1, 8, 64, dtype=torch.bfloat16)
     with pytest.raises(ValueError, match="CUDA"):
         fa.fa_fwd(x, x, x)
+    with pytest.raises(ValueError, match="CUDA"):
+        fa.fa_fwd_dropout(x, x, x, 0.1, seed=1)
+    lse = torch.zeros(1, 1, 8)
+    with pytest.raises(ValueError, match="CUDA"):
+        fa.fa_bwd_dropout(x, x, x, x, lse, x, 0.1, seed=1)
 
 
 def test_transfer_ledger_matches_page():
