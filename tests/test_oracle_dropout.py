@@ -4,7 +4,9 @@ The dropout arithmetic is pinned by its reduction to the dropout-free oracle,
 by central finite differences of the masked forward, by the identity
 D_i = sum_j P_ij dP_ij, and by the mean over many masks converging to the
 dropout-free output; the generator by its kept fraction, byte uniformity,
-avalanche and stream separation.
+avalanche and stream separation. Each check takes the oracle functions it
+exercises, so that the planted-mistake tests at the bottom can hand in a
+broken copy.
 """
 
 import numpy as np
@@ -17,23 +19,25 @@ def _rand(shape, seed):
     return np.random.default_rng(seed).standard_normal(shape)
 
 
-@pytest.mark.parametrize("causal", [False, True])
-def test_no_dropout_is_the_dense_oracle(causal):
+# --------------------------------------------------------------------------
+# Checks
+# --------------------------------------------------------------------------
+
+def check_no_dropout_is_dense(fwd, bwd, causal):
     q, k, v, do = (_rand((37, 8), s) for s in range(4))
     mask = dropout.keep_mask(3, 37, 37, 0.0, seed=123, offset=7)
     assert mask.all()
-    o, lse = dropout.forward_head_masked(q, k, v, mask, dropout.keep_probability(0.0), causal, 0.3)
+    o, lse = fwd(q, k, v, mask, dropout.keep_probability(0.0), causal, 0.3)
     o_ref, lse_ref = dense.forward_head(q, k, v, causal, 0.3)
     np.testing.assert_allclose(o, o_ref, rtol=0, atol=1e-12)
     np.testing.assert_allclose(lse, lse_ref, rtol=0, atol=1e-12)
-    g = dropout.backward_head_masked(q, k, v, o, lse, do, mask, 1.0, causal, 0.3)
+    g = bwd(q, k, v, o, lse, do, mask, 1.0, causal, 0.3)
     g_ref = dense.backward_head(q, k, v, o_ref, lse_ref, do, causal, 0.3)
     for a, b in zip(g, g_ref):
         np.testing.assert_allclose(a, b, rtol=0, atol=1e-12)
 
 
-@pytest.mark.parametrize("causal", [False, True])
-def test_backward_matches_finite_differences(causal):
+def check_finite_differences(fwd, bwd, causal):
     n, d = 6, 3
     q, k, v, do = (_rand((n, d), 10 + s) for s in range(4))
     mask = np.random.default_rng(5).random((n, n)) >= 0.4
@@ -44,10 +48,43 @@ def test_backward_matches_finite_differences(causal):
         return float((o * g).sum())
 
     num = finite_diff._numeric(loss, q, k, v, do, 1e-6)
-    o, lse = dropout.forward_head_masked(q, k, v, mask, keep, causal, 0.7)
-    ana = dropout.backward_head_masked(q, k, v, o, lse, do, mask, keep, causal, 0.7)
+    o, lse = fwd(q, k, v, mask, keep, causal, 0.7)
+    ana = bwd(q, k, v, o, lse, do, mask, keep, causal, 0.7)
     for a, b in zip(ana, num):
         np.testing.assert_allclose(a, b, rtol=1e-6, atol=1e-7)
+
+
+def check_mean_over_masks(fwd, p=0.3, trials=3000):
+    n, d = 12, 4
+    q, k, v = (_rand((n, d), 30 + s) for s in range(3))
+    keep = dropout.keep_probability(p)
+    outs = np.stack([fwd(q, k, v, dropout.keep_mask(0, n, n, p, seed=77, offset=t), keep, False, 0.5)[0]
+                     for t in range(trials)])
+    o_ref, _ = dense.forward_head(q, k, v, False, 0.5)
+    err = np.abs(outs.mean(axis=0) - o_ref)
+    sem = outs.std(axis=0) / np.sqrt(trials)
+    assert (err <= 5 * sem + 1e-12).all()
+
+
+def check_kept_fraction(mask_fn, p):
+    m = mask_fn(5, 1024, 1024, p, seed=2024, offset=3)
+    keep = dropout.keep_probability(p)
+    assert abs(m.mean() - keep) <= 6 * np.sqrt(keep * (1 - keep) / m.size)
+    assert abs(keep - (1 - p)) <= 1 / 512  # t = round(256 p)
+
+
+# --------------------------------------------------------------------------
+# Pins
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_no_dropout_is_the_dense_oracle(causal):
+    check_no_dropout_is_dense(dropout.forward_head_masked, dropout.backward_head_masked, causal)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_matches_finite_differences(causal):
+    check_finite_differences(dropout.forward_head_masked, dropout.backward_head_masked, causal)
 
 
 def test_row_vector_D_is_the_probability_weighted_dP():
@@ -62,26 +99,12 @@ def test_row_vector_D_is_the_probability_weighted_dP():
 
 
 def test_mean_over_masks_is_the_dropout_free_output():
-    n, d, trials, p = 12, 4, 3000, 0.3
-    q, k, v = (_rand((n, d), 30 + s) for s in range(3))
-    keep = dropout.keep_probability(p)
-    outs = np.stack([
-        dropout.forward_head_masked(q, k, v, dropout.keep_mask(0, n, n, p, seed=77, offset=t), keep,
-                                    False, 0.5)[0]
-        for t in range(trials)])
-    o_ref, _ = dense.forward_head(q, k, v, False, 0.5)
-    err = np.abs(outs.mean(axis=0) - o_ref)
-    sem = outs.std(axis=0) / np.sqrt(trials)
-    assert (err <= 5 * sem + 1e-12).all()
+    check_mean_over_masks(dropout.forward_head_masked)
 
 
 @pytest.mark.parametrize("p", [0.1, 0.25, 0.5, 0.9])
 def test_kept_fraction(p):
-    m = dropout.keep_mask(5, 512, 512, p, seed=2024, offset=3)
-    keep = dropout.keep_probability(p)
-    n = m.size
-    assert abs(m.mean() - keep) <= 6 * np.sqrt(keep * (1 - keep) / n)
-    assert abs(keep - (1 - p)) <= 1 / 512  # t = round(256 p)
+    check_kept_fraction(dropout.keep_mask, p)
 
 
 def test_bytes_are_uniform():
@@ -119,3 +142,57 @@ def test_streams_are_separate():
     # a prefix of a longer head is the same mask (element (i, j) depends only on i, j)
     big = dropout.keep_mask(0, 100, 100, p, seed=1, offset=0)
     assert (big[:64, :64] == a).all()
+
+
+# --------------------------------------------------------------------------
+# Planted mistakes: a broken copy of each oracle function must fail a pin.
+# --------------------------------------------------------------------------
+
+def _bwd_dv_unmasked(q, k, v, o, lse, do, mask, keep, causal, scale):
+    dq, dk, _ = dropout.backward_head_masked(q, k, v, o, lse, do, mask, keep, causal, scale)
+    p = dense.probabilities(q, k, causal, scale)
+    return dq, dk, p.T @ np.asarray(do, dtype=np.float64)
+
+
+def _bwd_dp_not_rescaled(q, k, v, o, lse, do, mask, keep, causal, scale):
+    """dP = (dO V^T) * M, the 1/keep left out (dV keeps it)."""
+    _, _, dv = dropout.backward_head_masked(q, k, v, o, lse, do, mask, keep, causal, scale)
+    dq, dk, _ = dropout.backward_head_masked(q, k, v, o, lse, do, mask, 1.0, causal, scale)
+    return dq, dk, dv
+
+
+def _bwd_D_without_dropout(q, k, v, o, lse, do, mask, keep, causal, scale):
+    """D from the dropout-free O."""
+    o_plain, _ = dense.forward_head(q, k, v, causal, scale)
+    return dropout.backward_head_masked(q, k, v, o_plain, lse, do, mask, keep, causal, scale)
+
+
+def _bwd_mask_transposed(q, k, v, o, lse, do, mask, keep, causal, scale):
+    return dropout.backward_head_masked(q, k, v, o, lse, do, np.asarray(mask).T, keep, causal, scale)
+
+
+def _fwd_not_rescaled(q, k, v, mask, keep, causal, scale):
+    o, lse = dropout.forward_head_masked(q, k, v, mask, keep, causal, scale)
+    return o * keep, lse
+
+
+def _mask_threshold_off_by_one(bh, nq, nk, p, seed, offset):
+    return dropout.keep_bytes(bh, nq, nk, seed, offset) > dropout.threshold(p)
+
+
+@pytest.mark.parametrize("case", [
+    ("backward, dV unmasked",
+     lambda: check_finite_differences(dropout.forward_head_masked, _bwd_dv_unmasked, False)),
+    ("backward, dP without 1/keep",
+     lambda: check_finite_differences(dropout.forward_head_masked, _bwd_dp_not_rescaled, True)),
+    ("backward, D from the dropout-free O",
+     lambda: check_finite_differences(dropout.forward_head_masked, _bwd_D_without_dropout, False)),
+    ("backward, mask transposed",
+     lambda: check_finite_differences(dropout.forward_head_masked, _bwd_mask_transposed, False)),
+    ("forward, 1/keep left out", lambda: check_mean_over_masks(_fwd_not_rescaled)),
+    ("mask, keep test off by one", lambda: check_kept_fraction(_mask_threshold_off_by_one, 0.1)),
+], ids=lambda c: c[0])
+def test_planted_mistake_is_caught(case):
+    _, run = case
+    with pytest.raises(AssertionError):
+        run()
