@@ -142,3 +142,36 @@ def test_offset_changes_the_mask_and_repeats_are_identical():
     torch.cuda.synchronize()
     assert torch.equal(a, b)
     assert not torch.equal(a, c)
+
+
+def test_fwdbwd_workload_full_size():
+    """The forward+backward workload at full size (B=8, H=12, N=2048, d=64, causal) with p = 0.1,
+    the configuration the bench's dropout leg times: sampled heads against the oracle, and on every
+    head finite outputs and sum_j dK_j = 0 (row sums of dS vanish with dropout too, because
+    D_i = sum_j P_ij dP_ij)."""
+    w = si.workload("causal_fwdbwd_b8h12_n2048_d64")
+    x = si.make_inputs(w)
+    g = {n: t.cuda() for n, t in x.items()}
+    p, seed, offset = 0.1, 2024, 1
+    o, lse = fa.fa_fwd_dropout(g["q"], g["k"], g["v"], p, seed, offset, causal=True, scale=w.scale)
+    dq, dk, dv = fa.fa_bwd_dropout(g["q"], g["k"], g["v"], o, lse, g["do"], p, seed, offset, causal=True,
+                                   scale=w.scale)
+    torch.cuda.synchronize()
+    assert fa.fa_get_last_device_status() == fa.FA_OK
+    heads = [(0, 0), (w.B - 1, w.H - 1), (3, 5)]
+    o_ref, lse_ref = dropout.forward(x["q"], x["k"], x["v"], True, w.scale, p, seed, offset, heads=heads)
+    refs = dropout.backward(x["q"], x["k"], x["v"], o_ref, lse_ref, x["do"], True, w.scale, p, seed, offset,
+                            heads=heads)
+    o_np, lse_np = o.float().cpu().double().numpy(), lse.cpu().double().numpy()
+    for b, h in heads:
+        err = np.abs(o_np[b, h] - o_ref[b, h])
+        assert err.max() <= 2e-2 and err.mean() <= 2e-3, ((b, h), err.max(), err.mean())
+        assert np.abs(lse_np[b, h] - lse_ref[b, h]).max() <= 1e-3
+        for name, got, ref in zip(("dq", "dk", "dv"), (dq, dk, dv), refs):
+            gg = got[b, h].float().cpu().double().numpy()
+            rel = float(np.abs(gg - ref[b, h]).max() / max(np.abs(ref[b, h]).max(), 1e-3))
+            assert rel <= 5e-2, ((b, h), name, rel)
+    for t in (o, dq, dk, dv):
+        assert torch.isfinite(t.float()).all()
+    dkf = dk.float()
+    assert float(dkf.sum(dim=2).abs().max()) <= 2e-2 * float(dkf.abs().sum(dim=2).max())
