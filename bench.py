@@ -588,12 +588,14 @@ def run_ours(args):
     }
     if not args.no_extras:
         runner2 = Runner(w, dev, seed_offset=rank_seed_offset(rank))
-        e_ms, h2d, d2h = e2e_loop([runner, runner2], max(3, args.steps // 2), 2, stream)
+        e_ms, h2d, d2h = e2e_loop([runner, runner2], max(3, args.steps), 2, stream)
         del runner2
         out["e2e"] = {"value": round(world * (f_fwd + f_bwd) / (e_ms * 1e-3) / 1e12, 2),
                       "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                       "ms_per_step": round(e_ms, 4),
-                      "pipeline": "uploads, compute and downloads on three streams, two buffer sets"}
+                      "steps": max(3, args.steps),
+                      "pipeline": "uploads, compute and downloads on three streams, two buffer sets; "
+                                  "timed from the first upload to the last download"}
         # the long causal forward (B=1, H=16, N=8192, d=128), the head-size-128 target shape
         wl = si.WORKLOADS[3]
         rl = Runner(wl, dev)
