@@ -80,6 +80,8 @@ int current_device(DeviceState** st) {
 
 bool aligned16(const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+}  // namespace
+
 // Common checks of both passes. Returns FA_OK, or an error code; sets
 // *empty when there is nothing to compute.
 int check_problem(int B, int H, int N, int d, float scale, bool* empty) {
@@ -97,8 +99,6 @@ int check_problem(int B, int H, int N, int d, float scale, bool* empty) {
   if (bh * static_cast<long long>(N) * d > (1LL << 46)) return FA_ERR_INVALID;
   return FA_OK;
 }
-
-}  // namespace
 
 bool make_map_bhnd(CUtensorMap* map, const void* ptr, int BH, int N, int d) {
   EncodeTiledFn enc = encode_fn();

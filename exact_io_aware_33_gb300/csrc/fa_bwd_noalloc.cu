@@ -12,8 +12,12 @@
 // of fixed size, so the call allocates nothing.
 //
 // Costs and limits of that choice:
-//   * the array is kScratchBytes (64 MiB) and is held by every GPU that
-//     loads this part of the library, until the process exits;
+//   * the array is kScratchBytes (64 MiB). With lazy module loading (the
+//     CUDA default) it is reserved on a device by the first call there: the
+//     cudaGetSymbolAddress below loads this file's device code onto that
+//     device. It stays reserved until the process exits. That first call can
+//     fail when the device is full and must not run inside a stream capture,
+//     so callers make it during set-up;
 //   * problems whose workspace (fa_bwd_workspace_bytes) exceeds it are
 //     rejected with FA_ERR_WORKSPACE before anything is launched;
 //   * all calls share the one array: two calls whose kernels overlap on the
@@ -65,20 +69,19 @@ extern "C" int fa_bwd_noalloc(const void* q, const void* k, const void* v, const
                               const float* lse, const void* dO, void* dq, void* dk, void* dv,
                               int B, int H, int N, int d, int causal, float scale,
                               void* cuda_stream) {
-  // Size and pointer checks match fa_bwd_stream's, with the built-in array
-  // standing in for the caller's workspace.
-  if (B < 0 || H < 0 || N < 0) return FA_ERR_INVALID;
-  if (!(scale >= 0.f) || scale > 3.4e38f) return FA_ERR_INVALID;
-  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
-  if (B == 0 || H == 0 || N == 0) return FA_OK;
+  // The size checks are fa_bwd_stream's own (check_problem), with the
+  // built-in array standing in for the caller's workspace.
+  bool empty = false;
+  const int chk = fa::check_problem(B, H, N, d, scale, &empty);
+  if (chk != FA_OK || empty) return chk;
   const void* ptrs[] = {q, k, v, o, lse, dO, dq, dk, dv};
   for (const void* ptr : ptrs)
     if (!fa::aligned16(ptr)) return FA_ERR_INVALID;
-  if (static_cast<long long>(B) * H > (1LL << 31) - 1) return FA_ERR_INVALID;
   if (fa::bwd_workspace_bytes(B, H, N, d) > fa::kScratchBytes) return FA_ERR_WORKSPACE;
   const int dev_rc = fa::current_device_status();
   if (dev_rc != FA_OK) return dev_rc;
-  // First call on a device: finds the array's device address (no allocation).
+  // First call on a device: finds the array's device address (and, with lazy
+  // module loading, loads this file's device code there).
   void* ws = fa::scratch_on_current_device();
   if (ws == nullptr) return FA_ERR_LAUNCH;
   const cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);

@@ -49,6 +49,10 @@ struct FwdProblem {
 // 128 rows x 64 columns and 128-byte swizzle. Returns false on failure.
 bool make_map_bhnd(CUtensorMap* map, const void* ptr, int BH, int N, int d);
 
+// Size and scale checks shared by the entry points taking (B, H, N, d):
+// FA_OK or an error code; *empty is set when there is nothing to compute.
+int check_problem(int B, int H, int N, int d, float scale, bool* empty);
+
 // FA_OK when the current device is a CC 10.3 GPU, else the error code.
 int current_device_status();
 

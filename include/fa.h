@@ -141,11 +141,15 @@ int fa_bwd_finish_stream(void* dq, int B, int H, int N, int d, const void* works
  * its hot path (the call can synchronise the device and can fail once memory
  * is fragmented).
  * The workspace is a file-scope device array of
- * FA_BWD_NOALLOC_MAX_SCRATCH_BYTES bytes inside the library, held by every
- * GPU that loads the library until the process exits. Problems whose
+ * FA_BWD_NOALLOC_MAX_SCRATCH_BYTES bytes inside the library. Problems whose
  * fa_bwd_workspace_bytes exceed it return FA_ERR_WORKSPACE and launch
- * nothing. The first call on a device looks up the array's device address
- * (no allocation); make that first call before any stream capture. All calls
+ * nothing. The first call on a device looks up the array's device address;
+ * with lazy module loading (the CUDA default) that lookup is also what loads
+ * the library's device code holding the array onto that device and reserves
+ * the 64 MiB there, until the process exits. That first call can therefore
+ * fail with FA_ERR_LAUNCH when the device is out of memory, and must not run
+ * inside a stream capture: make it during set-up, on every device the caller
+ * will use. Later calls on the device allocate and load nothing. All calls
  * share the array: calls whose kernels overlap on the GPU (other streams,
  * other host threads) race and corrupt each other's results, so serialise
  * them on one stream. Arguments and results are those of fa_bwd_stream.

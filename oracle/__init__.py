@@ -24,9 +24,14 @@ general
 merge
     The page's rule for merging partial softmax states, applied to the parts
     of a split key range.
+dropout
+    Dropout on the probabilities with a keep mask drawn from Philox4x32-10,
+    and the forward and backward for a given mask.
 
 Pins (what fixes each function other than itself) live in
-``tests/test_oracle_pins.py``; each function's docstring names its pins.
+``tests/test_oracle_pins.py``, ``tests/test_oracle_general.py``,
+``tests/test_oracle_dropout.py`` and ``tests/test_oracle_philox.py``; each
+module's docstring names its pins.
 No function here is "parity unpinned".
 
 Sources cited (title of the page, then its section):
@@ -35,6 +40,6 @@ Sources cited (title of the page, then its section):
   * "FlashAttention" (Road to Intelligence, Chapter 11)
 """
 
-from . import dense, tiled, finite_diff, general, merge  # noqa: F401
+from . import dense, tiled, finite_diff, general, merge, dropout  # noqa: F401
 
-__all__ = ["dense", "tiled", "finite_diff", "general", "merge"]
+__all__ = ["dense", "tiled", "finite_diff", "general", "merge", "dropout"]

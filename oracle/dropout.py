@@ -45,10 +45,13 @@ central finite differences of the masked forward pin the backward; the mean
 of O over many generator offsets converges to the dropout-free O (pins the
 1/keep scale and the mask's independence from the data); the kept fraction
 matches keep; the bytes are uniform and one flipped counter bit changes about
-half of the output bits. The generator's identity with the paper's is by
-construction only: parity unpinned for the generator constants themselves
-(any wrong constant would still give a statistically sound generator, which
-the GPU side must then match bit for bit).
+half of the output bits. The generator itself (``tests/test_oracle_philox.py``)
+is pinned to Triton's independent Philox4x32, run on the CPU through its
+interpreter, word for word at 1, 2, 7 and 10 rounds over edge and random
+counters and keys, and its two key increments to their closed forms (the
+first 32 fractional bits of the golden ratio and of sqrt(3)); near misses
+(swapped multipliers, a wrong increment, exchanged product halves, an early
+key bump, permuted words) each fail that pin.
 """
 
 from __future__ import annotations

@@ -5,11 +5,11 @@ Gate per tensor X in {dQ, dK, dV}: max|dX - dX_ref| / max|dX_ref| <= 5e-2
 at 1e-3: with a single key dQ is exactly zero (dS = P (dP - D) vanishes when
 P = 1), and fp32 rounding leaves ~1e-8 there. The GPU backward
 consumes the GPU forward's own O and LSE, as a training step would; the
-oracle uses its own float64 forward. Small problems are compared in full;
-the forward+backward workload runs at full size and is compared on a
-sample of whole heads, with invariants that hold at any size (finite
-gradients; the key gradients of a head sum to zero; the value gradients sum
-to the output gradients) checked on every head.
+oracle uses its own float64 forward. Small problems and the
+forward+backward workload at full size are compared on every head, with
+invariants that hold at any size (finite gradients; the key gradients of a
+head sum to zero; the value gradients sum to the output gradients) checked
+on top.
 """
 
 import math
@@ -81,11 +81,14 @@ def test_fwdbwd_workload_full_size():
     w = si.WORKLOADS[4]
     x = si.make_inputs(w)
     grads = _run(x, w.causal, w.scale)
-    heads = [(0, 0), (w.B - 1, w.H - 1), (3, 5)]
-    o_ref, lse_ref = dense.forward(x["q"], x["k"], x["v"], w.causal, w.scale, heads=heads)
-    refs = dense.backward(x["q"], x["k"], x["v"], o_ref, lse_ref, x["do"], w.causal, w.scale,
-                          heads=heads)
-    _check(grads, refs, heads)
+    # all 96 heads, element by element
+    o_ref, lse_ref = dense.forward(x["q"], x["k"], x["v"], w.causal, w.scale)
+    refs = dense.backward(x["q"], x["k"], x["v"], o_ref, lse_ref, x["do"], w.causal, w.scale)
+    _check(grads, refs)
+    # and head by head, so that one head's error cannot hide behind another's scale
+    for b in range(w.B):
+        for h in range(w.H):
+            _check([t[b:b + 1, h:h + 1] for t in grads], [r[b:b + 1, h:h + 1] for r in refs])
     dq, dk, dv = (t.float() for t in grads)
     assert torch.isfinite(dq).all() and torch.isfinite(dk).all() and torch.isfinite(dv).all()
     # invariants on every head (bf16 outputs: compare against the gradients' scale)

@@ -7,7 +7,7 @@ Two kinds of checks:
   (forward, O) or four queries (backward, dV); the codes are decoded from
   the kernel's outputs and compared with the oracle's mask;
 - O, LSE and the gradients on random inputs against ``oracle.dropout`` with
-  the gates of the dropout-free tests (forward: max |dO| <= 2e-2, mean
+  the gates of the dropout-free tests (forward: max |O - O_ref| <= 2e-2, mean
   <= 2e-3, LSE max <= 1e-3; backward: max-norm relative error <= 5e-2).
 """
 
@@ -146,8 +146,8 @@ def test_offset_changes_the_mask_and_repeats_are_identical():
 
 def test_fwdbwd_workload_full_size():
     """The forward+backward workload at full size (B=8, H=12, N=2048, d=64, causal) with p = 0.1,
-    the configuration the bench's dropout leg times: sampled heads against the oracle, and on every
-    head finite outputs and sum_j dK_j = 0 (row sums of dS vanish with dropout too, because
+    the configuration the bench's dropout leg times: every head against the oracle, head by head,
+    and finite outputs and sum_j dK_j = 0 (row sums of dS vanish with dropout too, because
     D_i = sum_j P_ij dP_ij)."""
     w = si.workload("causal_fwdbwd_b8h12_n2048_d64")
     x = si.make_inputs(w)
@@ -158,10 +158,9 @@ def test_fwdbwd_workload_full_size():
                                    scale=w.scale)
     torch.cuda.synchronize()
     assert fa.fa_get_last_device_status() == fa.FA_OK
-    heads = [(0, 0), (w.B - 1, w.H - 1), (3, 5)]
-    o_ref, lse_ref = dropout.forward(x["q"], x["k"], x["v"], True, w.scale, p, seed, offset, heads=heads)
-    refs = dropout.backward(x["q"], x["k"], x["v"], o_ref, lse_ref, x["do"], True, w.scale, p, seed, offset,
-                            heads=heads)
+    heads = [(b, h) for b in range(w.B) for h in range(w.H)]
+    o_ref, lse_ref = dropout.forward(x["q"], x["k"], x["v"], True, w.scale, p, seed, offset)
+    refs = dropout.backward(x["q"], x["k"], x["v"], o_ref, lse_ref, x["do"], True, w.scale, p, seed, offset)
     o_np, lse_np = o.float().cpu().double().numpy(), lse.cpu().double().numpy()
     for b, h in heads:
         err = np.abs(o_np[b, h] - o_ref[b, h])

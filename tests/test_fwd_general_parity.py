@@ -115,17 +115,16 @@ def test_fwd_ex_square_equals_fa_fwd():
     assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
 
 
-def test_decode_long_cache_sampled_heads():
+def test_decode_long_cache_every_head():
     # B=8 H=32 Nq=1 Nk=32768 d=128, causal: the decode workload at full size,
-    # compared on sampled heads.
+    # every one of the 256 heads compared.
     B, H, Nq, Nk, d = 8, 32, 1, 32768, 128
     q, k, v = _inputs(B, H, Nq, Nk, d, seed=31)
     o, lse = fa.fa_decode_splitkv(q.cuda(), k.cuda(), v.cuda(), causal=True)
     torch.cuda.synchronize()
     assert fa.fa_get_last_device_status() == fa.FA_OK
     assert torch.isfinite(o.float()).all() and torch.isfinite(lse).all()
-    heads = [(0, 0), (3, 17), (7, 31)]
-    _check(o, lse, q, k, v, True, 0, 1.0 / math.sqrt(d), heads=heads)
+    _check(o, lse, q, k, v, True, 0, 1.0 / math.sqrt(d))
 
 
 def test_invalid_extended_arguments_are_refused():

@@ -2,10 +2,10 @@
 
 Tolerances (bf16 inputs, fp32 accumulation): max |O - O_ref| <= 2e-2,
 mean |O - O_ref| <= 2e-3, max |LSE - LSE_ref| <= 1e-3, over every element
-compared. Small problems are compared in full; the five named workloads run
-at full size on the GPU and are compared on a sample of whole heads, with
-properties that hold at any size (finite outputs, outputs inside the convex
-hull of the values) checked on every head.
+compared. Small problems and the five named workloads at full size are all
+compared element by element on every head; properties that hold at any size
+(finite outputs, outputs inside the convex hull of the values) are checked
+on top.
 """
 
 import math
@@ -38,9 +38,9 @@ def _compare(o, lse, o_ref, lse_ref, heads=None):
         lse_ref = np.stack([lse_ref[b, h] for b, h in heads])
     err = np.abs(o - o_ref)
     lerr = np.abs(lse - lse_ref)
-    assert err.max() <= O_MAX, f"max |dO| = {err.max():.3e}"
-    assert err.mean() <= O_MEAN, f"mean |dO| = {err.mean():.3e}"
-    assert lerr.max() <= LSE_MAX, f"max |dLSE| = {lerr.max():.3e}"
+    assert err.max() <= O_MAX, f"max |O - O_ref| = {err.max():.3e}"
+    assert err.mean() <= O_MEAN, f"mean |O - O_ref| = {err.mean():.3e}"
+    assert lerr.max() <= LSE_MAX, f"max |LSE - LSE_ref| = {lerr.max():.3e}"
     return err.max(), err.mean(), lerr.max()
 
 
@@ -78,20 +78,15 @@ def test_small_against_oracle(B, H, N, d, causal):
     _compare(o, lse, o_ref, lse_ref)
 
 
-def _sample_heads(w, count=3):
-    heads = [(0, 0), (w.B - 1, w.H - 1), (w.B // 2, w.H // 2)]
-    return list(dict.fromkeys(heads))[:count]
-
-
 @pytest.mark.parametrize("idx", [0, 1, 2, 3, 4])
 def test_workload_full_size(idx):
     w = si.WORKLOADS[idx]
     x = si.make_inputs(w, with_grad=False)
     o, lse = _run(x, w.causal, w.scale)
-    heads = None if w.heads == 1 else _sample_heads(w)
-    o_ref, lse_ref = dense.forward(x["q"], x["k"], x["v"], w.causal, w.scale, heads=heads)
-    _compare(o, lse, o_ref, lse_ref, heads)
-    # every head: finite, and each output row inside the values' range
+    # every head, element by element
+    o_ref, lse_ref = dense.forward(x["q"], x["k"], x["v"], w.causal, w.scale)
+    _compare(o, lse, o_ref, lse_ref)
+    # finite, and each output row inside the values' range
     of = o.float()
     assert torch.isfinite(of).all() and torch.isfinite(lse).all()
     vf = x["v"].float().cuda()

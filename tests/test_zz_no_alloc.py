@@ -6,8 +6,9 @@ that must not call cudaMalloc while it runs. fa_bwd_noalloc serves them by
 keeping its workspace in a fixed-size device array inside the library. This
 file checks, through the C ABI, that two calls in a row give what the
 workspace-taking entry point gives (within the backward's tolerance, with
-dK and dV bitwise equal since each has one writer per element), and that a
-problem too large for the array is refused without a launch. It is collected
+dK and dV bitwise equal since each has one writer per element), that the
+Python binding's wrapper with caller-provided outputs does the same, and
+that a problem too large for the array is refused without a launch. It is collected
 last so that a failure here leaves every other test already run; it also
 passes on its own in a fresh process.
 """
@@ -63,6 +64,22 @@ def test_two_calls_match_the_workspace_entry_point(B, H, N, d, causal):
         assert torch.equal(dk, ref[1]) and torch.equal(dv, ref[2])
     # the two calls agree with each other as well (dQ up to atomic ordering)
     assert _rel(outs[1][0], outs[0][0]) <= REL_MAX
+
+
+def test_python_wrapper_with_preallocated_outputs():
+    # the binding's fa_bwd_noalloc (shape checks, caller-provided outputs,
+    # device and stream handling) gives what fa_bwd gives
+    B, H, N, d, causal = 1, 3, 300, 64, True
+    x = {k: t.cuda() for k, t in si.make_small(B, H, N, d, seed=5, with_grad=True).items()}
+    o, lse = fa.fa_fwd(x["q"], x["k"], x["v"], causal=causal)
+    ref = fa.fa_bwd(x["q"], x["k"], x["v"], o, lse, x["do"], causal=causal)
+    outs = tuple(torch.full_like(x["q"], float("nan")) for _ in range(3))
+    got = fa.fa_bwd_noalloc(x["q"], x["k"], x["v"], o, lse, x["do"], causal=causal, dq=outs[0],
+                            dk=outs[1], dv=outs[2], stream=torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    assert all(g is t for g, t in zip(got, outs))
+    assert _rel(got[0], ref[0]) <= REL_MAX
+    assert torch.equal(got[1], ref[1]) and torch.equal(got[2], ref[2])
 
 
 def test_problem_larger_than_the_scratch_is_refused():
