@@ -46,8 +46,8 @@ L2_FLUSH_BYTES = 256 << 20
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=si.WORKLOADS[4].name)
     ap.add_argument("--no-extras", action="store_true",
@@ -88,22 +88,39 @@ def window_pairs(N, window):
 
 def time_calls(fn, reps, warmup, stream, flush=None):
     """Median ms of fn() over `reps` launches on `stream` (CUDA events)."""
+    return time_segments([fn], reps, warmup, stream, flush)[0]["median"]
+
+
+def _stats(ts):
     import statistics
+    return {"median": statistics.median(ts), "min": min(ts), "mean": sum(ts) / len(ts), "n": len(ts)}
+
+
+def time_segments(fns, reps, warmup, stream, flush=None):
+    """Per-call ms statistics of a sequence of launches: each rep flushes L2
+    (outside the events), then runs fns[0], fns[1], ... on `stream` with a
+    CUDA event between consecutive calls. Returns one statistics dict
+    (median, min, mean, n) per call and one for the whole sequence."""
     import torch
     for _ in range(warmup):
-        fn()
-    torch.cuda.synchronize()
-    ts = []
-    for _ in range(reps):
         if flush is not None:
             flush()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        fn()
-        b.record(stream)
-        torch.cuda.synchronize()
-        ts.append(a.elapsed_time(b))
-    return statistics.median(ts)
+        for f in fns:
+            f()
+    torch.cuda.synchronize()
+    mk = lambda: torch.cuda.Event(enable_timing=True)
+    evs = [[mk() for _ in range(len(fns) + 1)] for _ in range(reps)]
+    for e in evs:
+        if flush is not None:
+            flush()
+        e[0].record(stream)
+        for i, f in enumerate(fns):
+            f()
+            e[i + 1].record(stream)
+    torch.cuda.synchronize()
+    per = [_stats([e[i].elapsed_time(e[i + 1]) for e in evs]) for i in range(len(fns))]
+    per.append(_stats([e[0].elapsed_time(e[-1]) for e in evs]))
+    return per
 
 
 def decode_leg(dev, stream, reps=20):
@@ -216,6 +233,134 @@ def dropout_leg(dev, stream, flush, reps=10):
             "bwd_tflops": round(f_bwd / (ms_b * 1e-3) / 1e12, 1),
             "step_tflops": round((f_fwd + f_bwd) / ((ms_f + ms_b) * 1e-3) / 1e12, 1),
             "note": "backward = preprocess + main + finish; keep mask from Philox4x32-10 in both"}
+
+
+class AbiProblem:
+    """Device buffers and C-ABI launches of one square problem [B, H, N, d]
+    (N queries = N keys, d = d_v): the forward and the three backward stages."""
+
+    def __init__(self, lib, x, causal, scale):
+        import torch
+        self.lib, self.x, self.causal, self.scale = lib, x, 1 if causal else 0, scale
+        self.B, self.H, self.N, self.d = (int(n) for n in x["q"].shape)
+        dev = x["q"].device
+        self.o = torch.empty_like(x["q"])
+        self.lse = torch.empty(self.B, self.H, self.N, dtype=torch.float32, device=dev)
+        if "do" in x:
+            self.dq, self.dk, self.dv = (torch.empty_like(x["q"]) for _ in range(3))
+            self.ws_bytes = lib.fa_bwd_workspace_bytes(self.B, self.H, self.N, self.d)
+            self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=dev)
+
+    @staticmethod
+    def _p(t):
+        return ctypes.c_void_p(t.data_ptr())
+
+    def _ok(self, rc, what):
+        if rc != 0:
+            raise RuntimeError(f"{what}: {rc}")
+
+    def fwd(self, stream):
+        p, x = self._p, self.x
+        self._ok(self.lib.fa_fwd_stream(p(x["q"]), p(x["k"]), p(x["v"]), p(self.o), p(self.lse),
+                                        self.B, self.H, self.N, self.d, self.causal, self.scale,
+                                        ctypes.c_void_p(stream.cuda_stream)), "fa_fwd_stream")
+
+    def pre(self, stream):
+        p = self._p
+        self._ok(self.lib.fa_bwd_preprocess_stream(p(self.o), p(self.lse), p(self.x["do"]), self.B,
+                                                   self.H, self.N, self.d, p(self.ws),
+                                                   ctypes.c_size_t(self.ws_bytes),
+                                                   ctypes.c_void_p(stream.cuda_stream)), "preprocess")
+
+    def main(self, stream):
+        p, x = self._p, self.x
+        self._ok(self.lib.fa_bwd_main_stream(p(x["q"]), p(x["k"]), p(x["v"]), p(x["do"]), p(self.dk),
+                                             p(self.dv), self.B, self.H, self.N, self.d, self.causal,
+                                             self.scale, p(self.ws), ctypes.c_size_t(self.ws_bytes),
+                                             ctypes.c_void_p(stream.cuda_stream)), "main")
+
+    def post(self, stream):
+        self._ok(self.lib.fa_bwd_finish_stream(self._p(self.dq), self.B, self.H, self.N, self.d,
+                                               self._p(self.ws), ctypes.c_size_t(self.ws_bytes),
+                                               ctypes.c_void_p(stream.cuda_stream)), "finish")
+
+
+def _rate(flops, st, peak):
+    """TFLOP/s at the median and the best launch, and the median's fraction of peak."""
+    tf = flops / (st["median"] * 1e-3) / 1e12
+    return {"ms_median": round(st["median"], 4), "ms_min": round(st["min"], 4), "launches": st["n"],
+            "tflops": round(tf, 1), "tflops_best": round(flops / (st["min"] * 1e-3) / 1e12, 1),
+            "frac": round(tf / peak, 4)}
+
+
+def mufu_ceiling(d, sm_mhz, sms):
+    """TFLOP/s the exponential unit allows: one exp2 per score element at 32
+    per clock per SM (measured on GB300), against 4 d FLOPs per element in the
+    forward (QK^T and PV) and 10 d in the backward (five contractions, one
+    recomputed exponential)."""
+    ex2_per_s = 32.0 * sms * sm_mhz * 1e6
+    return {"ex2_per_clk_per_sm": 32, "sm_mhz": sm_mhz, "sms": sms,
+            "fwd_tflops": round(ex2_per_s * 4 * d / 1e12, 1),
+            "bwd_tflops": round(ex2_per_s * 10 * d / 1e12, 1)}
+
+
+def config_legs(lib, dev, stream, flush, peak, sm_mhz, sms, reps=50, warmup=10):
+    """Every named workload, per pass: the forward, and where the workload has
+    a backward the whole backward and its main kernel alone; the median and
+    the best of `reps` launches, L2 flushed before each."""
+    import exact_io_aware_33_gb300 as fa
+    out = []
+    for w in si.WORKLOADS:
+        x = {n: t.to(dev) for n, t in si.make_inputs(w, with_grad=w.backward).items()}
+        pr = AbiProblem(lib, x, w.causal, w.scale)
+        f_fwd = fa.flops_fwd(w.B, w.H, w.N, w.d, w.causal)
+        mufu = mufu_ceiling(w.d, sm_mhz, sms)
+        st = time_segments([lambda: pr.fwd(stream)], reps, warmup, stream, flush)
+        out.append({"workload": w.name, "pass": "forward", **_rate(f_fwd, st[0], peak),
+                    "mufu_ceiling_tflops": mufu["fwd_tflops"]})
+        if w.backward:
+            pr.fwd(stream)
+            f_bwd = 2.5 * f_fwd
+            st = time_segments([lambda: pr.pre(stream), lambda: pr.main(stream), lambda: pr.post(stream)],
+                               reps, warmup, stream, flush)
+            out.append({"workload": w.name, "pass": "backward (preprocess + main + finish)",
+                        **_rate(f_bwd, st[3], peak), "mufu_ceiling_tflops": mufu["bwd_tflops"]})
+            out.append({"workload": w.name, "pass": "backward main kernel", **_rate(f_bwd, st[1], peak),
+                        "mufu_ceiling_tflops": mufu["bwd_tflops"]})
+        del pr, x
+    return out
+
+
+def sweep_leg(lib, dev, stream, flush, peak, sm_mhz, sms, reps=50, warmup=10):
+    """d = 128 at N = 4096, 8192 and 16384, causal and non-causal, with
+    B H N = 2^20 query rows at every N (1024 forward CTAs of 256 query rows:
+    6.7 waves over 152 SMs): forward, whole backward and backward main kernel.
+    Inputs: one seeded draw of iid N(0,1) bf16 rows, viewed as [B, H, N, 128]."""
+    import exact_io_aware_33_gb300 as fa
+    d, rows = 128, 1 << 20
+    x0 = si.make_small(1, 1, rows, d, seed=4096, with_grad=True)
+    x0 = {n: t.to(dev) for n, t in x0.items()}
+    out = []
+    for B, H, N in ((4, 16, 4096), (2, 16, 8192), (1, 16, 16384)):
+        x = {n: t.view(B, H, N, d) for n, t in x0.items()}
+        for causal in (True, False):
+            pr = AbiProblem(lib, x, causal, 1.0 / math.sqrt(d))
+            f_fwd = fa.flops_fwd(B, H, N, d, causal)
+            st_f = time_segments([lambda: pr.fwd(stream)], reps, warmup, stream, flush)
+            pr.fwd(stream)
+            st_b = time_segments([lambda: pr.pre(stream), lambda: pr.main(stream), lambda: pr.post(stream)],
+                                 reps, warmup, stream, flush)
+            out.append({"B": B, "H": H, "N": N, "d": d, "causal": causal,
+                        "fwd_ctas": B * H * ((N + 255) // 256),
+                        "fwd": _rate(f_fwd, st_f[0], peak),
+                        "bwd": _rate(2.5 * f_fwd, st_b[3], peak),
+                        "bwd_main": _rate(2.5 * f_fwd, st_b[1], peak)})
+            del pr
+    mufu = mufu_ceiling(d, sm_mhz, sms)
+    return {"points": out, "target_frac_fwd": 0.60,
+            "min_fwd_frac": min(r["fwd"]["frac"] for r in out),
+            "mufu_ceiling_tflops": {"fwd": mufu["fwd_tflops"], "bwd": mufu["bwd_tflops"]},
+            "timing": f"median and best of {reps} launches after {warmup} warm-ups, L2 flushed before each"}
 
 
 def max_over_ranks(values, device, world):
@@ -581,6 +726,8 @@ def run_ours(args):
         "kernels_ms": {"fa_fwd_kernel": round(ms_fwd, 4),
                        **({"fa_bwd_main": round(ms_bwd, 4)} if w.backward else {})},
         "kernels_tflops": {k: round(v[0] / (v[1] * 1e-3) / 1e12, 1) for k, v in kernels.items()},
+        "timed_region_stats_ms": {k: {m: round(x, 4) if m != "n" else x for m, x in _stats(v).items()}
+                                  for k, v in times.items()},
         "roofline": roofline,
         "gpu_launches": runner.launches_per_step * args.steps,
         "clocks": clocks,
@@ -596,15 +743,17 @@ def run_ours(args):
                       "steps": max(3, args.steps),
                       "pipeline": "uploads, compute and downloads on three streams, two buffer sets; "
                                   "timed from the first upload to the last download"}
-        # the long causal forward (B=1, H=16, N=8192, d=128), the head-size-128 target shape
-        wl = si.WORKLOADS[3]
-        rl = Runner(wl, dev)
-        tl, _ = timed_loop(rl, max(5, args.steps // 2), 3, barrier, stream)
-        ms_l = sum(tl["fwd"]) / len(tl["fwd"])
-        tf_l = step_flops(wl)[0] / (ms_l * 1e-3) / 1e12
-        out["fwd_long"] = {"workload": wl.name, "ms": round(ms_l, 4), "tflops": round(tf_l, 1),
-                           "frac": round(tf_l / peak, 4)}
-        del rl
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        sm_mhz = (clocks or {}).get("sm_mhz") or (clocks or {}).get("sm_max_mhz") or 2070.0
+        lib = runner.lib
+        out["configs"] = config_legs(lib, dev, stream, runner.flush_l2, peak, sm_mhz, sms)
+        long_fwd = next(r for r in out["configs"] if r["workload"] == si.WORKLOADS[3].name)
+        out["fwd_long"] = {"workload": si.WORKLOADS[3].name, "ms": long_fwd["ms_median"],
+                           "tflops": long_fwd["tflops"], "frac": long_fwd["frac"]}
+        out["sweep_d128"] = sweep_leg(lib, dev, stream, runner.flush_l2, peak, sm_mhz, sms)
+        out["mufu_ceiling"] = {"d64": mufu_ceiling(64, sm_mhz, sms), "d128": mufu_ceiling(128, sm_mhz, sms),
+                               "note": "exp2 at 32 per clock per SM (GB300, measured), one per score "
+                                       "element; FLOPs per element 4d forward, 10d backward"}
         out["decode"] = decode_leg(dev, stream)
         out["window"] = window_leg(dev, stream, runner.flush_l2)
         out["headsize"] = headsize_leg(dev, stream, runner.flush_l2)

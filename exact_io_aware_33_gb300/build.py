@@ -45,16 +45,23 @@ def _headers():
     return out
 
 
-def build(verbose: bool = False, force: bool = False, extra_flags=None) -> str:
-    """Compile the CUDA sources and link libfa.so; returns the library path."""
-    os.makedirs(BUILD, exist_ok=True)
+def build(verbose: bool = False, force: bool = False, extra_flags=None, out_dir: str | None = None,
+          lib_path: str | None = None) -> str:
+    """Compile the CUDA sources and link libfa.so; returns the library path.
+
+    ``out_dir`` / ``lib_path`` place the objects and the library elsewhere
+    (used for test-only variants built with extra ``-D`` flags; the product
+    library is always ``libfa.so`` next to this file)."""
+    build_dir = out_dir or BUILD
+    lib = lib_path or LIB
+    os.makedirs(build_dir, exist_ok=True)
     exe = nvcc()
     flags = NVCC_FLAGS + list(extra_flags or [])
     newest_header = max(os.path.getmtime(h) for h in _headers())
     procs, objs = [], []
     for src in SOURCES:
         path = os.path.join(CSRC, src)
-        obj = os.path.join(BUILD, src.replace(".cu", ".o"))
+        obj = os.path.join(build_dir, src.replace(".cu", ".o"))
         objs.append(obj)
         if (not force and os.path.exists(obj)
                 and os.path.getmtime(obj) >= max(os.path.getmtime(path), newest_header)):
@@ -75,15 +82,29 @@ def build(verbose: bool = False, force: bool = False, extra_flags=None) -> str:
     if failed:
         msg = "\n".join(f"--- {s}\n{t}" for s, t in failed)
         raise RuntimeError("nvcc failed:\n" + msg)
-    if force or procs or not os.path.exists(LIB) or any(
-            os.path.getmtime(o) > os.path.getmtime(LIB) for o in objs):
-        tmp = LIB + ".tmp"
+    if force or procs or not os.path.exists(lib) or any(
+            os.path.getmtime(o) > os.path.getmtime(lib) for o in objs):
+        tmp = lib + ".tmp"
         cmd = [exe, "-shared", "-o", tmp] + objs + ARCH
         r = subprocess.run(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT)
         if r.returncode != 0:
             raise RuntimeError("link failed:\n" + r.stdout.decode(errors="replace"))
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib)
+    return lib
+
+
+# Test-only variant for the bounded-wait (timeout) path: the forward's TMA
+# producer never loads the last V tile of its key stream, and every wait gives
+# up after 20 ms instead of about a second. It lives under _build/ and is
+# never loaded by the package; only tests/test_timeout_path.py uses it.
+TIMEOUT_TEST_DIR = os.path.join(BUILD, "timeout_test")
+TIMEOUT_TEST_FLAGS = ["-DFA_TEST_SKIP_ARRIVE", "-DFA_WAIT_BUDGET_NS=20000000ull"]
+
+
+def build_timeout_test_variant(verbose: bool = False) -> str:
+    """Build the test-only timeout variant of the library; returns its path."""
+    return build(verbose=verbose, extra_flags=TIMEOUT_TEST_FLAGS, out_dir=TIMEOUT_TEST_DIR,
+                 lib_path=os.path.join(TIMEOUT_TEST_DIR, "libfa_timeout_test.so"))
 
 
 if __name__ == "__main__":

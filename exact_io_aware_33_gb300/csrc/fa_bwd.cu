@@ -282,6 +282,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_steps = bwd_query_blocks_end(args, jb) - i0;
   const int warp = warp_id();
   const int lane = lane_id();
+  int issued = 0;  // producer: query stages whose copies were started
 
   if (threadIdx.x == 0) {
     mbar_init(bar(C::kBarKV), 1);
@@ -321,7 +322,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_3d(base + C::kKOff + c * C::kChunkBytes, &tmK, bar(C::kBarKV), c * 64, jb * kBlk, bh);
       for (int c = 0; c < C::kChunksV; ++c)
         tma_load_3d(base + C::kVOff + c * C::kChunkBytes, &tmV, bar(C::kBarKV), c * 64, jb * kBlk, bh);
-      int issued = 0;
       bool ok = true;
       for (int it = 0; it < n_steps; ++it) {
         const int s = it % C::kStages;
@@ -340,11 +340,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         bulk_load(st + C::kTileBytes + C::kVTileBytes, args.lse2 + voff, kBlk * 4, fb);
         bulk_load(st + C::kTileBytes + C::kVTileBytes + kBlk * 4, args.Dvec + voff, kBlk * 4, fb);
         issued = it + 1;
-      }
-      if (*abort_flag) {
-        mbar_wait_sleep(bar(C::kBarKV), 0, nullptr);
-        for (int it = issued - 1; it >= 0 && it >= issued - C::kStages; --it)
-          mbar_wait_sleep(bar(C::kBarQFull + it % C::kStages), (it / C::kStages) & 1, nullptr);
       }
     }
   } else if (warp == kMmaWarp) {
@@ -599,6 +594,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
+  if (warp == kLoadWarp && lane == 0 && *abort_flag) {
+    // Every role has stopped, so the flag is final here: let every copy this
+    // thread started land before the CTA exits (consumers that gave up no
+    // longer wait for them; only the last kStages stages can be pending).
+    mbar_wait_sleep(bar(C::kBarKV), 0, nullptr);
+    for (int it = issued - 1; it >= 0 && it >= issued - C::kStages; --it)
+      mbar_wait_sleep(bar(C::kBarQFull + it % C::kStages), (it / C::kStages) & 1, nullptr);
+  }
   if (warp == kMmaWarp) {
     __syncwarp();
     tc_fence_after();
@@ -744,6 +747,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
   const int warp = warp_id();
   const int lane = lane_id();
+  // producer: query steps and K/V items whose copies were started
+  int loaded_steps = 0, loaded_kv = 0;
 
   if (threadIdx.x == 0) {
     for (int b = 0; b < 2; ++b) {
@@ -785,7 +790,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_map(&tmK);
       tma_prefetch_map(&tmV);
       tma_prefetch_map(&tmDO);
-      int g = 0, n_kv = 0;
+      int& g = loaded_steps;
+      int& n_kv = loaded_kv;
       bool ok = true;
       auto load_q = [&](int bh, int row0) {  // query block of global step g
         const int s = g % kStages;
@@ -817,13 +823,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_3d(base + kVOff + kv * kKVBytes, &tmV, bar(kBarKV + kv), 0, jb * kBlk, bh);
         ++n_kv;
         for (int it = 1; it < ns && ok; ++it) load_q(bh, (i0 + it) * kBlk);
-      }
-      if (*abort_flag) {
-        // Let every copy this thread started land before the CTA exits.
-        for (int m = n_kv - 1; m >= 0 && m >= n_kv - 2; --m)
-          mbar_wait(bar(kBarKV + (m & 1)), (m >> 1) & 1, nullptr);
-        for (int q = g - 1; q >= 0 && q >= g - kStages; --q)
-          mbar_wait(bar(kBarQFull + q % kStages), (q / kStages) & 1, nullptr);
       }
     }
   } else if (warp == kMmaWarp) {
@@ -1190,6 +1189,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
+  if (warp == kLoadWarp && lane == 0 && *abort_flag) {
+    // Every role has stopped, so the flag is final here: let every copy this
+    // thread started land before the CTA exits (consumers that gave up no
+    // longer wait for them; only the last two K/V loads and the last kStages
+    // query stages can be pending).
+    for (int m = loaded_kv - 1; m >= 0 && m >= loaded_kv - 2; --m)
+      mbar_wait(bar(kBarKV + (m & 1)), (m >> 1) & 1, nullptr);
+    for (int q = loaded_steps - 1; q >= 0 && q >= loaded_steps - kStages; --q)
+      mbar_wait(bar(kBarQFull + q % kStages), (q / kStages) & 1, nullptr);
+  }
   if (warp == kMmaWarp) {
     __syncwarp();
     tc_fence_after();

@@ -187,6 +187,7 @@ __global__ void __launch_bounds__(FwdCfg<D, DV, QT>::kThreads, FwdCfg<D, DV, QT>
 
   const int warp = warp_id();
   const int lane = lane_id();
+  int issued = 0;  // producer: K/V copies started (K of step jj is 2 jj, its V 2 jj + 1)
 
   if (threadIdx.x == 0) {
     mbar_init(bar(C::kBarQFull), 1);
@@ -234,7 +235,6 @@ __global__ void __launch_bounds__(FwdCfg<D, DV, QT>::kThreads, FwdCfg<D, DV, QT>
           tma_load_3d(base + C::kQOff + t * C::kTileBytes + c * C::kChunkBytes, &tmQ,
                       bar(C::kBarQFull), c * 64, q_row0[t], bh);
       }
-      int issued = 0;
       bool ok = true;
       for (int jj = 0; jj < n_stream && ok; ++jj) {
         const int s = jj % C::kStages;
@@ -246,6 +246,15 @@ __global__ void __launch_bounds__(FwdCfg<D, DV, QT>::kThreads, FwdCfg<D, DV, QT>
         for (int c = 0; c < C::kChunks; ++c)
           tma_load_3d(base + C::kKOff + s * C::kTileBytes + c * C::kChunkBytes, &tmK,
                       bar(C::kBarKFull + s), c * 64, key0, bh);
+#ifdef FA_TEST_SKIP_ARRIVE
+        // Test-only build (never in libfa.so): the stream's last V tile is
+        // never loaded, so the MMA thread's bounded wait for it runs out and
+        // the CTA winds down through the abort path.
+        if (jj == n_stream - 1) {
+          issued = 2 * jj + 1;
+          break;
+        }
+#endif
         if (jj >= C::kStages) ok = mbar_wait(bar(C::kBarVEmpty + s), ph, abort_flag);
         if (!ok) {
           issued = 2 * jj + 1;
@@ -256,16 +265,6 @@ __global__ void __launch_bounds__(FwdCfg<D, DV, QT>::kThreads, FwdCfg<D, DV, QT>
           tma_load_3d(base + C::kVOff + s * C::kVTileBytes + c * C::kChunkBytes, &tmV,
                       bar(C::kBarVFull + s), c * 64, key0, bh);
         issued = 2 * jj + 2;
-      }
-      if (*abort_flag) {
-        // Let every copy this thread started land before the CTA exits.
-        mbar_wait(bar(C::kBarQFull), 0, nullptr);
-        for (int x = issued - 1; x >= 0 && x >= issued - 2 * C::kStages; --x) {
-          const int jj = x >> 1;
-          const int s = jj % C::kStages;
-          const int b = (x & 1) ? (C::kBarVFull + s) : (C::kBarKFull + s);
-          mbar_wait(bar(b), (jj / C::kStages) & 1, nullptr);
-        }
       }
     }
   } else if (warp == kMmaWarp) {
@@ -688,6 +687,19 @@ __global__ void __launch_bounds__(FwdCfg<D, DV, QT>::kThreads, FwdCfg<D, DV, QT>
 
   tc_fence_before();
   __syncthreads();
+  if (warp == kLoadWarp && lane == 0 && *abort_flag) {
+    // Every role has stopped, so the flag is final here. Consumers that gave
+    // up no longer wait for the copies in flight: let every copy this thread
+    // started land before the CTA exits (only the last 2 x stages can still
+    // be pending: each earlier one was waited for before its slot was reused).
+    mbar_wait(bar(C::kBarQFull), 0, nullptr);
+    for (int x = issued - 1; x >= 0 && x >= issued - 2 * C::kStages; --x) {
+      const int jj = x >> 1;
+      const int s = jj % C::kStages;
+      const int b = (x & 1) ? (C::kBarVFull + s) : (C::kBarKFull + s);
+      mbar_wait(bar(b), (jj / C::kStages) & 1, nullptr);
+    }
+  }
   if (warp == kMmaWarp) {
     __syncwarp();
     tc_fence_after();

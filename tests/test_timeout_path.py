@@ -1,0 +1,78 @@
+"""The bounded-wait (timeout) path of the kernels, on the GPU, without a fault.
+
+Every wait inside the kernels gives up after a wall-clock budget, raises the
+CTA's abort flag, and every role winds down: the TMA producer lets its copies
+in flight land, the MMA thread waits for its MMAs, TMEM is freed, and the
+kernel sets the device status word that ``fa_get_last_device_status`` turns
+into FA_ERR_TIMEOUT. A test-only variant of the library (built separately
+with ``-DFA_TEST_SKIP_ARRIVE``, never part of ``libfa.so``) makes that happen
+on purpose: the forward's producer never loads the last V tile of its key
+stream, so the MMA thread's wait for it runs out after the variant's 20 ms
+budget. The test checks that the call returns, that the status says
+FA_ERR_TIMEOUT (once: reading it clears it), and that the same process then
+runs the product library's forward and backward with results matching the
+oracle, i.e. the context is intact.
+"""
+
+import ctypes
+import math
+import time
+
+import numpy as np
+import pytest
+
+import synthetic_inputs as si
+from oracle import dense
+
+torch = pytest.importorskip("torch")
+fa = pytest.importorskip("exact_io_aware_33_gb300")
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def timeout_lib():
+    from exact_io_aware_33_gb300 import build as b
+    return fa.load_library(b.build_timeout_test_variant())
+
+
+def _p(t):
+    return ctypes.c_void_p(t.data_ptr())
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_wait_runs_out_and_the_context_survives(timeout_lib, d):
+    B, H, N, scale = 1, 1, 256, 1.0 / math.sqrt(d)
+    x = si.make_small(B, H, N, d, seed=3100 + d, with_grad=True)
+    g = {n: t.cuda() for n, t in x.items()}
+    o = torch.empty_like(g["q"])
+    lse = torch.empty(B, H, N, dtype=torch.float32, device="cuda")
+    torch.cuda.synchronize()
+    assert fa.fa_get_last_device_status() == fa.FA_OK
+
+    t0 = time.perf_counter()
+    rc = timeout_lib.fa_fwd_stream(_p(g["q"]), _p(g["k"]), _p(g["v"]), _p(o), _p(lse), B, H, N, d, 0,
+                                   scale, ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert rc == fa.FA_OK  # launched; the failure shows in the status word
+    status = timeout_lib.fa_get_last_device_status()  # synchronises the device
+    elapsed = time.perf_counter() - t0
+    assert status == fa.FA_ERR_TIMEOUT
+    assert elapsed < 10.0, f"the wind-down took {elapsed:.2f} s"
+    assert timeout_lib.fa_get_last_device_status() == fa.FA_OK  # read once, then cleared
+    # the product library's status word is separate and untouched
+    assert fa.fa_get_last_device_status() == fa.FA_OK
+
+    # the context still works: a normal forward and backward in the same process
+    torch.cuda.synchronize()
+    o2, lse2 = fa.fa_fwd(g["q"], g["k"], g["v"], causal=False, scale=scale)
+    grads = fa.fa_bwd(g["q"], g["k"], g["v"], o2, lse2, g["do"], causal=False, scale=scale)
+    torch.cuda.synchronize()
+    assert fa.fa_get_last_device_status() == fa.FA_OK
+    o_ref, lse_ref = dense.forward(x["q"], x["k"], x["v"], False, scale)
+    err = np.abs(o2.float().cpu().double().numpy() - o_ref)
+    assert err.max() <= 2e-2 and err.mean() <= 2e-3
+    assert np.abs(lse2.cpu().double().numpy() - lse_ref).max() <= 1e-3
+    refs = dense.backward(x["q"], x["k"], x["v"], o_ref, lse_ref, x["do"], False, scale)
+    for got, ref in zip(grads, refs):
+        gg = got.float().cpu().double().numpy()
+        assert np.abs(gg - ref).max() / np.abs(ref).max() <= 5e-2
