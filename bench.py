@@ -333,11 +333,11 @@ def config_legs(lib, dev, stream, flush, peak, sm_mhz, sms, reps=50, warmup=10):
 
 def sweep_leg(lib, dev, stream, flush, peak, sm_mhz, sms, reps=50, warmup=10):
     """d = 128 at N = 4096, 8192 and 16384, causal and non-causal, with
-    B H N = 2^20 query rows at every N (1024 forward CTAs of 256 query rows:
+    B H N = 2^18 query rows at every N (1024 forward CTAs of 256 query rows:
     6.7 waves over 152 SMs): forward, whole backward and backward main kernel.
     Inputs: one seeded draw of iid N(0,1) bf16 rows, viewed as [B, H, N, 128]."""
     import exact_io_aware_33_gb300 as fa
-    d, rows = 128, 1 << 20
+    d, rows = 128, 1 << 18
     x0 = si.make_small(1, 1, rows, d, seed=4096, with_grad=True)
     x0 = {n: t.to(dev) for n, t in x0.items()}
     out = []

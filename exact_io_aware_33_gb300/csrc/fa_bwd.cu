@@ -292,10 +292,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int h = 0; h < 2; ++h) {
       mbar_init(bar(C::kBarSFull + h), 1);
-      mbar_init(bar(C::kBarDSFull + h), 128);
+      mbar_init(bar(C::kBarDSFull + h), 4);  // one arrival per warp of warpgroup h
     }
     mbar_init(bar(C::kBarDQFull), 1);
-    mbar_init(bar(C::kBarDQEmpty), 128);
+    mbar_init(bar(C::kBarDQEmpty), 4);
     mbar_init(bar(C::kBarDKDV), 1);
     mbar_init(bar(C::kBarDrain), 1);
     *abort_flag = 0;
@@ -508,7 +508,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_st_wait();
       tc_fence_before();
       fence_async_smem();
-      mbar_arrive(bar(C::kBarDSFull + w));
+      mbar_arrive_warp(bar(C::kBarDSFull + w));
     }
   } else if (warp < kMmaWarp) {
     // ------------------------------------------------------------ dQ, dK, dV out
@@ -529,7 +529,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld_wait(g);
         if (c == D / 32 - 1) {  // dQ has left tensor memory: its columns are free
           tc_fence_before();
-          mbar_arrive(bar(C::kBarDQEmpty));
+          mbar_arrive_warp(bar(C::kBarDQEmpty));
         }
         if (q < N) {
 #pragma unroll
@@ -760,9 +760,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(kBarQEmpty + s), 1);
     }
     mbar_init(bar(kBarSFull), 1);
-    mbar_init(bar(kBarSFree), kPdsThreads);
+    mbar_init(bar(kBarSFree), kPdsThreads / 32);  // one arrival per warp
     mbar_init(bar(kBarPFree), 1);
-    mbar_init(bar(kBarDSFull), kPdsThreads + 128);
+    mbar_init(bar(kBarDSFull), kPdsThreads / 32 + 4);  // one arrival per warp
     mbar_init(bar(kBarDQFull), 1);
     mbar_init(bar(kBarDKDV), 1);
     mbar_init(bar(kBarDrain), 1);
@@ -993,7 +993,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // S^T and dP^T of this step are in registers: the next step's MMAs may
       // overwrite their columns (its Q and dO have landed, checked above).
       tc_fence_before();
-      mbar_arrive(bar(kBarSFree));
+      mbar_arrive_warp(bar(kBarSFree));
 
       const RowMask rm = bwd_row_mask(args, i0 + it, jb, key_row);
       const bool win = args.window != 0 && rm.active;
@@ -1073,7 +1073,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_st_wait();
       tc_fence_before();
       fence_async_smem();
-      mbar_arrive(bar(kBarDSFull));
+      mbar_arrive_warp(bar(kBarDSFull));
     }
     }
   } else if (warp < kMmaWarp) {
@@ -1105,7 +1105,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       pending = true;
     };
     int g = 0;
-    mbar_arrive(bar(kBarDSFull));  // the first step has no dQ to read out
+    mbar_arrive_warp(bar(kBarDSFull));  // the first step has no dQ to read out
     for (int n = 0; ok; ++n) {
       int xi, jb, bh, i0, ns;
       if (!item_of(n, num_items, &xi)) break;
@@ -1124,7 +1124,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld32(tmem + lane_base + kColDQ + 32, gr);
         tmem_ld_wait(gr);
         tc_fence_before();
-        if (it + 1 < ns) mbar_arrive(bar(kBarDSFull));  // dQ columns free for step g+1
+        if (it + 1 < ns) mbar_arrive_warp(bar(kBarDSFull));  // dQ columns free for step g+1
         put_block(gr, dst + 1024);
       }
       if (!ok) break;
@@ -1157,7 +1157,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld_wait(gr);
           if (which == 1 && c == kD / 32 - 1) {  // dQ, dK, dV columns free for the next item
             tc_fence_before();
-            mbar_arrive(bar(kBarDSFull));
+            mbar_arrive_warp(bar(kBarDSFull));
           }
           uint32_t pk[16];
 #pragma unroll

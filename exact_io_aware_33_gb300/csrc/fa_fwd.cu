@@ -199,9 +199,9 @@ __global__ void __launch_bounds__(FwdCfg<D, DV, QT>::kThreads, FwdCfg<D, DV, QT>
     }
     for (int t = 0; t < kQTiles; ++t) {
       mbar_init(bar(C::kBarSFull + t), 1);
-      mbar_init(bar(C::kBarPFull + t), 128);
+      mbar_init(bar(C::kBarPFull + t), 4);   // one arrival per softmax warp
       mbar_init(bar(C::kBarOFinal + t), 1);
-      mbar_init(bar(C::kBarSFree + t), 128);
+      mbar_init(bar(C::kBarSFree + t), 4);
       mbar_init(bar(C::kBarPVDone + t), 1);
     }
     mbar_init(bar(C::kBarDrain), 1);
@@ -498,7 +498,7 @@ __global__ void __launch_bounds__(FwdCfg<D, DV, QT>::kThreads, FwdCfg<D, DV, QT>
       for (int c = 0; c < 4; ++c) tmem_ld_wait(sr[c]);
       if constexpr (C::kSepP) {  // S is in registers: the next QK^T may overwrite it
         tc_fence_before();
-        mbar_arrive(bar(C::kBarSFree + t));
+        mbar_arrive_warp(bar(C::kBarSFree + t));
       }
       float x[128];
 #pragma unroll
@@ -598,7 +598,7 @@ __global__ void __launch_bounds__(FwdCfg<D, DV, QT>::kThreads, FwdCfg<D, DV, QT>
       }
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(bar(C::kBarPFull + t));
+      mbar_arrive_warp(bar(C::kBarPFull + t));
     }
     const bool live = row < Nq;
     const size_t prow = (static_cast<size_t>(blockIdx.y) * args.BH + bh) * Nq + row;  // split launch

@@ -60,6 +60,18 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
+// One arrival for the whole warp, from lane 0 once every lane has reached
+// this point: the warp barrier orders each lane's earlier shared-memory and
+// (waited-for) tensor-memory writes before lane 0's releasing arrive. A
+// barrier fed this way counts warps, not threads. Thirty-two lanes arriving
+// one by one on the same barrier word are serialised by the shared-memory
+// pipe, which the tensor core also reads its operands through.
+// All 32 lanes must call it together.
+__device__ __forceinline__ void mbar_arrive_warp(uint32_t bar) {
+  __syncwarp();
+  if ((threadIdx.x & 31u) == 0) mbar_arrive(bar);
+}
+
 __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
