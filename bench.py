@@ -52,6 +52,14 @@ def parse():
     ap.add_argument("--workload", default=si.WORKLOADS[4].name)
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the end-to-end, CPU-baseline and long-forward legs")
+    ap.add_argument("--only", default=None,
+                    help="run one extra leg alone and print its JSON (for profiling): configs, "
+                         "sweep, decode, window, headsize, dropout, or workload:<name>")
+    ap.add_argument("--decode-nk", type=int, default=32768,
+                    help="cached keys per sequence in the decode leg")
+    ap.add_argument("--sweep-n", default="4096,8192,16384",
+                    help="sequence lengths of the d=128 sweep (comma-separated)")
+    ap.add_argument("--sweep-causal", choices=["both", "causal", "noncausal"], default="both")
     return ap.parse_args()
 
 
@@ -102,34 +110,35 @@ def time_segments(fns, reps, warmup, stream, flush=None):
     CUDA event between consecutive calls. Returns one statistics dict
     (median, min, mean, n) per call and one for the whole sequence."""
     import torch
-    for _ in range(warmup):
-        if flush is not None:
-            flush()
-        for f in fns:
-            f()
-    torch.cuda.synchronize()
-    mk = lambda: torch.cuda.Event(enable_timing=True)
-    evs = [[mk() for _ in range(len(fns) + 1)] for _ in range(reps)]
-    for e in evs:
-        if flush is not None:
-            flush()
-        e[0].record(stream)
-        for i, f in enumerate(fns):
-            f()
-            e[i + 1].record(stream)
-    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):  # the flush runs on the timed stream, ahead of the calls
+        for _ in range(warmup):
+            if flush is not None:
+                flush()
+            for f in fns:
+                f()
+        torch.cuda.synchronize()
+        mk = lambda: torch.cuda.Event(enable_timing=True)
+        evs = [[mk() for _ in range(len(fns) + 1)] for _ in range(reps)]
+        for e in evs:
+            if flush is not None:
+                flush()
+            e[0].record(stream)
+            for i, f in enumerate(fns):
+                f()
+                e[i + 1].record(stream)
+        torch.cuda.synchronize()
     per = [_stats([e[i].elapsed_time(e[i + 1]) for e in evs]) for i in range(len(fns))]
     per.append(_stats([e[0].elapsed_time(e[-1]) for e in evs]))
     return per
 
 
-def decode_leg(dev, stream, reps=20):
-    """Split-key-range decode: 8 sequences x 32 heads, one query over 32768
-    cached keys (d = 128, causal). HBM-bound: every key and value is read
-    once; the roofline counts K, V, Q, O and the fp32 partial states."""
+def decode_leg(dev, stream, reps=20, Nk=32768):
+    """Split-key-range decode: 8 sequences x 32 heads, one query over Nk
+    (32768) cached keys (d = 128, causal). HBM-bound: every key and value is
+    read once; the roofline counts K, V, Q, O and the fp32 partial states."""
     import torch
     import exact_io_aware_33_gb300 as fa
-    B, H, Nq, Nk, d = 8, 32, 1, 32768, 128
+    B, H, Nq, d = 8, 32, 1, 128
     # drawn on the device (seeded): 2 x 1 G values would take long on the host
     g = torch.Generator(device=dev).manual_seed(4242)
     q = torch.randn(B, H, Nq, d, generator=g, device=dev).to(torch.bfloat16)
@@ -146,10 +155,10 @@ def decode_leg(dev, stream, reps=20):
     algo = 2 * B * H * Nk * d * 2 + 2 * B * H * Nq * d * 2 + B * H * Nq * 4 + 2 * part
     peak, src = measured_hbm_gbs()
     gbs = algo / (ms * 1e-3) / 1e9
-    return {"workload": "decode_b8h32_nq1_nk32768_d128_causal", "splits": splits, "ms": round(ms, 4),
+    return {"workload": f"decode_b8h32_nq1_nk{Nk}_d128_causal", "splits": splits, "ms": round(ms, 4),
             "bytes": algo, "gbs": round(gbs, 1), "peak_gbs": peak, "frac": round(gbs / peak, 4),
             "bound": "hbm", "peak_source": f"{src} copy bandwidth (MEASURED_PEAKS.json)",
-            "l2": "inputs (4.3 GB) larger than L2"}
+            "l2": f"inputs ({2 * B * H * Nk * d * 2 / 1e9:.1f} GB) larger than L2"}
 
 
 def headsize_leg(dev, stream, flush, reps=10):
@@ -304,13 +313,15 @@ def mufu_ceiling(d, sm_mhz, sms):
             "bwd_tflops": round(ex2_per_s * 10 * d / 1e12, 1)}
 
 
-def config_legs(lib, dev, stream, flush, peak, sm_mhz, sms, reps=50, warmup=10):
-    """Every named workload, per pass: the forward, and where the workload has
-    a backward the whole backward and its main kernel alone; the median and
-    the best of `reps` launches, L2 flushed before each."""
+def config_legs(lib, dev, stream, flush, peak, sm_mhz, sms, reps=50, warmup=10, names=None):
+    """Every named workload (or those in `names`), per pass: the forward, and
+    where the workload has a backward the whole backward and its main kernel
+    alone; the median and the best of `reps` launches, L2 flushed before each."""
     import exact_io_aware_33_gb300 as fa
     out = []
     for w in si.WORKLOADS:
+        if names is not None and w.name not in names:
+            continue
         x = {n: t.to(dev) for n, t in si.make_inputs(w, with_grad=w.backward).items()}
         pr = AbiProblem(lib, x, w.causal, w.scale)
         f_fwd = fa.flops_fwd(w.B, w.H, w.N, w.d, w.causal)
@@ -331,7 +342,8 @@ def config_legs(lib, dev, stream, flush, peak, sm_mhz, sms, reps=50, warmup=10):
     return out
 
 
-def sweep_leg(lib, dev, stream, flush, peak, sm_mhz, sms, reps=50, warmup=10):
+def sweep_leg(lib, dev, stream, flush, peak, sm_mhz, sms, reps=50, warmup=10,
+              lengths=(4096, 8192, 16384), masks=(True, False)):
     """d = 128 at N = 4096, 8192 and 16384, causal and non-causal, with
     B H N = 2^18 query rows at every N (1024 forward CTAs of 256 query rows:
     6.7 waves over 152 SMs): forward, whole backward and backward main kernel.
@@ -341,9 +353,11 @@ def sweep_leg(lib, dev, stream, flush, peak, sm_mhz, sms, reps=50, warmup=10):
     x0 = si.make_small(1, 1, rows, d, seed=4096, with_grad=True)
     x0 = {n: t.to(dev) for n, t in x0.items()}
     out = []
-    for B, H, N in ((4, 16, 4096), (2, 16, 8192), (1, 16, 16384)):
+    for N in lengths:
+        H = 16
+        B = rows // (H * N)
         x = {n: t.view(B, H, N, d) for n, t in x0.items()}
-        for causal in (True, False):
+        for causal in masks:
             pr = AbiProblem(lib, x, causal, 1.0 / math.sqrt(d))
             f_fwd = fa.flops_fwd(B, H, N, d, causal)
             st_f = time_segments([lambda: pr.fwd(stream)], reps, warmup, stream, flush)
@@ -754,7 +768,7 @@ def run_ours(args):
         out["mufu_ceiling"] = {"d64": mufu_ceiling(64, sm_mhz, sms), "d128": mufu_ceiling(128, sm_mhz, sms),
                                "note": "exp2 at 32 per clock per SM (GB300, measured), one per score "
                                        "element; FLOPs per element 4d forward, 10d backward"}
-        out["decode"] = decode_leg(dev, stream)
+        out["decode"] = decode_leg(dev, stream, Nk=args.decode_nk)
         out["window"] = window_leg(dev, stream, runner.flush_l2)
         out["headsize"] = headsize_leg(dev, stream, runner.flush_l2)
         out["dropout"] = dropout_leg(dev, stream, runner.flush_l2)
@@ -763,6 +777,41 @@ def run_ours(args):
     print(json.dumps(out), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
+
+
+def run_only(args):
+    """One extra leg alone, its JSON printed (a profiling target, not the
+    bench line)."""
+    import torch
+    import exact_io_aware_33_gb300 as fa
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.Stream(dev)
+    lib = fa.load_library()
+    flush_buf = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flush = flush_buf.zero_
+    peak = measured_peaks()[0]
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    leg = args.only
+    if leg.startswith("workload:"):
+        res = config_legs(lib, dev, stream, flush, peak, 2070.0, sms, names={leg.split(":", 1)[1]})
+    elif leg == "configs":
+        res = config_legs(lib, dev, stream, flush, peak, 2070.0, sms)
+    elif leg == "sweep":
+        masks = {"both": (True, False), "causal": (True,), "noncausal": (False,)}[args.sweep_causal]
+        res = sweep_leg(lib, dev, stream, flush, peak, 2070.0, sms,
+                        lengths=tuple(int(n) for n in args.sweep_n.split(",")), masks=masks)
+    elif leg == "decode":
+        res = decode_leg(dev, stream, Nk=args.decode_nk)
+    elif leg == "window":
+        res = window_leg(dev, stream, flush)
+    elif leg == "headsize":
+        res = headsize_leg(dev, stream, flush)
+    elif leg == "dropout":
+        res = dropout_leg(dev, stream, flush)
+    else:
+        raise SystemExit(f"unknown leg {leg!r}")
+    print(json.dumps({"only": leg, "result": res}), flush=True)
 
 
 def run_reference(args):
@@ -810,6 +859,8 @@ def main():
     args = parse()
     if args.impl == "reference":
         run_reference(args)
+    elif args.only:
+        run_only(args)
     else:
         run_ours(args)
 
