@@ -54,7 +54,7 @@ def parse():
                     help="skip the end-to-end, CPU-baseline and long-forward legs")
     ap.add_argument("--only", default=None,
                     help="run one extra leg alone and print its JSON (for profiling): configs, "
-                         "sweep, decode, window, headsize, dropout, or workload:<name>")
+                         "sweep, d256, decode, window, headsize, dropout, or workload:<name>")
     ap.add_argument("--decode-nk", type=int, default=32768,
                     help="cached keys per sequence in the decode leg")
     ap.add_argument("--sweep-n", default="4096,8192,16384",
@@ -375,6 +375,22 @@ def sweep_leg(lib, dev, stream, flush, peak, sm_mhz, sms, reps=50, warmup=10,
             "min_fwd_frac": min(r["fwd"]["frac"] for r in out),
             "mufu_ceiling_tflops": {"fwd": mufu["fwd_tflops"], "bwd": mufu["bwd_tflops"]},
             "timing": f"median and best of {reps} launches after {warmup} warm-ups, L2 flushed before each"}
+
+
+def d256_leg(lib, dev, stream, flush, peak, sm_mhz, sms, reps=50, warmup=10):
+    """Head size d = d_v = 256 (forward only: B=2 H=16 N=4096, causal and
+    non-causal; one 128-row query tile per CTA, 1024 CTAs)."""
+    import exact_io_aware_33_gb300 as fa
+    B, H, N, d = 2, 16, 4096, 256
+    x = {n: t.to(dev) for n, t in si.make_small(B, H, N, d, seed=256, with_grad=False).items()}
+    out = []
+    for causal in (True, False):
+        pr = AbiProblem(lib, x, causal, 1.0 / math.sqrt(d))
+        st = time_segments([lambda: pr.fwd(stream)], reps, warmup, stream, flush)
+        out.append({"B": B, "H": H, "N": N, "d": d, "causal": causal,
+                    "fwd": _rate(fa.flops_fwd(B, H, N, d, causal), st[0], peak)})
+        del pr
+    return {"points": out, "mufu_ceiling_tflops": mufu_ceiling(d, sm_mhz, sms)["fwd_tflops"]}
 
 
 def max_over_ranks(values, device, world):
@@ -768,6 +784,7 @@ def run_ours(args):
         out["mufu_ceiling"] = {"d64": mufu_ceiling(64, sm_mhz, sms), "d128": mufu_ceiling(128, sm_mhz, sms),
                                "note": "exp2 at 32 per clock per SM (GB300, measured), one per score "
                                        "element; FLOPs per element 4d forward, 10d backward"}
+        out["fwd_d256"] = d256_leg(lib, dev, stream, runner.flush_l2, peak, sm_mhz, sms)
         out["decode"] = decode_leg(dev, stream, Nk=args.decode_nk)
         out["window"] = window_leg(dev, stream, runner.flush_l2)
         out["headsize"] = headsize_leg(dev, stream, runner.flush_l2)
@@ -803,6 +820,8 @@ def run_only(args):
                         lengths=tuple(int(n) for n in args.sweep_n.split(",")), masks=masks)
     elif leg == "decode":
         res = decode_leg(dev, stream, Nk=args.decode_nk)
+    elif leg == "d256":
+        res = d256_leg(lib, dev, stream, flush, peak, 2070.0, sms)
     elif leg == "window":
         res = window_leg(dev, stream, flush)
     elif leg == "headsize":

@@ -88,7 +88,7 @@ int check_problem(int B, int H, int N, int d, float scale, bool* empty) {
   *empty = false;
   if (B < 0 || H < 0 || N < 0) return FA_ERR_INVALID;
   if (!std::isfinite(scale) || scale < 0.f) return FA_ERR_INVALID;
-  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (d != 64 && d != 128 && d != 256) return FA_ERR_UNSUPPORTED;
   if (B == 0 || H == 0 || N == 0) {
     *empty = true;
     return FA_OK;
@@ -158,7 +158,8 @@ const char* fa_strerror(int code) {
   switch (code) {
     case FA_OK: return "success";
     case FA_ERR_INVALID: return "invalid argument (pointer, size, alignment or scale)";
-    case FA_ERR_UNSUPPORTED: return "unsupported (head size must be 64 or 128; device must be CC 10.3)";
+    case FA_ERR_UNSUPPORTED:
+      return "unsupported (head size 64 or 128, or 256 in the forward; device must be CC 10.3)";
     case FA_ERR_LAUNCH: return "a CUDA call failed (launch, attribute or tensor map)";
     case FA_ERR_TIMEOUT: return "a bounded wait inside a kernel ran out";
     case FA_ERR_WORKSPACE: return "workspace missing or too small";
@@ -199,6 +200,7 @@ int check_bwd(int B, int H, int N, int d, float scale, std::initializer_list<con
               const void* workspace, size_t ws_bytes, bool* empty) {
   int rc = fa::check_problem(B, H, N, d, scale, empty);
   if (rc != FA_OK || *empty) return rc;
+  if (d == 256) return FA_ERR_UNSUPPORTED;  // the backward's accumulators need d <= 128
   for (const void* ptr : ptrs)
     if (!fa::aligned16(ptr)) return FA_ERR_INVALID;
   if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
@@ -333,6 +335,7 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
   bool empty = false;
   int rc = fa::check_problem(B, H, N, d, scale, &empty);
   if (rc != FA_OK || empty) return rc;
+  if (d == 256) return FA_ERR_UNSUPPORTED;
   const void* ptrs[] = {q, k, v, o, lse, dO, dq, dk, dv};
   for (const void* ptr : ptrs)
     if (!fa::aligned16(ptr)) return FA_ERR_INVALID;
@@ -356,7 +359,9 @@ int check_fwd_ex(int B, int H, int Nq, int Nk, int d, int dv, int causal, int wi
   *empty = false;
   if (B < 0 || H < 0 || Nq < 0 || Nk < 0 || window < 0) return FA_ERR_INVALID;
   if (!std::isfinite(scale) || scale < 0.f) return FA_ERR_INVALID;
-  if ((d != 64 && d != 128) || (dv != 64 && dv != 128)) return FA_ERR_UNSUPPORTED;
+  // (d, dv) in {64, 128}^2, or d = dv = 256
+  if (!(d == 256 && dv == 256) && ((d != 64 && d != 128) || (dv != 64 && dv != 128)))
+    return FA_ERR_UNSUPPORTED;
   if (window > 0 && !causal) return FA_ERR_INVALID;
   if (B == 0 || H == 0 || Nq == 0) {
     *empty = true;

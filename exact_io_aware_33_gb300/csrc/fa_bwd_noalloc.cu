@@ -74,6 +74,7 @@ extern "C" int fa_bwd_noalloc(const void* q, const void* k, const void* v, const
   bool empty = false;
   const int chk = fa::check_problem(B, H, N, d, scale, &empty);
   if (chk != FA_OK || empty) return chk;
+  if (d == 256) return FA_ERR_UNSUPPORTED;  // as fa_bwd_stream: the backward takes d <= 128
   const void* ptrs[] = {q, k, v, o, lse, dO, dq, dk, dv};
   for (const void* ptr : ptrs)
     if (!fa::aligned16(ptr)) return FA_ERR_INVALID;

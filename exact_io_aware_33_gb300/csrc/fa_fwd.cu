@@ -18,7 +18,10 @@
 // only a few instructions deep, so that shows directly in the step time.
 // Each CTA owns 256 query rows of one (batch, head): two 128-row tiles that
 // ping-pong, so the tensor core works on one tile's QK^T / PV while the
-// other tile's softmax runs.
+// other tile's softmax runs. The one-tile form (QT = 1; 192 threads) is used
+// at d = d_v = 64, two CTAs per SM, and at d = d_v = 256, where a tile's S
+// (128 columns) and O (256 columns) fill the tensor memory and its Q, K and
+// V tiles (64 KiB each, a single K/V stage) the shared memory.
 //
 // Tensor memory (512 columns x 128 lanes, fp32):
 //   [  0,128)  S of tile 0; its first 64 columns are overwritten by P (bf16
@@ -29,8 +32,8 @@
 //
 // Shared memory: Q tiles (2 x 128 x d bf16), and rings of K and V tiles
 // (stages x 128 x d bf16 each), all in the 128-byte-swizzled layout TMA
-// writes and the tensor core reads; d = 128 is stored as two 64-column
-// halves. The online-softmax statistics never leave registers.
+// writes and the tensor core reads; d = 128 (256) is stored as two (four)
+// 64-column chunks. The online-softmax statistics never leave registers.
 //
 // Exactness note: the reference maximum of a row only moves when a tile's
 // maximum exceeds it by more than 2^8 in the exponent (log2 units); until
@@ -64,15 +67,19 @@ struct FwdCfg {
   static constexpr int kMmaWarp = kSoftmaxThreads / 32;
   static constexpr int kLoadWarp = kMmaWarp + 1;
   static constexpr int kThreads = kSoftmaxThreads + 64;  // + the MMA warp and the TMA warp
-  static constexpr int kCtasPerSm = QT == 1 ? 2 : 1;
+  // two CTAs per SM for the one-tile form at d = d_v = 64; d = d_v = 256
+  // (one tile, 192 KiB of tiles) fills the SM alone
+  static constexpr int kCtasPerSm = (QT == 1 && D + DV <= 128) ? 2 : 1;
   static constexpr int kChunks = D / 64;
   static constexpr int kChunksV = DV / 64;
   static constexpr int kChunkBytes = kBlockM * 64 * 2;        // 16 KiB
   static constexpr int kTileBytes = kChunks * kChunkBytes;    // 128 rows x d (Q, K)
   static constexpr int kVTileBytes = kChunksV * kChunkBytes;  // 128 rows x d_v (V)
-  // K/V ring depth: as many stages as fit next to the Q tiles (QT = 1: two
-  // CTAs per SM)
-  static constexpr int kStages = QT == 1 ? 2 : (D == 64 && DV == 64) ? 4 : (D + DV == 192 ? 3 : 2);
+  // K/V ring depth: as many stages as fit next to the Q tiles (QT = 1 at
+  // d = 64: two CTAs per SM; at d = 256 a 64 KiB Q tile and one 64 KiB K
+  // and V tile each fill the shared memory)
+  static constexpr int kStages =
+      QT == 1 ? (D + DV <= 128 ? 2 : 1) : (D == 64 && DV == 64) ? 4 : (D + DV == 192 ? 3 : 2);
   static constexpr int kQOff = 0;
   static constexpr int kKOff = kQOff + kQTiles * kTileBytes;
   static constexpr int kVOff = kKOff + kStages * kTileBytes;
@@ -92,15 +99,18 @@ struct FwdCfg {
   static constexpr int kNumBars = kBarDrain + 1;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kSmemBytes = kMiscOff + 16 + 1024;  // + slack to align the base
-  static constexpr uint32_t kTmemCols = 256 * QT;
   static constexpr uint32_t kColO = 128 * QT;
   // With d_v = 64 the two S tiles and two O accumulators take 384 columns,
   // so each tile's P gets 64 columns of its own at kColP: the softmax
   // releases S as soon as it has loaded it and the next tile's QK^T
-  // overlaps the exponentials. With d_v = 128 the columns are full and P
-  // overwrites S.
+  // overlaps the exponentials. With d_v = 128 (or 256) the columns are full
+  // and P overwrites S.
   static constexpr bool kSepP = (DV == 64);
   static constexpr uint32_t kColP = kColO + QT * DV;
+  // S, O (and P) of every tile, rounded up to a power of two for the allocation
+  static constexpr uint32_t kColsUsed = kColP + (kSepP ? QT * 64 : 0);
+  static constexpr uint32_t kTmemCols = kColsUsed <= 256 ? 256 : 512;
+  static_assert(kColsUsed <= 512, "forward accumulators exceed tensor memory");
   static_assert(kSmemBytes <= 232448, "forward tiles exceed shared memory");
 };
 
@@ -766,8 +776,9 @@ int launch_fwd_d(const FwdProblem& p, void* o, float* lse, float* part_o, float*
   int* status = device_status_word();
   if (!status) return -3;
   auto kern = fa_fwd_kernel<D, DV, QT, kDrop>;
-  // attribute slots 0, 1, 4, 5, 9 and with dropout 10, 11 (the backward uses 2, 3, 6-8, 12, 13)
-  constexpr int kSlot = kDrop ? (QT == 1 ? 10 : 11) : QT == 1 ? 9 : (D == 64 ? 0 : 1) + (DV == 64 ? 0 : 4);
+  // attribute slots 0, 1, 4, 5, 9, 14 and with dropout 10, 11 (the backward uses 2, 3, 6-8, 12, 13)
+  constexpr int kSlot = kDrop ? (QT == 1 ? 10 : 11)
+                              : D == 256 ? 14 : QT == 1 ? 9 : (D == 64 ? 0 : 1) + (DV == 64 ? 0 : 4);
   if (!ensure_smem_attr(reinterpret_cast<const void*>(kern), C::kSmemBytes, kSlot))
     return -3;
   const int n_kv = (p.Nk + kBlockN - 1) / kBlockN;
@@ -859,6 +870,8 @@ int launch_fwd_general(const FwdProblem& p, void* o, float* lse, float* part_o, 
     return launch_fwd_d<64, 64, 2>(p, o, lse, part_o, part_lse, n_splits, stream);
   }
   if (p.d == 128 && p.dv == 128) return launch_fwd_d<128, 128, 2>(p, o, lse, part_o, part_lse, n_splits, stream);
+  // d = d_v = 256: one query tile per CTA (S 128 + O 256 tensor-memory columns)
+  if (p.d == 256 && p.dv == 256) return launch_fwd_d<256, 256, 1>(p, o, lse, part_o, part_lse, n_splits, stream);
   if (p.d == 128 && p.dv == 64) return launch_fwd_d<128, 64, 2>(p, o, lse, part_o, part_lse, n_splits, stream);
   if (p.d == 64 && p.dv == 128) return launch_fwd_d<64, 128, 2>(p, o, lse, part_o, part_lse, n_splits, stream);
   return -2;

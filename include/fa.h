@@ -24,8 +24,9 @@
  *    library keeps no allocation of its own between calls.
  *  - q, k, v, o, dO, dq, dk, dv: bfloat16, shape [B, H, N, d], contiguous
  *    row-major (d fastest). lse and the backward's D: float32 [B, H, N].
- *  - d must be 64 or 128. N may be any length (ragged tail tiles are
- *    masked). Keys and queries have the same length N, except in
+ *  - d must be 64 or 128; the forward forms (fa_fwd, fa_fwd_ex,
+ *    fa_decode_splitkv) also take d = 256 (with d_v = 256). N may be any
+ *    length (ragged tail tiles are masked). Keys and queries have the same length N, except in
  *    fa_fwd_ex and fa_decode_splitkv, which take Nq queries over Nk keys.
  *  - causal != 0 masks key j for query i when j > i (the diagonal is
  *    visible). scale multiplies Q K^T before masking and softmax; it must be
@@ -57,7 +58,7 @@ extern "C" {
 /* Return codes. */
 #define FA_OK 0
 #define FA_ERR_INVALID -1      /* bad pointer, size, alignment or scale      */
-#define FA_ERR_UNSUPPORTED -2  /* d not in {64,128}, or not a CC 10.3 device */
+#define FA_ERR_UNSUPPORTED -2  /* head size not supported by the call, or not a CC 10.3 device */
 #define FA_ERR_LAUNCH -3       /* a CUDA call failed (launch, attribute, map) */
 #define FA_ERR_TIMEOUT -4      /* a bounded wait in a kernel ran out          */
 #define FA_ERR_WORKSPACE -5    /* workspace missing or too small              */
@@ -93,6 +94,9 @@ int fa_fwd_stream(const void* q, const void* k, const void* v, void* o, float* l
  * Source: "FlashAttention" (Road to Intelligence), sections "The solution"
  * and "What to remember" (scores recomputed from Q, K, V rather than
  * stored); the gradient formulas follow from the forward's definition.
+ * d must be 64 or 128 (d = 256, which the forward takes, returns
+ * FA_ERR_UNSUPPORTED here and in every backward form: its five tensor-memory
+ * accumulators would not fit).
  * This form allocates its float32 workspace (fa_bwd_workspace_bytes) with
  * cudaMallocAsync on stream 0 and frees it stream-ordered after the call.
  */
@@ -170,10 +174,10 @@ size_t fa_bwd_workspace_bytes(int B, int H, int N, int d);
  *   v       : in,  bf16 [B,H,Nk,dv]
  *   o       : out, bf16 [B,H,Nq,dv]
  *   lse     : out, fp32 [B,H,Nq]     natural-log log-sum-exp of each row
- * d and dv are each 64 or 128 (FA_ERR_UNSUPPORTED otherwise); the pages
- * count the forward's work as O(N^2 (d + d_v)) ("Flash Attention: IO-Aware
- * Exact Attention", section "Storage, arithmetic and IO are separate
- * quantities"), with d_v = d as the square special case.
+ * d and dv are each 64 or 128, or both 256 (FA_ERR_UNSUPPORTED otherwise);
+ * the pages count the forward's work as O(N^2 (d + d_v)) ("Flash Attention:
+ * IO-Aware Exact Attention", section "Storage, arithmetic and IO are
+ * separate quantities"), with d_v = d as the square special case.
  * With causal != 0 the queries are the last Nq positions of the Nk keys:
  * query i sits at position p = i + Nk - Nq and sees keys j <= p (Nq <= Nk
  * required). window = W >= 1 (causal only) further keeps only the keys

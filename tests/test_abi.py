@@ -69,7 +69,8 @@ MISALIGNED = ctypes.c_void_p(0x100008)
     ((1, 1, 8, 64, float("inf")), fa.FA_ERR_INVALID),
     ((1, 1, 8, 64, -0.5), fa.FA_ERR_INVALID),
     ((1, 1, 8, 96, 0.125), fa.FA_ERR_UNSUPPORTED),
-    ((1, 1, 8, 256, 0.125), fa.FA_ERR_UNSUPPORTED),
+    ((1, 1, 8, 512, 0.125), fa.FA_ERR_UNSUPPORTED),
+    ((1, 1, 8, 32, 0.125), fa.FA_ERR_UNSUPPORTED),
 ])
 def test_fwd_rejects_bad_sizes(lib, args, code):
     B, H, N, d, scale = args
@@ -95,6 +96,11 @@ def test_bwd_rejects_bad_arguments(lib):
     p, n = ALIGNED, NULL
     assert lib.fa_bwd(p, p, p, p, p, p, p, p, n, 1, 1, 8, 64, 0, 0.125) == fa.FA_ERR_INVALID
     assert lib.fa_bwd(p, p, p, p, p, p, p, p, p, 1, 1, 8, 80, 0, 0.125) == fa.FA_ERR_UNSUPPORTED
+    # d = 256 is a forward-only head size
+    assert lib.fa_bwd(p, p, p, p, p, p, p, p, p, 1, 1, 8, 256, 0, 0.125) == fa.FA_ERR_UNSUPPORTED
+    assert lib.fa_bwd_stream(p, p, p, p, p, p, p, p, p, 1, 1, 8, 256, 0, 0.125, p, 1 << 20,
+                             n) == fa.FA_ERR_UNSUPPORTED
+    assert lib.fa_bwd_noalloc(p, p, p, p, p, p, p, p, p, 1, 1, 8, 256, 0, 0.125, n) == fa.FA_ERR_UNSUPPORTED
     # the stream form wants a workspace of the advertised size, 256-byte aligned
     ws_need = lib.fa_bwd_workspace_bytes(1, 1, 8, 64)
     assert lib.fa_bwd_stream(p, p, p, p, p, p, p, p, p, 1, 1, 8, 64, 0, 0.125, n, ws_need,
