@@ -21,7 +21,7 @@ __device__ int g_status_word;
 namespace {
 
 constexpr int kMaxDevices = 64;
-constexpr int kSmemSlots = 16;
+constexpr int kSmemSlots = 20;
 
 struct DeviceState {
   bool probed = false;
