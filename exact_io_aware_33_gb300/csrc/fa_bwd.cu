@@ -698,8 +698,10 @@ enum : int {
   kBarQEmpty = kBarQFull + kStages,
   kBarSFull = kBarQEmpty + kStages,
   kBarSFree,     // S^T, dP^T are in registers and the next Q/dO have landed
-  kBarPFree,
-  kBarDSFull,    // P^T and dS written; dQ (and at an item start dK, dV) read out
+  kBarPFree,     // the step's dV MMA has read P^T
+  kBarDSFull,    // dS written; dQ (and at an item start dK, dV) read out
+  kBarPFull,     // P^T written
+  kBarDSFree,    // the step's dQ and dK MMAs have read dS
   kBarDQFull,
   kBarDKDV,
   kBarDrain,     // two: one per issuing thread
@@ -763,6 +765,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(kBarSFree), kPdsThreads / 32);  // one arrival per warp
     mbar_init(bar(kBarPFree), 1);
     mbar_init(bar(kBarDSFull), kPdsThreads / 32 + 4);  // one arrival per warp
+    mbar_init(bar(kBarPFull), kPdsThreads / 32);
+    mbar_init(bar(kBarDSFree), 1);
     mbar_init(bar(kBarDQFull), 1);
     mbar_init(bar(kBarDKDV), 1);
     mbar_init(bar(kBarDrain), 1);
@@ -863,15 +867,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int kk = 0; kk < kBlk / 16; ++kk)
             mma_ss(tmem + kColDQ, dsmn + 128 * kk, kKmn + 128 * kk, kIdQ, kk > 0 ? 1u : 0u);
           mma_commit(bar(kBarDQFull));
-          // dV += P^T dO   (A = P^T bf16 pairs in TMEM, B = dO MN-major, 16 rows per step)
-#pragma unroll
-          for (int kk = 0; kk < kBlk / 16; ++kk)
-            mma_ts(tmem + kColDV, tmem + kColP + kk * 8, omn + 128 * kk, kIdKV, (it > 0 || kk > 0) ? 1u : 0u);
           // dK += dS^T Q   (A = dS^T K-major, query halves in two 16 KiB regions; B = Q MN-major)
 #pragma unroll
           for (int kk = 0; kk < kBlk / 16; ++kk)
             mma_ss(tmem + kColDK, dsk + (kk >> 2) * kTileStep + (kk & 3) * 2, qmn + 128 * kk, kIdKV,
                    (it > 0 || kk > 0) ? 1u : 0u);
+          // the dS buffer is free once dQ and dK have read it: the P/dS warps
+          // write the next step's dS while dV runs
+          mma_commit(bar(kBarDSFree));
+          // dV += P^T dO   (A = P^T bf16 pairs in TMEM, B = dO MN-major, 16 rows per step)
+          ok = mbar_wait(bar(kBarPFull), g & 1, abort_flag);
+          if (!ok) break;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < kBlk / 16; ++kk)
+            mma_ts(tmem + kColDV, tmem + kColP + kk * 8, omn + 128 * kk, kIdKV, (it > 0 || kk > 0) ? 1u : 0u);
           mma_commit(bar(kBarPFree));
           mma_commit(bar(kBarQEmpty + g % kStages));
         }
@@ -1050,18 +1060,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         half(std::integral_constant<int, 0>{}, s1, d1, 1);
       }
 
-      // P^T into its own columns once the previous step's dV MMA has read them
-      if (g > 0) {
-        ok = mbar_wait(bar(kBarPFree), (g - 1) & 1, abort_flag);
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok) break;
-        tc_fence_after();
-      }
-      tmem_st32(tP, pp);
       // dS^T row of this key into the dS buffer once step g-1's dQ and dK
-      // MMAs have read it: 64 queries -> eight swizzled 16-byte chunks
-      if (g >= 1) {
-        ok = mbar_wait(bar(kBarDQFull), (g - 1) & 1, abort_flag);  // dK read it before PFree (above)
+      // MMAs have read it (step g-1's dV may still run): 64 queries -> eight
+      // swizzled 16-byte chunks
+      if (g > 0) {
+        ok = mbar_wait(bar(kBarDSFree), (g - 1) & 1, abort_flag);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
       }
@@ -1070,10 +1073,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int v = 0; v < 8; ++v)
         *reinterpret_cast<uint4*>(ds_row + ((v ^ key_sw) * 16)) =
             make_uint4(dd[4 * v], dd[4 * v + 1], dd[4 * v + 2], dd[4 * v + 3]);
-      tmem_st_wait();
-      tc_fence_before();
       fence_async_smem();
       mbar_arrive_warp(bar(kBarDSFull));
+      // P^T into its own columns once the previous step's dV MMA has read them
+      if (g > 0) {
+        ok = mbar_wait(bar(kBarPFree), (g - 1) & 1, abort_flag);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc_fence_after();
+      }
+      tmem_st32(tP, pp);
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive_warp(bar(kBarPFull));
     }
     }
   } else if (warp < kMmaWarp) {
