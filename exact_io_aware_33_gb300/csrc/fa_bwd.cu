@@ -697,7 +697,7 @@ enum : int {
   kBarQFull = kBarKVFree + 2,
   kBarQEmpty = kBarQFull + kStages,
   kBarSFull = kBarQEmpty + kStages,
-  kBarSFree,     // S^T, dP^T are in registers and the next Q/dO have landed
+  kBarSFree,     // S^T, dP^T are in registers
   kBarPFree,     // the step's dV MMA has read P^T
   kBarDSFull,    // dS written; dQ (and at an item start dK, dV) read out
   kBarPFull,     // P^T written
@@ -932,6 +932,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = mbar_wait(bar(kBarSFree), g & 1, abort_flag);
           if (!ok) break;
           if (it + 1 < ns) {
+            // the next step's Q and dO: waited for here rather than by the P/dS
+            // warps, whose step must not wait on a load it does not read
+            ok = mbar_wait(bar(kBarQFull + (g + 1) % kStages), ((g + 1) / kStages) & 1, abort_flag);
+            if (!ok) break;
             tc_fence_after();
             issue_sdp(g + 1, kK, kV);
           }
@@ -980,14 +984,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int q = 0; q < 4; ++q) kball[4 * ch + q] = kb[q];
         }
       }
-      // the stage's vectors arrive with its Q/dO tiles; S^T, dP^T with the MMA
-      // commit. The next step's Q and dO are checked here too, so that the
-      // release of S^T below also tells the MMA thread they have landed and
-      // it has one wait less.
-      ok = mbar_wait(bar(kBarQFull + s), (g / kStages) & 1, abort_flag);
-      if (ok && it + 1 < ns)
-        ok = mbar_wait(bar(kBarQFull + (g + 1) % kStages), ((g + 1) / kStages) & 1, abort_flag);
-      if (ok) ok = mbar_wait(bar(kBarSFull), g & 1, abort_flag);
+      // S^T, dP^T arrive with the MMA commit; the stage's vectors with its
+      // Q/dO tiles (which S^T, dP^T needed, so that wait is already satisfied
+      // and only makes the vectors visible here)
+      ok = mbar_wait(bar(kBarSFull), g & 1, abort_flag);
+      if (ok) ok = mbar_wait(bar(kBarQFull + s), (g / kStages) & 1, abort_flag);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
