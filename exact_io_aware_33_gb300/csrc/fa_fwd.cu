@@ -994,25 +994,23 @@ __global__ void __launch_bounds__(kThreads, 2)
       while (have && ok) {
         Item nxt;
         const bool have_next = next_item(&nxt);
+        // S(u + 1) once the softmax holds S(u) in registers; qb: its Q buffer
+        auto next_s = [&](int u, int qb, bool new_item) {
+          ok = mbar_wait(bar(kBarSFree), u & 1, abort_flag);
+          if (ok && new_item) ok = mbar_wait(bar(kBarQFull + qb), ((q + 1) >> 1) & 1, abort_flag);
+          if (ok) ok = mbar_wait(bar(kBarKFull + (u + 1) % kStages), ((u + 1) / kStages) & 1, abort_flag);
+          if (!ok) return;
+          tc_fence_after();
+          issue_s(qb, u + 1);
+          mma_commit(bar(kBarKEmpty + (u + 1) % kStages));
+        };
         for (int jj = 0; jj < cur.n && ok; ++jj) {
           const int u = u0 + jj;
-          // the next S (this tile's successor, or the next item's first tile) as
-          // soon as the softmax holds S(u) in registers
-          if (jj + 1 < cur.n || have_next) {
-            ok = mbar_wait(bar(kBarSFree), u & 1, abort_flag);
-            if (!ok) break;
-            int qb = q & 1;
-            if (jj + 1 == cur.n) {  // next item: its Q has landed in the other buffer
-              qb = (q + 1) & 1;
-              ok = mbar_wait(bar(kBarQFull + qb), ((q + 1) >> 1) & 1, abort_flag);
-              if (!ok) break;
-            }
-            ok = mbar_wait(bar(kBarKFull + (u + 1) % kStages), ((u + 1) / kStages) & 1, abort_flag);
-            if (!ok) break;
-            tc_fence_after();
-            issue_s(qb, u + 1);
-            mma_commit(bar(kBarKEmpty + (u + 1) % kStages));
-          }
+          const bool last = jj + 1 == cur.n;
+          // within an item: the next tile's S first, so that it computes while
+          // the softmax forms P(u)
+          if (!last) next_s(u, q & 1, false);
+          if (!ok) break;
           ok = mbar_wait(bar(kBarVFull + u % kStages), (u / kStages) & 1, abort_flag);
           if (!ok) break;
           ok = mbar_wait(bar(kBarPFull), u & 1, abort_flag);
@@ -1021,6 +1019,10 @@ __global__ void __launch_bounds__(kThreads, 2)
           issue_pv(u, jj == 0);
           mma_commit(bar(kBarPVDone));
           mma_commit(bar(kBarVEmpty + u % kStages));
+          // the item's last tile: its P.V goes first, so the write-back is not held
+          // up by the next item's Q and K loads; the next item's first S then
+          // computes during the write-back
+          if (last && have_next) next_s(u, (q + 1) & 1, true);
         }
         u0 += cur.n;
         ++q;
