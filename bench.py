@@ -657,27 +657,58 @@ def traffic_from_profiles(kernel):
     return None
 
 
-def cpu_baseline(w, budget_s=12.0):
-    """The float64 oracle on a bounded sample of the workload's heads."""
+def cpu_model():
+    """The host CPU's model name from /proc/cpuinfo (x86: "model name"; Arm:
+    implementer and part numbers), else the platform's machine name."""
+    import platform
+    fields = {}
+    try:
+        for line in open("/proc/cpuinfo"):
+            if ":" in line:
+                k, v = line.split(":", 1)
+                fields.setdefault(k.strip().lower(), v.strip())
+    except OSError:
+        pass
+    if "model name" in fields:
+        return fields["model name"]
+    if "cpu part" in fields:
+        return f"{platform.machine()} implementer {fields.get('cpu implementer', '?')} part {fields['cpu part']}"
+    return platform.processor() or platform.machine()
+
+
+def cpu_baseline(w, budget_s=12.0, per_config_s=2.0):
+    """The float64 oracle on a bounded sample of the workload's heads, and a
+    shorter bounded sample of every named workload."""
     import numpy as np  # noqa: F401
     from oracle import dense
-    x = si.make_inputs(w)
-    heads = [(b, h) for b in range(w.B) for h in range(w.H)]
-    done, t0 = 0, time.perf_counter()
-    for b, h in heads:
-        o, lse = dense.forward_head(x["q"][b, h], x["k"][b, h], x["v"][b, h], w.causal, w.scale)
-        if w.backward:
-            dense.backward_head(x["q"][b, h], x["k"][b, h], x["v"][b, h], o, lse, x["do"][b, h],
-                                w.causal, w.scale)
-        done += 1
-        if time.perf_counter() - t0 > budget_s and done >= 2:
-            break
-    dt = time.perf_counter() - t0
-    f_fwd, f_bwd = step_flops(w)
-    flops = (f_fwd + f_bwd) * done / w.heads
-    return {"value": flops / dt / 1e12, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
+
+    def run(wl, budget):
+        x = si.make_inputs(wl)
+        heads = [(b, h) for b in range(wl.B) for h in range(wl.H)]
+        done, t0 = 0, time.perf_counter()
+        for b, h in heads:
+            o, lse = dense.forward_head(x["q"][b, h], x["k"][b, h], x["v"][b, h], wl.causal, wl.scale)
+            if wl.backward:
+                dense.backward_head(x["q"][b, h], x["k"][b, h], x["v"][b, h], o, lse, x["do"][b, h],
+                                    wl.causal, wl.scale)
+            done += 1
+            if time.perf_counter() - t0 > budget and done >= 1:
+                break
+        dt = time.perf_counter() - t0
+        f_fwd, f_bwd = step_flops(wl)
+        return (f_fwd + f_bwd) * done / wl.heads / dt / 1e12, done, dt
+
+    value, done, dt = run(w, budget_s)
+    per_config = []
+    for wl in si.WORKLOADS:
+        v, n, t = run(wl, per_config_s)
+        per_config.append({"workload": wl.name, "pass": "forward+backward" if wl.backward else "forward",
+                           "tflops": v, "heads": f"{n} of {wl.heads}", "s": round(t, 2)})
+    return {"value": value, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
             "sample": f"{done} of {w.heads} heads of {w.name} (dense float64 numpy "
-                      f"{'forward+backward' if w.backward else 'forward'}), {dt:.1f} s"}
+                      f"{'forward+backward' if w.backward else 'forward'}), {dt:.1f} s",
+            "os_cpu_count": os.cpu_count(), "blas_threads": blas_threads(), "cpu_model": cpu_model(),
+            "per_config": per_config}
 
 
 def blas_threads():
