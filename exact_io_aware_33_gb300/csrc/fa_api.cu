@@ -100,14 +100,14 @@ int check_problem(int B, int H, int N, int d, float scale, bool* empty) {
   return FA_OK;
 }
 
-bool make_map_bhnd(CUtensorMap* map, const void* ptr, int BH, int N, int d) {
+bool make_map_bhnd(CUtensorMap* map, const void* ptr, int BH, int N, int d, int box_rows) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
                               static_cast<cuuint64_t>(BH)};
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
                                  static_cast<cuuint64_t>(N) * static_cast<cuuint64_t>(d) * 2};
-  const cuuint32_t box[3] = {64, 128, 1};
+  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   const CUresult r =
       enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box,

@@ -851,7 +851,8 @@ __device__ __forceinline__ bool item_of(int k, int num_items, int* x) {
 template <bool kDrop>
 __global__ void __launch_bounds__(kThreads, 2)
     fa_fwd_persist(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                   const __grid_constant__ CUtensorMap tmV, const FwdArgs args) {
+                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                   const FwdArgs args) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_u32 = smem_u32(smem_raw);
   const uint32_t base = (raw_u32 + 1023u) & ~1023u;
@@ -903,6 +904,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       tma_prefetch_map(&tmQ);
       tma_prefetch_map(&tmK);
       tma_prefetch_map(&tmV);
+      const uint64_t once = policy_evict_first();  // a Q tile is read by one item only
       bool ok = true;
       int q = 0, u = 0;
       for (int k = 0; ok; ++k) {
@@ -915,7 +917,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (q >= 2) ok = mbar_wait(bar(kBarQFree + b), ((q >> 1) - 1) & 1, abort_flag);
         if (!ok) break;
         mbar_arrive_expect_tx(bar(kBarQFull + b), kTileBytes);
-        tma_load_3d(base + kQOff + b * kTileBytes, &tmQ, bar(kBarQFull + b), 0, it.row0, it.bh);
+        tma_load_3d_hint(base + kQOff + b * kTileBytes, &tmQ, bar(kBarQFull + b), 0, it.row0, it.bh, once);
         q_loaded = ++q;
         for (int jj = 0; jj < it.n && ok; ++jj) {
           const int st = u % kStages;
@@ -1185,9 +1187,11 @@ __global__ void __launch_bounds__(kThreads, 2)
       const float lse_row = l > 0.f ? (m_use + log2f(l)) * kLn2 : -INFINITY;
       const float2 il2 = make_float2(inv_l, inv_l);
       // each warp swizzles its 32 rows into 4 KiB of this item's Q buffer (every
-      // QK^T of the item has completed) and writes four whole lines per store
-      __nv_bfloat16* obase = args.o + static_cast<size_t>(bh) * Nq * 64;
-      uint8_t* stage_blk = base_ptr + kQOff + b * kTileBytes + (warp & 3) * 4096;
+      // QK^T of the item has completed), in the layout of the O map's 128-byte
+      // swizzle, and one lane stores them with a TMA bulk store (rows past Nq
+      // are not written), so the warp does not wait on 32 global stores
+      const int wblk = (warp & 3) * 4096;
+      uint8_t* stage_blk = base_ptr + kQOff + b * kTileBytes + wblk;
       uint8_t* stage_row = stage_blk + lane * 128;
       const int row0 = row - lane;  // first row of this warp
 #pragma unroll
@@ -1206,20 +1210,23 @@ __global__ void __launch_bounds__(kThreads, 2)
           *reinterpret_cast<uint4*>(stage_row + (((4 * c + e) ^ (lane & 7)) * 16)) =
               make_uint4(pko[4 * e], pko[4 * e + 1], pko[4 * e + 2], pko[4 * e + 3]);
       }
+      fence_async_smem();  // the staged rows are visible to the bulk store
       __syncwarp();
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int r = 4 * j + (lane >> 3), v = lane & 7;
-        const uint4 val = *reinterpret_cast<const uint4*>(stage_blk + r * 128 + ((v ^ (r & 7)) * 16));
-        if (row0 + r < Nq)
-          *reinterpret_cast<uint4*>(obase + static_cast<size_t>(row0 + r) * 64 + v * 8) = val;
+      if (lane == 0) {
+        tma_store_3d(&tmO, base + kQOff + b * kTileBytes + wblk, 0, row0, bh);
+        bulk_commit_group();
       }
       if (live) args.lse[static_cast<size_t>(bh) * Nq + row] = lse_row;
-      // the staging reads are done: the producer may load the item after next into buffer b
-      fence_async_smem();
+      // once the store has read the staging block, the producer may load the
+      // item after next into buffer b
+      if (lane == 0) bulk_wait_read<0>();
+      __syncwarp();
       mbar_arrive_warp(bar(kBarQFree + b));
       ++q;
     }
+    // the write-backs' global writes complete before the CTA exits
+    if (lane == 0) bulk_wait<0>();
+    __syncwarp();
   }
 
   tc_fence_before();
@@ -1250,9 +1257,9 @@ __global__ void __launch_bounds__(kThreads, 2)
 template <bool kDrop>
 int launch_fwd_persist(const FwdProblem& p, void* o, float* lse, cudaStream_t stream) {
   const int BH = p.B * p.H;
-  CUtensorMap mq, mk, mv;
+  CUtensorMap mq, mk, mv, mo;
   if (!make_map_bhnd(&mq, p.q, BH, p.Nq, 64) || !make_map_bhnd(&mk, p.k, BH, p.Nk, 64) ||
-      !make_map_bhnd(&mv, p.v, BH, p.Nk, 64))
+      !make_map_bhnd(&mv, p.v, BH, p.Nk, 64) || !make_map_bhnd(&mo, o, BH, p.Nq, 64, 32))
     return -3;
   int* status = device_status_word();
   const int sms = device_sm_count();
@@ -1279,7 +1286,7 @@ int launch_fwd_persist(const FwdProblem& p, void* o, float* lse, cudaStream_t st
   const long long items = static_cast<long long>(a.num_pairs) * BH;
   if (items > 0x7fffffffLL) return -1;
   const long long grid = items < 2LL * sms ? items : 2LL * sms;
-  kern<<<static_cast<unsigned>(grid), pf::kThreads, pf::kSmemBytes, stream>>>(mq, mk, mv, a);
+  kern<<<static_cast<unsigned>(grid), pf::kThreads, pf::kSmemBytes, stream>>>(mq, mk, mv, mo, a);
   return cudaGetLastError() == cudaSuccess ? 0 : -3;
 }
 

@@ -46,8 +46,8 @@ struct FwdProblem {
 };
 
 // Encodes a 3-D tiled TMA map over a bf16 [BH, N, d] tensor with boxes of
-// 128 rows x 64 columns and 128-byte swizzle. Returns false on failure.
-bool make_map_bhnd(CUtensorMap* map, const void* ptr, int BH, int N, int d);
+// box_rows rows x 64 columns and 128-byte swizzle. Returns false on failure.
+bool make_map_bhnd(CUtensorMap* map, const void* ptr, int BH, int N, int d, int box_rows = 128);
 
 // Size and scale checks shared by the entry points taking (B, H, N, d):
 // FA_OK or an error code; *empty is set when there is nothing to compute.
