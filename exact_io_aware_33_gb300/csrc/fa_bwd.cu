@@ -835,7 +835,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issue
-    if (lane == 0) {
+    // the whole warp runs the issue loop (one elected lane issues)
+    {
       constexpr uint32_t kIdKV = idesc_bf16_f32(kBlk, kD, false, true);     // dV, dK
       constexpr uint32_t kIdQ = idesc_bf16_f32(kBlk, kD, true, true);       // dQ
       // Shared-memory descriptors, built once (K and V: once per item).
@@ -860,7 +861,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int it = 0; it < ns && ok; ++it, ++g) {
           // P^T and dS of step g written, dQ of step g-1 (and at an item's
           // first step the previous item's dK, dV) read out of tensor memory
-          ok = mbar_wait(bar(kBarDSFull), g & 1, abort_flag);
+          ok = mbar_wait_w(bar(kBarDSFull), g & 1, abort_flag);
           if (!ok) break;
           tc_fence_after();
           const uint64_t qmn = kQmn0 + (g % kStages) * kStageStep, omn = qmn + kTileStep;
@@ -869,38 +870,39 @@ __global__ void __launch_bounds__(kThreads, 1)
           // (A = dS MN-major: the same bytes as dS^T, B = K MN-major)
 #pragma unroll
           for (int kk = 0; kk < kBlk / 16; ++kk)
-            mma_ss(tmem + kColDQ, dsmn + 128 * kk, kKmn + 128 * kk, kIdQ, kk > 0 ? 1u : 0u);
-          mma_commit(bar(kBarDQFull));
+            mma_ss_w(tmem + kColDQ, dsmn + 128 * kk, kKmn + 128 * kk, kIdQ, kk > 0 ? 1u : 0u);
+          mma_commit_w(bar(kBarDQFull));
           // dK += dS^T Q   (A = dS^T K-major, query halves in two 16 KiB regions; B = Q MN-major)
 #pragma unroll
           for (int kk = 0; kk < kBlk / 16; ++kk)
-            mma_ss(tmem + kColDK, dsk + (kk >> 2) * kTileStep + (kk & 3) * 2, qmn + 128 * kk, kIdKV,
+            mma_ss_w(tmem + kColDK, dsk + (kk >> 2) * kTileStep + (kk & 3) * 2, qmn + 128 * kk, kIdKV,
                    (it > 0 || kk > 0) ? 1u : 0u);
           // the dS buffer is free once dQ and dK have read it: the P/dS warps
           // write the next step's dS while dV runs
-          mma_commit(bar(kBarDSFree));
+          mma_commit_w(bar(kBarDSFree));
           // dV += P^T dO   (A = P^T bf16 pairs in TMEM, B = dO MN-major, 16 rows per step)
-          ok = mbar_wait(bar(kBarPFull), g & 1, abort_flag);
+          ok = mbar_wait_w(bar(kBarPFull), g & 1, abort_flag);
           if (!ok) break;
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < kBlk / 16; ++kk)
-            mma_ts(tmem + kColDV, tmem + kColP + kk * 8, omn + 128 * kk, kIdKV, (it > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(bar(kBarPFree));
-          mma_commit(bar(kBarQEmpty + g % kStages));
+            mma_ts_w(tmem + kColDV, tmem + kColP + kk * 8, omn + 128 * kk, kIdKV, (it > 0 || kk > 0) ? 1u : 0u);
+          mma_commit_w(bar(kBarPFree));
+          mma_commit_w(bar(kBarQEmpty + g % kStages));
         }
         if (!ok) break;
-        mma_commit(bar(kBarDKDV));    // dK, dV of this item are complete
+        mma_commit_w(bar(kBarDKDV));    // dK, dV of this item are complete
         // and this K/V buffer may be refilled (the item's S^T/dP^T MMAs on
         // the other issuer completed before its last P and dS were formed)
-        mma_commit(bar(kBarKVFree + kv));
+        mma_commit_w(bar(kBarKVFree + kv));
       }
-      mma_commit(bar(kBarDrain));
-      mbar_wait(bar(kBarDrain), 0, nullptr);
+      mma_commit_w(bar(kBarDrain));
+      mbar_wait_w(bar(kBarDrain), 0, nullptr);
     }
   } else if (warp == kSWarp) {
     // ------------------------------------------------------------ S^T / dP^T issue
-    if (lane == 0) {
+    // the whole warp runs the issue loop (one elected lane issues)
+    {
       constexpr uint32_t kIdS = idesc_bf16_f32(kBlk, kBlk, false, false);
       const uint64_t kQ0 = sdesc_sw128(base + kStageOff, 16, 1024);  // stage 0 Q, K-major
       constexpr uint64_t kStageStep = kStageBytes >> 4, kTileStep = kTileBytes >> 4;
@@ -909,11 +911,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t q = kQ0 + (g % kStages) * kStageStep, o = q + kTileStep;
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk)
-          mma_ss(tmem + kColS, kK + 2 * kk, q + 2 * kk, kIdS, kk > 0 ? 1u : 0u);
+          mma_ss_w(tmem + kColS, kK + 2 * kk, q + 2 * kk, kIdS, kk > 0 ? 1u : 0u);
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk)
-          mma_ss(tmem + kColDP, kV + 2 * kk, o + 2 * kk, kIdS, kk > 0 ? 1u : 0u);
-        mma_commit(bar(kBarSFull));
+          mma_ss_w(tmem + kColDP, kV + 2 * kk, o + 2 * kk, kIdS, kk > 0 ? 1u : 0u);
+        mma_commit_w(bar(kBarSFull));
       };
       bool ok = true;
       int g = 0;
@@ -925,29 +927,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t kvb = base + kv * kKVBytes;
         const uint64_t kK = sdesc_sw128(kvb + kKOff, 16, 1024);
         const uint64_t kV = sdesc_sw128(kvb + kVOff, 16, 1024);
-        ok = mbar_wait(bar(kBarKV + kv), (n >> 1) & 1, abort_flag);
-        if (ok) ok = mbar_wait(bar(kBarQFull + g % kStages), (g / kStages) & 1, abort_flag);
+        ok = mbar_wait_w(bar(kBarKV + kv), (n >> 1) & 1, abort_flag);
+        if (ok) ok = mbar_wait_w(bar(kBarQFull + g % kStages), (g / kStages) & 1, abort_flag);
         if (!ok) break;
         tc_fence_after();
         issue_sdp(g, kK, kV);
         // S^T of every step is released before the next S^T is issued (the
         // next item's first one included)
         for (int it = 0; it < ns && ok; ++it, ++g) {
-          ok = mbar_wait(bar(kBarSFree), g & 1, abort_flag);
+          ok = mbar_wait_w(bar(kBarSFree), g & 1, abort_flag);
           if (!ok) break;
           if (it + 1 < ns) {
             // the next step's Q and dO: waited for here rather than by the P/dS
             // warps, whose step must not wait on a load it does not read
-            ok = mbar_wait(bar(kBarQFull + (g + 1) % kStages), ((g + 1) / kStages) & 1, abort_flag);
+            ok = mbar_wait_w(bar(kBarQFull + (g + 1) % kStages), ((g + 1) / kStages) & 1, abort_flag);
             if (!ok) break;
             tc_fence_after();
             issue_sdp(g + 1, kK, kV);
           }
         }
       }
-      // Let every MMA this thread issued finish before TMEM is released.
-      mma_commit(bar(kBarDrain + 1));
-      mbar_wait(bar(kBarDrain + 1), 0, nullptr);
+      // Let every MMA this warp issued finish before TMEM is released.
+      mma_commit_w(bar(kBarDrain + 1));
+      mbar_wait_w(bar(kBarDrain + 1), 0, nullptr);
     }
   } else if (warp < kDqWarp0) {
     // ------------------------------------------------------------ P and dS

@@ -948,7 +948,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issue
-    if (lane == 0) {
+    // the whole warp runs the issue loop (one elected lane issues)
+    {
       constexpr uint32_t kIdS = idesc_bf16_f32(kBlockM, kBlockN, false, false);
       constexpr uint32_t kIdO = idesc_bf16_f32(kBlockM, 64, false, true);
       // descriptors built once, advanced by byte offsets / 16
@@ -960,15 +961,15 @@ __global__ void __launch_bounds__(kThreads, 2)
         const uint64_t qd = dQ0 + static_cast<uint64_t>((b * kTileBytes) >> 4);
         const uint64_t kd = dK0 + static_cast<uint64_t>(((u % kStages) * kTileBytes) >> 4);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) mma_ss(tmem + kColS, qd + 2 * kk, kd + 2 * kk, kIdS, kk > 0 ? 1u : 0u);
-        mma_commit(bar(kBarSFull));
+        for (int kk = 0; kk < 4; ++kk) mma_ss_w(tmem + kColS, qd + 2 * kk, kd + 2 * kk, kIdS, kk > 0 ? 1u : 0u);
+        mma_commit_w(bar(kBarSFull));
       };
       // O (+)= P V for stream step u, P from its TMEM columns
       auto issue_pv = [&](int u, bool first) {
         const uint64_t vd = dV0 + static_cast<uint64_t>(((u % kStages) * kTileBytes) >> 4);
 #pragma unroll
         for (int kk = 0; kk < kBlockN / 16; ++kk)
-          mma_ts(tmem + kColO, tmem + kColP + kk * 8, vd + 128 * kk, kIdO, (!first || kk > 0) ? 1u : 0u);
+          mma_ts_w(tmem + kColO, tmem + kColP + kk * 8, vd + 128 * kk, kIdO, (!first || kk > 0) ? 1u : 0u);
       };
       int k_next = 0;
       auto next_item = [&](Item* it) -> bool {  // this CTA's next item with work
@@ -985,12 +986,12 @@ __global__ void __launch_bounds__(kThreads, 2)
       bool have = next_item(&cur);
       int q = 0, u0 = 0;  // q: ordinal of cur among items with work; u0: stream step of its first tile
       if (have) {
-        ok = mbar_wait(bar(kBarQFull + 0), 0, abort_flag);
-        if (ok) ok = mbar_wait(bar(kBarKFull + 0), 0, abort_flag);
+        ok = mbar_wait_w(bar(kBarQFull + 0), 0, abort_flag);
+        if (ok) ok = mbar_wait_w(bar(kBarKFull + 0), 0, abort_flag);
         tc_fence_after();
         if (ok) {
           issue_s(0, 0);
-          mma_commit(bar(kBarKEmpty + 0));
+          mma_commit_w(bar(kBarKEmpty + 0));
         }
       }
       while (have && ok) {
@@ -998,13 +999,13 @@ __global__ void __launch_bounds__(kThreads, 2)
         const bool have_next = next_item(&nxt);
         // S(u + 1) once the softmax holds S(u) in registers; qb: its Q buffer
         auto next_s = [&](int u, int qb, bool new_item) {
-          ok = mbar_wait(bar(kBarSFree), u & 1, abort_flag);
-          if (ok && new_item) ok = mbar_wait(bar(kBarQFull + qb), ((q + 1) >> 1) & 1, abort_flag);
-          if (ok) ok = mbar_wait(bar(kBarKFull + (u + 1) % kStages), ((u + 1) / kStages) & 1, abort_flag);
+          ok = mbar_wait_w(bar(kBarSFree), u & 1, abort_flag);
+          if (ok && new_item) ok = mbar_wait_w(bar(kBarQFull + qb), ((q + 1) >> 1) & 1, abort_flag);
+          if (ok) ok = mbar_wait_w(bar(kBarKFull + (u + 1) % kStages), ((u + 1) / kStages) & 1, abort_flag);
           if (!ok) return;
           tc_fence_after();
           issue_s(qb, u + 1);
-          mma_commit(bar(kBarKEmpty + (u + 1) % kStages));
+          mma_commit_w(bar(kBarKEmpty + (u + 1) % kStages));
         };
         for (int jj = 0; jj < cur.n && ok; ++jj) {
           const int u = u0 + jj;
@@ -1013,14 +1014,14 @@ __global__ void __launch_bounds__(kThreads, 2)
           // the softmax forms P(u)
           if (!last) next_s(u, q & 1, false);
           if (!ok) break;
-          ok = mbar_wait(bar(kBarVFull + u % kStages), (u / kStages) & 1, abort_flag);
+          ok = mbar_wait_w(bar(kBarVFull + u % kStages), (u / kStages) & 1, abort_flag);
           if (!ok) break;
-          ok = mbar_wait(bar(kBarPFull), u & 1, abort_flag);
+          ok = mbar_wait_w(bar(kBarPFull), u & 1, abort_flag);
           if (!ok) break;
           tc_fence_after();
           issue_pv(u, jj == 0);
-          mma_commit(bar(kBarPVDone));
-          mma_commit(bar(kBarVEmpty + u % kStages));
+          mma_commit_w(bar(kBarPVDone));
+          mma_commit_w(bar(kBarVEmpty + u % kStages));
           // the item's last tile: its P.V goes first, so the write-back is not held
           // up by the next item's Q and K loads; the next item's first S then
           // computes during the write-back
@@ -1031,9 +1032,9 @@ __global__ void __launch_bounds__(kThreads, 2)
         cur = nxt;
         have = have_next;
       }
-      // Let every MMA this thread issued finish before TMEM is released.
-      mma_commit(bar(kBarDrain));
-      mbar_wait(bar(kBarDrain), 0, nullptr);
+      // Let every MMA this warp issued finish before TMEM is released.
+      mma_commit_w(bar(kBarDrain));
+      mbar_wait_w(bar(kBarDrain), 0, nullptr);
     }
   } else {
     // ------------------------------------------------------------ softmax
