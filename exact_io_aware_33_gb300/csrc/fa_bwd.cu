@@ -344,17 +344,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issue
-    if (lane == 0) {
+    // the whole warp runs the issue loop (one elected lane issues)
+    {
       constexpr uint32_t kIdT = idesc_bf16_f32(kBlk, kHalf, false, false); // S^T, dP^T halves
       constexpr uint32_t kIdV = idesc_bf16_f32(kBlk, DV, false, true);     // dV
       constexpr uint32_t kIdK = idesc_bf16_f32(kBlk, D, false, true);      // dK
       constexpr uint32_t kIdQ = idesc_bf16_f32(kBlk, D, true, true);       // dQ
       const uint32_t kb = base + C::kKOff, vb = base + C::kVOff, dsb = base + C::kDSOff;
-      bool ok = mbar_wait_sleep(bar(C::kBarKV), 0, abort_flag);
+      bool ok = mbar_wait_sleep_w(bar(C::kBarKV), 0, abort_flag);
       tc_fence_after();
       for (int it = 0; it < n_steps && ok; ++it) {
         const int s = it % C::kStages;
-        ok = mbar_wait_sleep(bar(C::kBarQFull + s), (it / C::kStages) & 1, abort_flag);
+        ok = mbar_wait_sleep_w(bar(C::kBarQFull + s), (it / C::kStages) & 1, abort_flag);
         if (!ok) break;
         tc_fence_after();
         const uint32_t qb = base + C::kStageOff + s * C::kStageBytes;
@@ -366,62 +367,62 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {  // S^T_h = K Q_h^T
             const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
-            mma_ss(tmem + C::kColS + kHalf * h, sdesc_sw128(kb + off, 16, 1024),
+            mma_ss_w(tmem + C::kColS + kHalf * h, sdesc_sw128(kb + off, 16, 1024),
                    sdesc_sw128(qb + off + h * 8192, 16, 1024), kIdT, kk > 0 ? 1u : 0u);
           }
           if (C::kDqAliasDp && h == 0 && it > 0) {  // dQ of the last step shares dP's columns
-            ok = mbar_wait_sleep(bar(C::kBarDQEmpty), (it - 1) & 1, abort_flag);
+            ok = mbar_wait_sleep_w(bar(C::kBarDQEmpty), (it - 1) & 1, abort_flag);
             if (!ok) break;
             tc_fence_after();
           }
 #pragma unroll
           for (int kk = 0; kk < DV / 16; ++kk) {  // dP^T_h = V dO_h^T
             const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
-            mma_ss(tmem + C::kColDP + kHalf * h, sdesc_sw128(vb + off, 16, 1024),
+            mma_ss_w(tmem + C::kColDP + kHalf * h, sdesc_sw128(vb + off, 16, 1024),
                    sdesc_sw128(dob + off + h * 8192, 16, 1024), kIdT, kk > 0 ? 1u : 0u);
           }
-          mma_commit(bar(C::kBarSFull + h));
+          mma_commit_w(bar(C::kBarSFull + h));
         }
         if (!ok) break;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          ok = mbar_wait_sleep(bar(C::kBarDSFull + h), it & 1, abort_flag);
+          ok = mbar_wait_sleep_w(bar(C::kBarDSFull + h), it & 1, abort_flag);
           if (!ok) break;
           tc_fence_after();
           if (h == 1) {
             // dQ as soon as both dS halves are written: its read-out gates the
             // next step (dQ shares the dP^T columns at d = 128)
             if (!C::kDqAliasDp && it > 0) {
-              ok = mbar_wait_sleep(bar(C::kBarDQEmpty), (it - 1) & 1, abort_flag);
+              ok = mbar_wait_sleep_w(bar(C::kBarDQEmpty), (it - 1) & 1, abort_flag);
               if (!ok) break;
               tc_fence_after();
             }
             // dQ = dS K          (A = dS MN-major in smem, B = K MN-major)
 #pragma unroll
             for (int kk = 0; kk < kBlk / 16; ++kk)
-              mma_ss(tmem + C::kColDQ, sdesc_sw128(dsb + kk * 2048, C::kChunkBytes, 1024),
+              mma_ss_w(tmem + C::kColDQ, sdesc_sw128(dsb + kk * 2048, C::kChunkBytes, 1024),
                      sdesc_sw128(kb + kk * 2048, C::kChunkBytes, 1024), kIdQ, kk > 0 ? 1u : 0u);
-            mma_commit(bar(C::kBarDQFull));
+            mma_commit_w(bar(C::kBarDQFull));
           }
           // dV += P_h^T dO_h   (A = P^T in TMEM, B = dO rows of half h, MN-major)
 #pragma unroll
           for (int kk = 0; kk < kHalf / 16; ++kk)
-            mma_ts(tmem + C::kColDV, tmem + C::kColS + kHalf * h + kk * 8,
+            mma_ts_w(tmem + C::kColDV, tmem + C::kColS + kHalf * h + kk * 8,
                    sdesc_sw128(dob + (4 * h + kk) * 2048, C::kChunkBytes, 1024), kIdV,
                    (it > 0 || h > 0 || kk > 0) ? 1u : 0u);
           // dK += dS_h^T Q_h   (A = dS^T K-major in smem region h, B = Q MN-major)
 #pragma unroll
           for (int kk = 0; kk < kHalf / 16; ++kk)
-            mma_ss(tmem + C::kColDK, sdesc_sw128(dsb + h * C::kChunkBytes + kk * 32, 16, 1024),
+            mma_ss_w(tmem + C::kColDK, sdesc_sw128(dsb + h * C::kChunkBytes + kk * 32, 16, 1024),
                    sdesc_sw128(qb + (4 * h + kk) * 2048, C::kChunkBytes, 1024), kIdK,
                    (it > 0 || h > 0 || kk > 0) ? 1u : 0u);
         }
         if (!ok) break;
-        mma_commit(bar(C::kBarQEmpty + s));
+        mma_commit_w(bar(C::kBarQEmpty + s));
       }
-      if (ok) mma_commit(bar(C::kBarDKDV));
-      mma_commit(bar(C::kBarDrain));
-      mbar_wait_sleep(bar(C::kBarDrain), 0, nullptr);
+      if (ok) mma_commit_w(bar(C::kBarDKDV));
+      mma_commit_w(bar(C::kBarDrain));
+      mbar_wait_sleep_w(bar(C::kBarDrain), 0, nullptr);
     }
   } else if (warp < kDqWarp0) {
     // ------------------------------------------------------------ P and dS

@@ -11,7 +11,7 @@
 // CTA organisation (320 threads, one CTA per SM):
 //   warps 0-3  softmax warpgroup of query tile 0 (thread = row = TMEM lane)
 //   warps 4-7  softmax warpgroup of query tile 1
-//   warp  8    tcgen05 MMA issue (one thread) and TMEM allocation
+//   warp  8    tcgen05 MMA issue (one elected lane) and TMEM allocation
 //   warp  9    TMA producer (one thread)
 // Every warp keeps the launch allocation (168 registers): lowering the MMA
 // warp's budget slows its issue loop, and the tensor core's issue queue is
@@ -279,15 +279,16 @@ __global__ void __launch_bounds__(FwdCfg<D, DV, QT>::kThreads, FwdCfg<D, DV, QT>
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issue
-    if (lane == 0) {
+    // the whole warp runs the issue loop (one elected lane issues)
+    {
       constexpr uint32_t kIdS = idesc_bf16_f32(kBlockM, kBlockN, false, false);
       constexpr uint32_t kIdO = idesc_bf16_f32(kBlockM, DV, false, true);
-      bool ok = n_stream > 0 ? mbar_wait(bar(C::kBarQFull), 0, abort_flag) : false;
+      bool ok = n_stream > 0 ? mbar_wait_w(bar(C::kBarQFull), 0, abort_flag) : false;
       tc_fence_after();
       int k_ready = -1;
       auto ensure_k = [&](int jj) {
         if (ok && jj > k_ready) {
-          ok = mbar_wait(bar(C::kBarKFull + jj % C::kStages), (jj / C::kStages) & 1, abort_flag);
+          ok = mbar_wait_w(bar(C::kBarKFull + jj % C::kStages), (jj / C::kStages) & 1, abort_flag);
           tc_fence_after();
           k_ready = jj;
         }
@@ -306,9 +307,9 @@ __global__ void __launch_bounds__(FwdCfg<D, DV, QT>::kThreads, FwdCfg<D, DV, QT>
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint64_t off = static_cast<uint64_t>(((kk >> 2) * C::kChunkBytes + (kk & 3) * 32) >> 4);
-          mma_ss(tmem + t * 128, q + off, k + off, kIdS, kk > 0 ? 1u : 0u);
+          mma_ss_w(tmem + t * 128, q + off, k + off, kIdS, kk > 0 ? 1u : 0u);
         }
-        mma_commit(bar(C::kBarSFull + t));
+        mma_commit_w(bar(C::kBarSFull + t));
       };
       // O_t (+)= P_t V for stream step jj; P_t from its TMEM columns
       auto issue_pv = [&](int t, int jj, bool first) {
@@ -316,7 +317,7 @@ __global__ void __launch_bounds__(FwdCfg<D, DV, QT>::kThreads, FwdCfg<D, DV, QT>
         const uint32_t pcol = C::kSepP ? C::kColP + t * 64 : t * 128;
 #pragma unroll
         for (int kk = 0; kk < kBlockN / 16; ++kk)
-          mma_ts(tmem + C::kColO + t * DV, tmem + pcol + kk * 8, v + 128 * kk, kIdO,
+          mma_ts_w(tmem + C::kColO + t * DV, tmem + pcol + kk * 8, v + 128 * kk, kIdO,
                  (!first || kk > 0) ? 1u : 0u);
       };
       auto step_of = [&](int t, int jj) -> int {  // tile-local step, or -1
@@ -328,7 +329,7 @@ __global__ void __launch_bounds__(FwdCfg<D, DV, QT>::kThreads, FwdCfg<D, DV, QT>
 #pragma unroll
         for (int t = 0; t < kQTiles; ++t)
           if (step_of(t, 0) == 0) issue_s(t, 0);
-        mma_commit(bar(C::kBarKEmpty + 0));
+        mma_commit_w(bar(C::kBarKEmpty + 0));
       }
       // The MMA thread shares its scheduler with busy softmax warps and the
       // tensor core's issue queue is short, so its loop is kept lean: when
@@ -341,7 +342,7 @@ __global__ void __launch_bounds__(FwdCfg<D, DV, QT>::kThreads, FwdCfg<D, DV, QT>
 #pragma unroll
             for (int t = 0; t < kQTiles; ++t) {
               if (!ok || jj + 1 >= (t == 0 ? b0 : b1)) continue;
-              ok = mbar_wait(bar(C::kBarSFree + t), jj & 1, abort_flag);
+              ok = mbar_wait_w(bar(C::kBarSFree + t), jj & 1, abort_flag);
               if (!ok) break;
               ensure_k(jj + 1);
               if (!ok) break;
@@ -349,20 +350,20 @@ __global__ void __launch_bounds__(FwdCfg<D, DV, QT>::kThreads, FwdCfg<D, DV, QT>
               issue_s(t, jj + 1);
             }
             if (!ok) break;
-            if (jj + 1 < n_stream) mma_commit(bar(C::kBarKEmpty + (jj + 1) % C::kStages));
-            ok = mbar_wait(bar(C::kBarVFull + jj % C::kStages), (jj / C::kStages) & 1, abort_flag);
+            if (jj + 1 < n_stream) mma_commit_w(bar(C::kBarKEmpty + (jj + 1) % C::kStages));
+            ok = mbar_wait_w(bar(C::kBarVFull + jj % C::kStages), (jj / C::kStages) & 1, abort_flag);
             tc_fence_after();
 #pragma unroll
             for (int t = 0; t < kQTiles; ++t) {
               if (!ok || jj >= (t == 0 ? b0 : b1)) continue;
-              ok = mbar_wait(bar(C::kBarPFull + t), jj & 1, abort_flag);
+              ok = mbar_wait_w(bar(C::kBarPFull + t), jj & 1, abort_flag);
               if (!ok) break;
               tc_fence_after();
               issue_pv(t, jj, jj == 0);
-              mma_commit(bar(C::kBarPVDone + t));
+              mma_commit_w(bar(C::kBarPVDone + t));
             }
             if (!ok) break;
-            mma_commit(bar(C::kBarVEmpty + jj % C::kStages));
+            mma_commit_w(bar(C::kBarVEmpty + jj % C::kStages));
           }
         }
         // General case: per stream step jj, QK^T of step jj+1 for each query
@@ -373,7 +374,7 @@ __global__ void __launch_bounds__(FwdCfg<D, DV, QT>::kThreads, FwdCfg<D, DV, QT>
           for (int t = 0; t < kQTiles; ++t) {
             const int u = step_of(t, jj + 1);
             if (!ok || u < 0) continue;
-            if (u > 0) ok = mbar_wait(bar(C::kBarSFree + t), (u - 1) & 1, abort_flag);
+            if (u > 0) ok = mbar_wait_w(bar(C::kBarSFree + t), (u - 1) & 1, abort_flag);
             if (!ok) break;
             ensure_k(jj + 1);
             if (!ok) break;
@@ -381,34 +382,34 @@ __global__ void __launch_bounds__(FwdCfg<D, DV, QT>::kThreads, FwdCfg<D, DV, QT>
             issue_s(t, jj + 1);
           }
           if (!ok) break;
-          if (jj + 1 < n_stream) mma_commit(bar(C::kBarKEmpty + (jj + 1) % C::kStages));
-          ok = mbar_wait(bar(C::kBarVFull + jj % C::kStages), (jj / C::kStages) & 1, abort_flag);
+          if (jj + 1 < n_stream) mma_commit_w(bar(C::kBarKEmpty + (jj + 1) % C::kStages));
+          ok = mbar_wait_w(bar(C::kBarVFull + jj % C::kStages), (jj / C::kStages) & 1, abort_flag);
           tc_fence_after();
 #pragma unroll
           for (int t = 0; t < kQTiles; ++t) {
             const int u = step_of(t, jj);
             if (!ok || u < 0) continue;
-            ok = mbar_wait(bar(C::kBarPFull + t), u & 1, abort_flag);
+            ok = mbar_wait_w(bar(C::kBarPFull + t), u & 1, abort_flag);
             if (!ok) break;
             tc_fence_after();
             issue_pv(t, jj, u == 0);
-            mma_commit(bar(C::kBarPVDone + t));
+            mma_commit_w(bar(C::kBarPVDone + t));
           }
           if (!ok) break;
-          mma_commit(bar(C::kBarVEmpty + jj % C::kStages));
+          mma_commit_w(bar(C::kBarVEmpty + jj % C::kStages));
         }
       } else {
         // P overwrites S: each tile's next QK^T is issued after its P.V, so
         // the P.V reads P before the new S lands in the same columns.
         if (aligned) {
           for (int jj = 0; jj < n_stream && ok; ++jj) {
-            ok = mbar_wait(bar(C::kBarVFull + jj % C::kStages), (jj / C::kStages) & 1, abort_flag);
+            ok = mbar_wait_w(bar(C::kBarVFull + jj % C::kStages), (jj / C::kStages) & 1, abort_flag);
             tc_fence_after();
 #pragma unroll
             for (int t = 0; t < kQTiles; ++t) {
               const int bt = t == 0 ? b0 : b1;
               if (!ok || jj >= bt) continue;
-              ok = mbar_wait(bar(C::kBarPFull + t), jj & 1, abort_flag);
+              ok = mbar_wait_w(bar(C::kBarPFull + t), jj & 1, abort_flag);
               if (!ok) break;
               tc_fence_after();
               issue_pv(t, jj, jj == 0);
@@ -417,22 +418,22 @@ __global__ void __launch_bounds__(FwdCfg<D, DV, QT>::kThreads, FwdCfg<D, DV, QT>
                 if (!ok) break;
                 issue_s(t, jj + 1);
               } else {
-                mma_commit(bar(C::kBarOFinal + t));
+                mma_commit_w(bar(C::kBarOFinal + t));
               }
             }
             if (!ok) break;
-            mma_commit(bar(C::kBarVEmpty + jj % C::kStages));
-            if (jj + 1 < n_stream) mma_commit(bar(C::kBarKEmpty + (jj + 1) % C::kStages));
+            mma_commit_w(bar(C::kBarVEmpty + jj % C::kStages));
+            if (jj + 1 < n_stream) mma_commit_w(bar(C::kBarKEmpty + (jj + 1) % C::kStages));
           }
         }
         for (int jj = 0; jj < n_stream && ok && !aligned; ++jj) {
-          ok = mbar_wait(bar(C::kBarVFull + jj % C::kStages), (jj / C::kStages) & 1, abort_flag);
+          ok = mbar_wait_w(bar(C::kBarVFull + jj % C::kStages), (jj / C::kStages) & 1, abort_flag);
           tc_fence_after();
 #pragma unroll
           for (int t = 0; t < kQTiles; ++t) {
             const int u = step_of(t, jj);
             if (!ok || u < 0) continue;
-            ok = mbar_wait(bar(C::kBarPFull + t), u & 1, abort_flag);
+            ok = mbar_wait_w(bar(C::kBarPFull + t), u & 1, abort_flag);
             if (!ok) break;
             tc_fence_after();
             issue_pv(t, jj, u == 0);
@@ -441,7 +442,7 @@ __global__ void __launch_bounds__(FwdCfg<D, DV, QT>::kThreads, FwdCfg<D, DV, QT>
               if (!ok) break;
               issue_s(t, jj + 1);
             } else {
-              mma_commit(bar(C::kBarOFinal + t));
+              mma_commit_w(bar(C::kBarOFinal + t));
             }
           }
           if (!ok) break;
@@ -453,13 +454,13 @@ __global__ void __launch_bounds__(FwdCfg<D, DV, QT>::kThreads, FwdCfg<D, DV, QT>
             issue_s(t, jj + 1);
           }
           if (!ok) break;
-          mma_commit(bar(C::kBarVEmpty + jj % C::kStages));
-          if (jj + 1 < n_stream) mma_commit(bar(C::kBarKEmpty + (jj + 1) % C::kStages));
+          mma_commit_w(bar(C::kBarVEmpty + jj % C::kStages));
+          if (jj + 1 < n_stream) mma_commit_w(bar(C::kBarKEmpty + (jj + 1) % C::kStages));
         }
       }
-      // Let every MMA this thread issued finish before TMEM is released.
-      mma_commit(bar(C::kBarDrain));
-      mbar_wait(bar(C::kBarDrain), 0, nullptr);
+      // Let every MMA this warp issued finish before TMEM is released.
+      mma_commit_w(bar(C::kBarDrain));
+      mbar_wait_w(bar(C::kBarDrain), 0, nullptr);
     }
   } else if (warp < kMmaWarp) {
     // ------------------------------------------------------------ softmax

@@ -434,6 +434,11 @@ __device__ __forceinline__ bool mbar_wait_w(uint32_t bar, uint32_t parity, volat
   return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort));
 }
 
+// mbar_wait_sleep by all 32 lanes of a warp, with one verdict for all.
+__device__ __forceinline__ bool mbar_wait_sleep_w(uint32_t bar, uint32_t parity, volatile int* abort) {
+  return __all_sync(0xffffffffu, mbar_wait_sleep(bar, parity, abort));
+}
+
 // ---------------------------------------------------------------- math
 // 3-input maximum (one instruction on sm_100 and later).
 __device__ __forceinline__ float max3(float a, float b, float c) {
