@@ -436,6 +436,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* ds_base = base_ptr + C::kDSOff + w * C::kChunkBytes + key_row * 128;
     const int key_sw = key_row & 7;
     const float2 sl2x2 = make_float2(sl2, sl2);
+    const KeepTest kt = keep_test(args.drop.t);
     bool ok = true;
     for (int it = 0; it < n_steps; ++it) {
       const float* nlse2_s =
@@ -472,6 +473,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld_wait(sr);
         tmem_ld_wait(dr);
         uint32_t pp[16], dd[16];
+        [[maybe_unused]] uint32_t kbits = 0;  // dropout: keep bits (0x80 per kept byte) of the current query group
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
           const int ql = c * 32 + e;            // query column within this half
@@ -485,16 +487,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (qc < rm.qc_lo || qc >= rm.qc_hi) p.x = 0.f;
             if (qc + 1 < rm.qc_lo || qc + 1 >= rm.qc_hi) p.y = 0.f;
           }
-          float2 dpv = make_float2(__uint_as_float(dr[e]), __uint_as_float(dr[e + 1]));
-          float2 pk = p;
-          if constexpr (kDrop) {  // queries e, e + 1: bytes (e & 3), (e & 3) + 1 of group (e >> 2) & 3
-            const uint32_t word = kball[ql >> 2] >> ((e & 3) * 8);
-            const float ik = args.drop.inv_keep;
-            if ((word & 0xffu) < args.drop.t) { pk.x = 0.f; dpv.x = 0.f; } else { dpv.x *= ik; }
-            if (((word >> 8) & 0xffu) < args.drop.t) { pk.y = 0.f; dpv.y = 0.f; } else { dpv.y *= ik; }
+          const float2 dpv = make_float2(__uint_as_float(dr[e]), __uint_as_float(dr[e + 1]));
+          float2 g;
+          uint32_t pkd = pack_bf16(p.x, p.y);
+          if constexpr (kDrop) {
+            // queries e, e + 1 are bytes (e & 3), (e & 3) + 1 of group (e >> 2) & 3: a kept
+            // query's dP is scaled by 1 / (1 - p), a dropped one's is 0 and its P is cleared
+            if ((e & 3) == 0) kbits = keep_bits4(kball[ql >> 2], kt);
+            const uint32_t ikb = __float_as_uint(args.drop.inv_keep);
+            const float2 f =
+                (e & 3) ? make_float2(__uint_as_float(ikb & sign_bytes<0xAAAAu>(kbits)),
+                                      __uint_as_float(ikb & sign_bytes<0xBBBBu>(kbits)))
+                        : make_float2(__uint_as_float(ikb & sign_bytes<0x8888u>(kbits)),
+                                      __uint_as_float(ikb & sign_bytes<0x9999u>(kbits)));
+            g = __fmul2_rn(p, __ffma2_rn(dpv, f, nd));
+            pkd &= (e & 3) ? sign_bytes<0xBBAAu>(kbits) : sign_bytes<0x9988u>(kbits);
+          } else {
+            g = __fmul2_rn(p, __fadd2_rn(dpv, nd));
           }
-          const float2 g = __fmul2_rn(p, __fadd2_rn(dpv, nd));
-          pp[e >> 1] = pack_bf16(pk.x, pk.y);
+          pp[e >> 1] = pkd;
           dd[e >> 1] = pack_bf16(g.x, g.y);
         }
         tmem_st16(tS + c * 16, pp);
@@ -964,6 +975,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float sl2 = args.scale_log2;
     const float2 sl2x2 = make_float2(sl2, sl2);
     const int key_sw = key_row & 7;
+    const KeepTest kt = keep_test(args.drop.t);
     bool ok = true;
     int g = 0;
     for (int n = 0; ok; ++n) {
@@ -1027,6 +1039,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int qc = 64 * w + ql;    // ... within the query block
           const float4 nl = *reinterpret_cast<const float4*>(nlse2_s + ql);
           const float4 nd = *reinterpret_cast<const float4*>(nd_s + ql);
+          [[maybe_unused]] uint32_t kbits = 0;  // dropout: keep bits (0x80 per kept byte) of queries ql .. ql + 3
+          if constexpr (kDrop) kbits = keep_bits4(kball[ql >> 2], kt);
 #pragma unroll
           for (int u = 0; u < 2; ++u) {
             const float2 nl2 = u ? make_float2(nl.z, nl.w) : make_float2(nl.x, nl.y);
@@ -1043,16 +1057,24 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (qc + 2 * u < key_row) p.x = 0.f;
               if (qc + 2 * u + 1 < key_row) p.y = 0.f;
             }
-            float2 dpv = make_float2(__uint_as_float(dr[x]), __uint_as_float(dr[x + 1]));
-            float2 pk = p;
-            if constexpr (kDrop) {  // queries x, x + 1: bytes 2u, 2u + 1 of group (e >> 2) & 3
-              const uint32_t word = kball[ql >> 2] >> (16 * u);
-              const float ik = args.drop.inv_keep;
-              if ((word & 0xffu) < args.drop.t) { pk.x = 0.f; dpv.x = 0.f; } else { dpv.x *= ik; }
-              if (((word >> 8) & 0xffu) < args.drop.t) { pk.y = 0.f; dpv.y = 0.f; } else { dpv.y *= ik; }
+            const float2 dpv = make_float2(__uint_as_float(dr[x]), __uint_as_float(dr[x + 1]));
+            float2 gs;
+            uint32_t pkd = pack_bf16(p.x, p.y);
+            if constexpr (kDrop) {
+              // queries x, x + 1 are bytes 2u, 2u + 1 of kbits: a kept query's dP is scaled by
+              // 1 / (1 - p), a dropped one's is 0 and its half of the P^T pair is cleared
+              const uint32_t ikb = __float_as_uint(args.drop.inv_keep);
+              const float2 f =
+                  u ? make_float2(__uint_as_float(ikb & sign_bytes<0xAAAAu>(kbits)),
+                                  __uint_as_float(ikb & sign_bytes<0xBBBBu>(kbits)))
+                    : make_float2(__uint_as_float(ikb & sign_bytes<0x8888u>(kbits)),
+                                  __uint_as_float(ikb & sign_bytes<0x9999u>(kbits)));
+              gs = __fmul2_rn(p, __ffma2_rn(dpv, f, nd2));
+              pkd &= u ? sign_bytes<0xBBAAu>(kbits) : sign_bytes<0x9988u>(kbits);
+            } else {
+              gs = __fmul2_rn(p, __fadd2_rn(dpv, nd2));
             }
-            const float2 gs = __fmul2_rn(p, __fadd2_rn(dpv, nd2));
-            pp[(ql >> 1) + u] = pack_bf16(pk.x, pk.y);
+            pp[(ql >> 1) + u] = pkd;
             dd[(ql >> 1) + u] = pack_bf16(gs.x, gs.y);
           }
         }

@@ -543,8 +543,10 @@ __global__ void __launch_bounds__(FwdCfg<D, DV, QT>::kThreads, FwdCfg<D, DV, QT>
       const float2 sl2x2 = make_float2(sl2, sl2);
       const float2 negm = make_float2(-m_use, -m_use);
       float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+      const KeepTest kt = keep_test(args.drop.t);
       auto exp_half = [&](int h, uint32_t (&pk)[32]) {
         uint32_t kb[4];  // dropout, second half: keep bytes of this row for the current 16 keys
+        [[maybe_unused]] uint32_t kbits = 0;  // keep bits (0x80 per kept byte) of the current key group
 #pragma unroll
         for (int c = 0; c < 32; ++c) {
           const int e = 64 * h + 2 * c;
@@ -558,12 +560,13 @@ __global__ void __launch_bounds__(FwdCfg<D, DV, QT>::kThreads, FwdCfg<D, DV, QT>
           float2 pr = make_float2(ex2(a.x), ex2(a.y));
           if (c & 1) acc1 = __fadd2_rn(acc1, pr);
           else acc0 = __fadd2_rn(acc0, pr);
-          if constexpr (kDrop) {  // keys e, e + 1: bytes 2 (c & 1), 2 (c & 1) + 1 of key group e >> 2
-            const uint32_t word = (h == 0 ? kpre[c >> 1] : kb[(c >> 1) & 3]) >> ((c & 1) * 16);
-            if ((word & 0xffu) < args.drop.t) pr.x = 0.f;
-            if (((word >> 8) & 0xffu) < args.drop.t) pr.y = 0.f;
-          }
           pk[c] = pack_bf16(pr.x, pr.y);
+          if constexpr (kDrop) {
+            // keys e, e + 1 are bytes 2 (c & 1), 2 (c & 1) + 1 of key group e >> 2; a dropped
+            // key's half of the bf16 pair is cleared (its p still counts in the row sum)
+            if ((c & 1) == 0) kbits = keep_bits4(h == 0 ? kpre[c >> 1] : kb[(c >> 1) & 3], kt);
+            pk[c] &= (c & 1) ? sign_bytes<0xBBAAu>(kbits) : sign_bytes<0x9988u>(kbits);
+          }
         }
       };
       uint32_t pk[32];
@@ -1118,8 +1121,10 @@ __global__ void __launch_bounds__(kThreads, 2)
         const float2 sl2x2 = make_float2(sl2, sl2);
         const float2 negm = make_float2(-m_use, -m_use);
         float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+        const KeepTest kt = keep_test(args.drop.t);
         auto exp_half = [&](int h, uint32_t (&pk)[32]) {
           uint32_t kb[4];  // dropout, second half: keep bytes of this row for the current 16 keys
+          [[maybe_unused]] uint32_t kbits = 0;  // keep bits (0x80 per kept byte) of the current key group
 #pragma unroll
           for (int c = 0; c < 32; ++c) {
             const int e = 64 * h + 2 * c;
@@ -1133,12 +1138,13 @@ __global__ void __launch_bounds__(kThreads, 2)
             float2 pr = make_float2(ex2(a.x), ex2(a.y));
             if (c & 1) acc1 = __fadd2_rn(acc1, pr);
             else acc0 = __fadd2_rn(acc0, pr);
-            if constexpr (kDrop) {  // keys e, e + 1: bytes 2 (c & 1), 2 (c & 1) + 1 of key group e >> 2
-              const uint32_t word = (h == 0 ? kpre[c >> 1] : kb[(c >> 1) & 3]) >> ((c & 1) * 16);
-              if ((word & 0xffu) < args.drop.t) pr.x = 0.f;
-              if (((word >> 8) & 0xffu) < args.drop.t) pr.y = 0.f;
-            }
             pk[c] = pack_bf16(pr.x, pr.y);
+            if constexpr (kDrop) {
+              // keys e, e + 1 are bytes 2 (c & 1), 2 (c & 1) + 1 of key group e >> 2; a dropped
+              // key's half of the bf16 pair is cleared (its p still counts in the row sum)
+              if ((c & 1) == 0) kbits = keep_bits4(h == 0 ? kpre[c >> 1] : kb[(c >> 1) & 3], kt);
+              pk[c] &= (c & 1) ? sign_bytes<0xBBAAu>(kbits) : sign_bytes<0x9988u>(kbits);
+            }
           }
         };
         uint32_t pk[32];

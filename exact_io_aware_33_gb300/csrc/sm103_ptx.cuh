@@ -488,10 +488,9 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1
   return c;
 }
 
-// Word idx (0..3, run-time) of four registers.
-__device__ __forceinline__ uint32_t pick4(uint32_t a, uint32_t b, uint32_t c, uint32_t d, uint32_t idx) {
-  const uint32_t lo = (idx & 1u) ? b : a, hi = (idx & 1u) ? d : c;
-  return (idx & 2u) ? hi : lo;
+// Exchange with lane ^ mask: send `if_set` when bit is 1, else `if_clear`.
+__device__ __forceinline__ uint32_t shfl_xor_sel(uint32_t bit, uint32_t if_set, uint32_t if_clear, int mask) {
+  return __shfl_xor_sync(0xffffffffu, bit ? if_set : if_clear, mask);
 }
 
 // Dropout keep bytes. One generator call covers a 4 x 4 block of (query,
@@ -500,7 +499,7 @@ __device__ __forceinline__ uint32_t pick4(uint32_t a, uint32_t b, uint32_t c, ui
 // consecutive rows of one kind (queries in the forward, keys in the
 // backward, lane & 3 = row & 3) and need the same 16 columns of the other
 // kind: lane r makes the call for column group r and the four words are
-// rotated among the quad in four shuffles. On return out[g] holds this
+// exchanged among the quad in four shuffles. On return out[g] holds this
 // lane's four bytes of column group g (byte c = column 4g + c).
 //   row_major = true:  calls are indexed (column group, row group): the
 //                      forward (rows = queries, columns = keys)
@@ -528,17 +527,48 @@ __device__ __forceinline__ void keep_bytes_quad(uint32_t row_group, uint32_t col
     t2 = __byte_perm(hi01, hi23, 0x5410);
     t3 = __byte_perm(hi01, hi23, 0x7632);
   }
-  const int quad = static_cast<int>(threadIdx.x & 31u) & ~3;
-  uint32_t rot[4];
-#pragma unroll
-  for (int s = 0; s < 4; ++s) {
-    // round s: lane r receives, from lane (r + s) & 3, that lane's call's part for lane r
-    const uint32_t send = pick4(t0, t1, t2, t3, (r - static_cast<uint32_t>(s)) & 3u);
-    rot[s] = __shfl_sync(0xffffffffu, send, quad | static_cast<int>((r + s) & 3u));
-  }
-  // rot[s] belongs to column group (r + s) & 3
-#pragma unroll
-  for (int g = 0; g < 4; ++g) out[g] = pick4(rot[0], rot[1], rot[2], rot[3], (static_cast<uint32_t>(g) - r) & 3u);
+  // 4 x 4 transpose of words across the quad: lane j needs word j of every
+  // lane's call. Two butterfly exchanges (lane bit 0, then bit 1), each
+  // sending the two words whose index differs from the lane in that bit.
+  const uint32_t b0 = r & 1u, b1 = (r >> 1) & 1u;
+  const uint32_t s0 = shfl_xor_sel(b0, t0, t1, 1), s1 = shfl_xor_sel(b0, t2, t3, 1);
+  const uint32_t n0 = b0 ? s0 : t0, n1 = b0 ? t1 : s0, n2 = b0 ? s1 : t2, n3 = b0 ? t3 : s1;
+  const uint32_t u0 = shfl_xor_sel(b1, n0, n2, 2), u1 = shfl_xor_sel(b1, n1, n3, 2);
+  // out[g]: this lane's part of lane g's call, i.e. of column group g
+  out[0] = b1 ? u0 : n0;
+  out[1] = b1 ? u1 : n1;
+  out[2] = b1 ? n2 : u0;
+  out[3] = b1 ? n3 : u1;
+}
+
+// Dropout keep test on the four bytes of a word at once (an element is kept
+// when its byte is >= t, t in [0, 255]). Per byte b, (b | 0x80) - t' cannot
+// borrow from the next byte for t' <= 128, and its top bit says whether the
+// low seven bits of b reach t'. For t <= 128 a byte is kept when its top bit
+// is set or the low bits reach t (t' = t); for t > 128 only when its top
+// bit is set and the low bits reach t - 128 (t' = t - 128).
+struct KeepTest {
+  uint32_t t4;    // t' in every byte
+  uint32_t high;  // all ones when t > 128
+};
+__device__ __forceinline__ KeepTest keep_test(uint32_t t) {
+  const bool hi = t > 128u;
+  return KeepTest{(hi ? t - 128u : t) * 0x01010101u, hi ? 0xffffffffu : 0u};
+}
+// 0x80 in each byte of w that is kept, 0 in each byte that is dropped.
+__device__ __forceinline__ uint32_t keep_bits4(uint32_t w, KeepTest k) {
+  const uint32_t x = (w | 0x80808080u) - k.t4;
+  return (((w & x) & k.high) | ((w | x) & ~k.high)) & 0x80808080u;
+}
+// prmt with sign replication: each selector nibble 8 + i fills its result
+// byte with the top bit of byte i of a, so keep bits become byte masks
+// (0x9988: bytes 0, 1 -> the low and high halves of a bf16 pair; 0x8888:
+// byte 0 -> a whole 32-bit word).
+template <uint32_t kSel>
+__device__ __forceinline__ uint32_t sign_bytes(uint32_t a) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %1, %2;" : "=r"(d) : "r"(a), "n"(kSel));
+  return d;
 }
 
 }  // namespace fa
