@@ -328,6 +328,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (it >= C::kStages)
           ok = mbar_wait_sleep(bar(C::kBarQEmpty + s), ((it / C::kStages) + 1) & 1, abort_flag);
         if (!ok) break;
+#ifdef FA_TEST_SKIP_ARRIVE
+        // Test-only build (never in libfa.so): the item's last query step is
+        // never loaded, so the MMA warp's bounded wait for it runs out and the
+        // CTA winds down through the abort path.
+        if (it == n_steps - 1 && n_steps > 1) break;
+#endif
         const int row0 = (i0 + it) * kBlk;
         const uint32_t st = base + C::kStageOff + s * C::kStageBytes;
         const uint32_t fb = bar(C::kBarQFull + s);
@@ -842,7 +848,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_3d_hint(base + kKOff + kv * kKVBytes, &tmK, bar(kBarKV + kv), 0, jb * kBlk, bh, once);
         tma_load_3d_hint(base + kVOff + kv * kKVBytes, &tmV, bar(kBarKV + kv), 0, jb * kBlk, bh, once);
         ++n_kv;
-        for (int it = 1; it < ns && ok; ++it) load_q(bh, (i0 + it) * kBlk);
+        for (int it = 1; it < ns && ok; ++it) {
+#ifdef FA_TEST_SKIP_ARRIVE
+          // Test-only build (never in libfa.so): the first item's last query
+          // step is never loaded and nothing more is, so the issuing warps'
+          // bounded waits for it run out and the CTA winds down.
+          if (n == 0 && it == ns - 1) {
+            ok = false;
+            break;
+          }
+#endif
+          load_q(bh, (i0 + it) * kBlk);
+        }
       }
     }
   } else if (warp == kMmaWarp) {

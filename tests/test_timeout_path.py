@@ -7,8 +7,10 @@ kernel sets the device status word that ``fa_get_last_device_status`` turns
 into FA_ERR_TIMEOUT. A test-only variant of the library (built separately
 with ``-DFA_TEST_SKIP_ARRIVE``, never part of ``libfa.so``) makes that happen
 on purpose: the forward's producer never loads the last V tile of its key
-stream, so the MMA thread's wait for it runs out after the variant's 20 ms
-budget. The test checks that the call returns, that the status says
+stream, and the backward's producers never load the last query step of an
+item (the d = 64 kernel: of each CTA's first item, after which it loads
+nothing more), so the issuing warps' waits run out after the variant's 20 ms
+budget. Each test checks that the call returns, that the status says
 FA_ERR_TIMEOUT (once: reading it clears it), and that the same process then
 runs the product library's forward and backward with results matching the
 oracle, i.e. the context is intact.
@@ -75,4 +77,41 @@ def test_wait_runs_out_and_the_context_survives(timeout_lib, d):
     refs = dense.backward(x["q"], x["k"], x["v"], o_ref, lse_ref, x["do"], False, scale)
     for got, ref in zip(grads, refs):
         gg = got.float().cpu().double().numpy()
+        assert np.abs(gg - ref).max() / np.abs(ref).max() <= 5e-2
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_backward_wait_runs_out_and_the_context_survives(timeout_lib, d):
+    # d = 64: the persistent pipelined kernel; d = 128: the sequential one.
+    # N = 384 causal gives items of 3, 2 and 1 query steps per head.
+    B, H, N, scale = 1, 2, 384, 1.0 / math.sqrt(d)
+    x = si.make_small(B, H, N, d, seed=3200 + d, with_grad=True)
+    g = {n: t.cuda() for n, t in x.items()}
+    o, lse = fa.fa_fwd(g["q"], g["k"], g["v"], causal=True, scale=scale)  # product library
+    grads = [torch.empty_like(g["q"]) for _ in range(3)]
+    ws_bytes = timeout_lib.fa_bwd_workspace_bytes(B, H, N, d)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    torch.cuda.synchronize()
+    assert fa.fa_get_last_device_status() == fa.FA_OK
+
+    t0 = time.perf_counter()
+    rc = timeout_lib.fa_bwd_stream(_p(g["q"]), _p(g["k"]), _p(g["v"]), _p(o), _p(lse), _p(g["do"]),
+                                   _p(grads[0]), _p(grads[1]), _p(grads[2]), B, H, N, d, 1, scale, _p(ws),
+                                   ws_bytes, ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert rc == fa.FA_OK
+    status = timeout_lib.fa_get_last_device_status()
+    elapsed = time.perf_counter() - t0
+    assert status == fa.FA_ERR_TIMEOUT
+    assert elapsed < 10.0, f"the wind-down took {elapsed:.2f} s"
+    assert timeout_lib.fa_get_last_device_status() == fa.FA_OK
+    assert fa.fa_get_last_device_status() == fa.FA_OK
+
+    # the product library's backward in the same process, against the oracle
+    got = fa.fa_bwd(g["q"], g["k"], g["v"], o, lse, g["do"], causal=True, scale=scale)
+    torch.cuda.synchronize()
+    assert fa.fa_get_last_device_status() == fa.FA_OK
+    o_ref, lse_ref = dense.forward(x["q"], x["k"], x["v"], True, scale)
+    refs = dense.backward(x["q"], x["k"], x["v"], o_ref, lse_ref, x["do"], True, scale)
+    for t, ref in zip(got, refs):
+        gg = t.float().cpu().double().numpy()
         assert np.abs(gg - ref).max() / np.abs(ref).max() <= 5e-2
