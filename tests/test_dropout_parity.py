@@ -50,7 +50,9 @@ def _expected_codes(mask, d):
     return sum(mask[:, t * d:(t + 1) * d].astype(np.int64) << t for t in range(n // d))
 
 
-@pytest.mark.parametrize("d,p", [(64, 0.1), (64, 0.5), (128, 0.25)])
+# p = 0.5 and below: byte thresholds t <= 128; 0.6 and 0.75: t = 154 and 192,
+# the keep test's other branch (a byte is kept only with its top bit set)
+@pytest.mark.parametrize("d,p", [(64, 0.1), (64, 0.5), (128, 0.25), (64, 0.75), (128, 0.6)])
 def test_forward_mask_bit_exact(d, p):
     B, H, N = 2, 3, 4 * d
     q, k, v, do = _codes_inputs(B, H, N, d, "fwd")
@@ -68,7 +70,9 @@ def test_forward_mask_bit_exact(d, p):
     np.testing.assert_allclose(lse.cpu().numpy(), math.log(N), rtol=0, atol=1e-5)
 
 
-@pytest.mark.parametrize("d,p", [(64, 0.1), (64, 0.5), (128, 0.25)])
+# p = 0.5 and below: byte thresholds t <= 128; 0.6 and 0.75: t = 154 and 192,
+# the keep test's other branch (a byte is kept only with its top bit set)
+@pytest.mark.parametrize("d,p", [(64, 0.1), (64, 0.5), (128, 0.25), (64, 0.75), (128, 0.6)])
 def test_backward_mask_bit_exact(d, p):
     B, H, N = 2, 3, 4 * d
     q, k, v, do = _codes_inputs(B, H, N, d, "bwd")
