@@ -717,11 +717,13 @@ enum : int {
   kBarSFull = kBarQEmpty + kStages,
   kBarSFree,     // S^T, dP^T are in registers
   kBarPFree,     // the step's dV MMA has read P^T
-  kBarDSFull,    // dS written; dQ (and at an item start dK, dV) read out
+  kBarDSFull,    // dS written; the previous step's dQ read out
   kBarPFull,     // P^T written
   kBarDSFree,    // the step's dQ and dK MMAs have read dS
   kBarDQFull,
   kBarDKDV,
+  kBarDKFree,    // an item's dK read out of tensor memory (4 dQ warps)
+  kBarDVFree,    // an item's dV read out (4 dQ warps)
   kBarDrain,     // two: one per issuing thread
   kNumBars = kBarDrain + 2
 };
@@ -787,6 +789,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(kBarDSFree), 1);
     mbar_init(bar(kBarDQFull), 1);
     mbar_init(bar(kBarDKDV), 1);
+    mbar_init(bar(kBarDKFree), 4);
+    mbar_init(bar(kBarDVFree), 4);
     mbar_init(bar(kBarDrain), 1);
     mbar_init(bar(kBarDrain + 1), 1);
     *abort_flag = 0;
@@ -888,8 +892,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // step's P and dS were formed
         const uint64_t kKmn = sdesc_sw128(kvb + kKOff, kTileBytes, 1024);  // K as MN-major B
         for (int it = 0; it < ns && ok; ++it, ++g) {
-          // P^T and dS of step g written, dQ of step g-1 (and at an item's
-          // first step the previous item's dK, dV) read out of tensor memory
+          // P^T and dS of step g written, dQ of step g-1 read out of tensor
+          // memory (at an item's first step the previous item's dK and dV
+          // read-outs are waited for separately, just before dK and dV)
           ok = mbar_wait_w(bar(kBarDSFull), g & 1, abort_flag);
           if (!ok) break;
           tc_fence_after();
@@ -901,6 +906,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int kk = 0; kk < kBlk / 16; ++kk)
             mma_ss_w(tmem + kColDQ, dsmn + 128 * kk, kKmn + 128 * kk, kIdQ, kk > 0 ? 1u : 0u);
           mma_commit_w(bar(kBarDQFull));
+          if (it == 0 && n > 0) {  // the previous item's dK has been read out
+            ok = mbar_wait_w(bar(kBarDKFree), (n - 1) & 1, abort_flag);
+            if (!ok) break;
+            tc_fence_after();
+          }
           // dK += dS^T Q   (A = dS^T K-major, query halves in two 16 KiB regions; B = Q MN-major)
 #pragma unroll
           for (int kk = 0; kk < kBlk / 16; ++kk)
@@ -911,6 +921,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_commit_w(bar(kBarDSFree));
           // dV += P^T dO   (A = P^T bf16 pairs in TMEM, B = dO MN-major, 16 rows per step)
           ok = mbar_wait_w(bar(kBarPFull), g & 1, abort_flag);
+          if (ok && it == 0 && n > 0) ok = mbar_wait_w(bar(kBarDVFree), (n - 1) & 1, abort_flag);
           if (!ok) break;
           tc_fence_after();
 #pragma unroll
@@ -1183,7 +1194,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld32(tmem + lane_base + kColDQ + 32, gr);
         tmem_ld_wait(gr);
         tc_fence_before();
-        if (it + 1 < ns) mbar_arrive_warp(bar(kBarDSFull));  // dQ columns free for step g+1
+        mbar_arrive_warp(bar(kBarDSFull));  // dQ columns free for step g+1
         put_block(gr, dst + 1024);
       }
       if (!ok) break;
@@ -1214,9 +1225,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t gr[32];
           tmem_ld32(tmem + lane_base + col + c * 32, gr);
           tmem_ld_wait(gr);
-          if (which == 1 && c == kD / 32 - 1) {  // dQ, dK, dV columns free for the next item
+          if (c == kD / 32 - 1) {  // this item's dK (dV) columns free for the next item
             tc_fence_before();
-            mbar_arrive_warp(bar(kBarDSFull));
+            mbar_arrive_warp(bar(which == 0 ? kBarDKFree : kBarDVFree));
           }
           uint32_t pk[16];
 #pragma unroll
