@@ -1057,8 +1057,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool win = args.window != 0 && rm.active;
       const bool diag = args.causal && it == 0;
       uint32_t pp[32], dd[32];
-      // kind 0: no mask; 1: causal diagonal block; 2: window boundary block.
-      // A compile-time kind keeps the unmasked blocks free of per-element tests.
+      // kind 0: no mask (the causal diagonal block is masked afterwards, on
+      // the packed words); 2: window boundary block. A compile-time kind
+      // keeps the unmasked blocks free of per-element tests.
       auto half = [&](auto kind, const uint32_t (&sr)[32], const uint32_t (&dr)[32], int c) {
         constexpr int kKind = decltype(kind)::value;
 #pragma unroll
@@ -1081,9 +1082,6 @@ __global__ void __launch_bounds__(kThreads, 1)
               const int q0 = qc + 2 * u;
               if (q0 < rm.qc_lo || q0 >= rm.qc_hi) p.x = 0.f;
               if (q0 + 1 < rm.qc_lo || q0 + 1 >= rm.qc_hi) p.y = 0.f;
-            } else if constexpr (kKind == 1) {  // causal diagonal: a query before the key is masked
-              if (qc + 2 * u < key_row) p.x = 0.f;
-              if (qc + 2 * u + 1 < key_row) p.y = 0.f;
             }
             const float2 dpv = make_float2(__uint_as_float(dr[x]), __uint_as_float(dr[x + 1]));
             float2 gs;
@@ -1110,12 +1108,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (win) {
         half(std::integral_constant<int, 2>{}, s0, d0, 0);
         half(std::integral_constant<int, 2>{}, s1, d1, 1);
-      } else if (diag) {
-        half(std::integral_constant<int, 1>{}, s0, d0, 0);
-        half(std::integral_constant<int, 1>{}, s1, d1, 1);
       } else {
         half(std::integral_constant<int, 0>{}, s0, d0, 0);
         half(std::integral_constant<int, 0>{}, s1, d1, 1);
+        if (diag) {
+          // Causal diagonal block, through the unmasked code above (which is
+          // hot; a masked copy of it ran cold once per item): query column
+          // 64 w + j comes before this key for j < lim, and there P and dS
+          // are 0, so those halves of the packed words are cleared.
+          const int lim = key_row - 64 * w;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const int t = lim - 2 * i;  // masked elements among 2i, 2i + 1
+            const uint32_t m = t <= 0 ? 0xffffffffu : (t == 1 ? 0xffff0000u : 0u);
+            pp[i] &= m;
+            dd[i] &= m;
+          }
+        }
       }
 
       // dS^T row of this key into the dS buffer once step g-1's dQ and dK
