@@ -797,8 +797,8 @@ constexpr int kVOff = kKOff + kStages * kTileBytes;
 constexpr int kBarOff = kVOff + kStages * kTileBytes;
 enum : int {
   kBarQFull = 0,               // two
-  kBarQFree = kBarQFull + 2,   // two: the tile's write-back is done with its Q buffer (4 warps)
-  kBarKFull = kBarQFree + 2,
+  kBarOStaged = kBarQFull + 2,  // two: the tile's O rows are staged in its Q buffer (4 warps)
+  kBarKFull = kBarOStaged + 2,
   kBarKEmpty = kBarKFull + kStages,
   kBarVFull = kBarKEmpty + kStages,
   kBarVEmpty = kBarVFull + kStages,
@@ -810,7 +810,10 @@ enum : int {
   kNumBars
 };
 constexpr int kMiscOff = kBarOff + kNumBars * 8;
-constexpr int kSmemBytes = kMiscOff + 16 + 1024;  // + slack to align the base
+// two item records (int4: bh, row0, lo, n), 16-byte aligned for their vector accesses
+constexpr int kRecOff = (kMiscOff + 16 + 15) & ~15;
+static_assert(kRecOff % 16 == 0, "item records need 16-byte alignment");
+constexpr int kSmemBytes = kRecOff + 32 + 1024;   // + slack to align the base
 static_assert(2 * kSmemBytes <= 233472, "two persistent CTAs must fit on an SM");
 constexpr uint32_t kTmemCols = 256;
 constexpr uint32_t kColS = 0, kColO = 128, kColP = 192;
@@ -874,7 +877,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   if (threadIdx.x == 0) {
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar(kBarQFull + b), 1);
-      mbar_init(bar(kBarQFree + b), 4);
+      mbar_init(bar(kBarOStaged + b), 4);
     }
     for (int st = 0; st < kStages; ++st) {
       mbar_init(bar(kBarKFull + st), 1);
@@ -908,18 +911,46 @@ __global__ void __launch_bounds__(kThreads, 2)
       tma_prefetch_map(&tmQ);
       tma_prefetch_map(&tmK);
       tma_prefetch_map(&tmV);
+      tma_prefetch_map(&tmO);
       const uint64_t once = policy_evict_first();  // a Q tile is read by one item only
       bool ok = true;
       int q = 0, u = 0;
+      // write-back coordinates of the items in Q buffers 0 and 1
+      int wb_row0[2] = {0, 0}, wb_bh[2] = {0, 0};
+      // Item qi's O, staged by the softmax warps in its Q buffer: one TMA
+      // store per warp's 32 rows (rows past Nq are clipped by the O map).
+      auto store_o = [&](int qi) {
+        const int bb = qi & 1;
+        ok = mbar_wait(bar(kBarOStaged + bb), (qi >> 1) & 1, abort_flag);
+        if (!ok) return;
+#pragma unroll
+        for (int w4 = 0; w4 < 4; ++w4)
+          tma_store_3d(&tmO, base + kQOff + bb * kTileBytes + w4 * 4096, 0, wb_row0[bb] + 32 * w4, wb_bh[bb]);
+        bulk_commit_group();
+      };
+      // the record of the item in Q buffer bb, read by the softmax warps once
+      // the buffer's QFull phase has completed (n = 0 ends the list)
+      auto put_record = [&](int bb, int bh, int row0, int lo, int n) {
+        asm volatile("st.shared.v4.s32 [%0], {%1, %2, %3, %4};" ::"r"(base + kRecOff + 16 * bb), "r"(bh),
+                     "r"(row0), "r"(lo), "r"(n)
+                     : "memory");
+      };
       for (int k = 0; ok; ++k) {
         int x;
         if (!item_of(k, num_items, &x)) break;
         const Item it = item_geom(args, x);
         if (it.n == 0) continue;
         const int b = q & 1;
-        // Q buffer b is free once the write-back of the tile before last has read it
-        if (q >= 2) ok = mbar_wait(bar(kBarQFree + b), ((q >> 1) - 1) & 1, abort_flag);
-        if (!ok) break;
+        // Q buffer b is free once the write-back of the tile before last, staged
+        // in it, has been stored and the store has read it
+        if (q >= 2) {
+          store_o(q - 2);
+          if (!ok) break;
+          bulk_wait_read<0>();
+        }
+        wb_row0[b] = it.row0;
+        wb_bh[b] = it.bh;
+        put_record(b, it.bh, it.row0, it.lo, it.n);
         mbar_arrive_expect_tx(bar(kBarQFull + b), kTileBytes);
         tma_load_3d_hint(base + kQOff + b * kTileBytes, &tmQ, bar(kBarQFull + b), 0, it.row0, it.bh, once);
         q_loaded = ++q;
@@ -949,6 +980,15 @@ __global__ void __launch_bounds__(kThreads, 2)
           ++u;
         }
       }
+      if (ok) {
+        // the end of the item list for the softmax warps (a plain arrival
+        // completes the QFull phase they wait for), then the last two
+        // write-backs
+        put_record(q & 1, 0, 0, 0, 0);
+        mbar_arrive(bar(kBarQFull + (q & 1)));
+        for (int qi = q >= 2 ? q - 2 : 0; qi < q && ok; ++qi) store_o(qi);
+      }
+      bulk_wait<0>();  // the write-backs' global writes complete before the CTA exits
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issue
@@ -1049,12 +1089,20 @@ __global__ void __launch_bounds__(kThreads, 2)
     const float sl2 = args.scale_log2;
     bool ok = true;
     int q = 0, u = 0;
-    for (int k = 0; ok; ++k) {
-      int xi;
-      if (!item_of(k, num_items, &xi)) break;
-      const Item it = item_geom(args, xi);
-      if (it.n == 0) continue;
+    while (ok) {
       const int b = q & 1;
+      // the item's record (written by the producer before its Q load) and Q
+      // tile have arrived; n = 0 ends the list
+      ok = mbar_wait(bar(kBarQFull + b), (q >> 1) & 1, abort_flag);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      const int4 rec = *reinterpret_cast<const int4*>(base_ptr + kRecOff + 16 * b);
+      if (rec.w == 0) break;
+      Item it;
+      it.bh = rec.x;
+      it.row0 = rec.y;
+      it.lo = rec.z;
+      it.n = rec.w;
       const int bh = it.bh;
       const int row = it.row0 + (threadIdx.x & 127);
       // keys visible to this row: pos - window < key <= pos (pos = row + kv_off)
@@ -1196,12 +1244,12 @@ __global__ void __launch_bounds__(kThreads, 2)
       const float2 il2 = make_float2(inv_l, inv_l);
       // each warp swizzles its 32 rows into 4 KiB of this item's Q buffer (every
       // QK^T of the item has completed), in the layout of the O map's 128-byte
-      // swizzle, and one lane stores them with a TMA bulk store (rows past Nq
-      // are not written), so the warp does not wait on 32 global stores
+      // swizzle; the producer stores them with TMA bulk stores (rows past Nq
+      // are not written), so the warps wait neither on 32 global stores nor on
+      // the store reading the block
       const int wblk = (warp & 3) * 4096;
       uint8_t* stage_blk = base_ptr + kQOff + b * kTileBytes + wblk;
       uint8_t* stage_row = stage_blk + lane * 128;
-      const int row0 = row - lane;  // first row of this warp
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         uint32_t o[32];
@@ -1218,23 +1266,11 @@ __global__ void __launch_bounds__(kThreads, 2)
           *reinterpret_cast<uint4*>(stage_row + (((4 * c + e) ^ (lane & 7)) * 16)) =
               make_uint4(pko[4 * e], pko[4 * e + 1], pko[4 * e + 2], pko[4 * e + 3]);
       }
-      fence_async_smem();  // the staged rows are visible to the bulk store
-      __syncwarp();
-      if (lane == 0) {
-        tma_store_3d(&tmO, base + kQOff + b * kTileBytes + wblk, 0, row0, bh);
-        bulk_commit_group();
-      }
+      fence_async_smem();  // the staged rows are visible to the producer's bulk store
+      mbar_arrive_warp(bar(kBarOStaged + b));
       if (live) args.lse[static_cast<size_t>(bh) * Nq + row] = lse_row;
-      // once the store has read the staging block, the producer may load the
-      // item after next into buffer b
-      if (lane == 0) bulk_wait_read<0>();
-      __syncwarp();
-      mbar_arrive_warp(bar(kBarQFree + b));
       ++q;
     }
-    // the write-backs' global writes complete before the CTA exits
-    if (lane == 0) bulk_wait<0>();
-    __syncwarp();
   }
 
   tc_fence_before();
