@@ -781,7 +781,10 @@ __global__ void __launch_bounds__(256) fa_merge_splits(const float* __restrict__
 // read, so it overlaps the current tile's last softmax, P.V and write-back.
 //
 // CTA (192 threads): warps 0-3 softmax (thread = row = TMEM lane), warp 4
-// MMA issue and TMEM allocation, warp 5 TMA producer.
+// MMA issue and TMEM allocation, warp 5 TMA producer, which also writes each
+// tile's geometry record for the softmax warps and issues the O write-back
+// stores from the staging block they fill, so neither sits on the softmax
+// warps' path between tiles.
 // Tensor memory (256 columns): S [0,128), O [128,192), P (bf16 pairs) [192,256).
 // Shared memory: two Q buffers, two K and two V stages (16 KiB each).
 namespace pf {
