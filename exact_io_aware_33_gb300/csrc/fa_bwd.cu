@@ -128,6 +128,8 @@ __global__ void __launch_bounds__(256) fa_bwd_pre(const __nv_bfloat16* __restric
                                                   float* __restrict__ dq_acc, int BH) {
   constexpr int kTpr = DV / 8;              // lanes per row (8 or 16)
   constexpr int kRowsPerCta = 256 / kTpr;
+  grid_dep_wait();
+  grid_dep_launch();
   for (int bh = blockIdx.y; bh < BH; bh += gridDim.y) {
   const int sub = threadIdx.x % kTpr;
   const int n = blockIdx.x * kRowsPerCta + threadIdx.x / kTpr;  // < n_pad (grid covers n_pad)
@@ -172,6 +174,8 @@ __global__ void __launch_bounds__(256) fa_bwd_post(const float* __restrict__ acc
                                                    uint4* __restrict__ dq, int N, int n_pad, int BH) {
   constexpr int kTpr = D / 8;
   constexpr int kRowsPerCta = 256 / kTpr;
+  grid_dep_wait();
+  grid_dep_launch();
   const int n = blockIdx.x * kRowsPerCta + threadIdx.x / kTpr;
   if (n >= N) return;
   const int c = (threadIdx.x % kTpr) * 8;
@@ -271,6 +275,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(base_ptr + C::kMiscOff + 4);
   if (base - raw_u32 + C::kLayoutBytes > static_cast<uint32_t>(C::kSmemBytes)) {
     // The dynamic shared memory base is not aligned enough for this layout.
+    grid_dep_wait();
     if (threadIdx.x == 0) atomicExch(args.status, kStatusTimeout);
     return;
   }
@@ -309,6 +314,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  grid_dep_wait();
+  grid_dep_launch();
 
   if (warp == kLoadWarp) {
     // ------------------------------------------------------------ producer
@@ -804,6 +811,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  grid_dep_wait();
+  grid_dep_launch();
   if (warp >= kMmaWarp) regs_decrease<kRegsMma>();
   else if (warp >= kDqWarp0) regs_decrease<kRegsDq>();
 
@@ -1317,10 +1326,10 @@ int launch_pre_d(const Problem& p, const void* o, const float* lse, const void* 
   constexpr int kRowsPerCta = 256 / (DV / 8);
   const int BH = p.B * p.H;
   const dim3 grid(w.n_pad / kRowsPerCta, BH < 65535 ? BH : 65535);
-  fa_bwd_pre<DV, DQ><<<grid, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(o),
-                                           static_cast<const __nv_bfloat16*>(dO), lse, w.Dvec,
-                                           w.lse2, p.N, w.n_pad, w.acc, BH);
-  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+  const cudaError_t e =
+      launch_overlapped(fa_bwd_pre<DV, DQ>, grid, dim3(256), 0, stream, static_cast<const __nv_bfloat16*>(o),
+                        static_cast<const __nv_bfloat16*>(dO), lse, w.Dvec, w.lse2, p.N, w.n_pad, w.acc, BH);
+  return cudaGetLastError() == cudaSuccess && e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
 BwdArgs make_args(const Problem& p, const Workspace& w, void* dk, void* dv, int* status) {
@@ -1349,7 +1358,11 @@ bool launch_seq(long long grid, int slot, const CUtensorMap& mq, const CUtensorM
   using C = wide::BwdCfg<D, DV>;
   auto kern = wide::fa_bwd_main_seq<D, DV, kDrop>;
   if (!ensure_smem_attr(reinterpret_cast<const void*>(kern), C::kSmemBytes, slot)) return false;
-  kern<<<static_cast<unsigned>(grid), wide::kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, mdo, a);
+  if (launch_overlapped(kern, dim3(static_cast<unsigned>(grid)), dim3(wide::kThreads), C::kSmemBytes, stream,
+                        mq, mk, mv, mdo, a) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return false;
+  }
   return true;
 }
 
@@ -1376,7 +1389,11 @@ int launch_main_any(const Problem& p, const void* dO, void* dk, void* dv, void* 
     const int sms = device_sm_count();
     if (sms <= 0) return FA_ERR_LAUNCH;
     const long long g = grid < sms ? grid : sms;
-    kern<<<static_cast<unsigned>(g), pipe::kThreads, pipe::kSmemBytes, stream>>>(mq, mk, mv, mdo, a);
+    if (launch_overlapped(kern, dim3(static_cast<unsigned>(g)), dim3(pipe::kThreads), pipe::kSmemBytes,
+                          stream, mq, mk, mv, mdo, a) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return FA_ERR_LAUNCH;
+    }
   } else if (p.d == 128 && dvh == 128) {
     const bool ok = p.drop.t > 0 ? launch_seq<128, 128, true>(grid, 13, mq, mk, mv, mdo, a, stream)
                                  : launch_seq<128, 128>(grid, 3, mq, mk, mv, mdo, a, stream);
@@ -1419,16 +1436,19 @@ int launch_bwd_post(const Problem& p, void* dq, const void* workspace, cudaStrea
   const Workspace w = carve(p, const_cast<void*>(workspace));
   const int BH = p.B * p.H;
   const unsigned gy = BH < 65535 ? BH : 65535;
+  cudaError_t e = cudaSuccess;
   if (p.d == 64) {
     const dim3 grid((p.N + 31) / 32, gy);
-    fa_bwd_post<64><<<grid, 256, 0, stream>>>(w.acc, static_cast<uint4*>(dq), p.N, w.n_pad, BH);
+    e = launch_overlapped(fa_bwd_post<64>, grid, dim3(256), 0, stream, static_cast<const float*>(w.acc),
+                          static_cast<uint4*>(dq), p.N, w.n_pad, BH);
   } else if (p.d == 128) {
     const dim3 grid((p.N + 15) / 16, gy);
-    fa_bwd_post<128><<<grid, 256, 0, stream>>>(w.acc, static_cast<uint4*>(dq), p.N, w.n_pad, BH);
+    e = launch_overlapped(fa_bwd_post<128>, grid, dim3(256), 0, stream, static_cast<const float*>(w.acc),
+                          static_cast<uint4*>(dq), p.N, w.n_pad, BH);
   } else {
     return FA_ERR_UNSUPPORTED;
   }
-  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+  return cudaGetLastError() == cudaSuccess && e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
 }  // namespace fa

@@ -226,6 +226,8 @@ __global__ void __launch_bounds__(FwdCfg<D, DV, QT>::kThreads, FwdCfg<D, DV, QT>
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  grid_dep_wait();
+  grid_dep_launch();
 
   if (warp == kLoadWarp) {
     // ------------------------------------------------------------ producer
@@ -735,6 +737,8 @@ __global__ void __launch_bounds__(256) fa_merge_splits(const float* __restrict__
                                                        int n_splits) {
   constexpr int kTpr = D / 8;
   constexpr int kRowsPerCta = 256 / kTpr;
+  grid_dep_wait();
+  grid_dep_launch();
   const int row = blockIdx.x * kRowsPerCta + threadIdx.x / kTpr;
   if (row >= Nq) return;
   const int c = (threadIdx.x % kTpr) * 8;
@@ -904,6 +908,8 @@ __global__ void __launch_bounds__(kThreads, 2)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  grid_dep_wait();
+  grid_dep_launch();
 
   // Every role walks the same items; q counts the items with work (their Q
   // buffer is q & 1) and u the key tiles over all of them (one stream step
@@ -1333,8 +1339,9 @@ int launch_fwd_persist(const FwdProblem& p, void* o, float* lse, cudaStream_t st
   const long long items = static_cast<long long>(a.num_pairs) * BH;
   if (items > 0x7fffffffLL) return -1;
   const long long grid = items < 2LL * sms ? items : 2LL * sms;
-  kern<<<static_cast<unsigned>(grid), pf::kThreads, pf::kSmemBytes, stream>>>(mq, mk, mv, mo, a);
-  return cudaGetLastError() == cudaSuccess ? 0 : -3;
+  const cudaError_t e = launch_overlapped(kern, dim3(static_cast<unsigned>(grid)), dim3(pf::kThreads),
+                                          pf::kSmemBytes, stream, mq, mk, mv, mo, a);
+  return cudaGetLastError() == cudaSuccess && e == cudaSuccess ? 0 : -3;
 }
 
 template <int D, int DV, int QT, bool kDrop = false>
@@ -1382,14 +1389,15 @@ int launch_fwd_d(const FwdProblem& p, void* o, float* lse, float* part_o, float*
   const long long gx = static_cast<long long>(a.num_pairs) * BH;
   if (gx > 0x7fffffffLL || n_splits > 65535) return -1;
   const dim3 grid(static_cast<unsigned>(gx), a.split_mode ? n_splits : 1);
-  kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, a);
-  if (cudaGetLastError() != cudaSuccess) return -3;
+  const cudaError_t e = launch_overlapped(kern, grid, dim3(C::kThreads), C::kSmemBytes, stream, mq, mk, mv, a);
+  if (cudaGetLastError() != cudaSuccess || e != cudaSuccess) return -3;
   if (a.split_mode) {
     constexpr int kRowsPerCta = 256 / (DV / 8);
     const dim3 mgrid((p.Nq + kRowsPerCta - 1) / kRowsPerCta, BH < 65535 ? BH : 65535);
-    fa_merge_splits<DV><<<mgrid, 256, 0, stream>>>(part_o, part_lse, static_cast<__nv_bfloat16*>(o),
-                                                   lse, p.Nq, BH, n_splits);
-    if (cudaGetLastError() != cudaSuccess) return -3;
+    const cudaError_t em = launch_overlapped(fa_merge_splits<DV>, mgrid, dim3(256), 0, stream, part_o,
+                                             part_lse, static_cast<__nv_bfloat16*>(o), lse, p.Nq, BH,
+                                             n_splits);
+    if (cudaGetLastError() != cudaSuccess || em != cudaSuccess) return -3;
   }
   return 0;
 }

@@ -65,6 +65,26 @@ int device_sm_count();
 // Sets the dynamic shared memory limit of `func` once per device.
 bool ensure_smem_attr(const void* func, int bytes, int slot);
 
+// Launches `kern` on `stream` with programmatic stream serialization allowed:
+// its CTAs may be scheduled, and run their set-up, while the previous kernel
+// on the stream finishes; each kernel waits for that kernel
+// (griddepcontrol.wait) before it touches global memory.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_overlapped(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem_bytes,
+                              cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem_bytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 int launch_fwd(const Problem& p, void* o, float* lse, cudaStream_t stream);
 // part_o / part_lse == nullptr: one pass over the whole key range writing o and
 // lse; otherwise the key range is split into n_splits parts whose fp32 states

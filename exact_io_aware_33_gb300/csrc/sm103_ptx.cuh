@@ -32,6 +32,21 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// ---------------------------------------------------------------- launch overlap
+// Every kernel of this library is launched with programmatic stream
+// serialization allowed, so its CTAs may start while the kernel before it on
+// the stream is still running. Each kernel calls grid_dep_wait() before its
+// first global-memory access (only shared-memory set-up, tensor-memory
+// allocation and tensor-map prefetches come earlier): it returns once that
+// kernel has completed and its writes are visible (at once when there is no
+// such kernel). grid_dep_launch() then lets the next kernel's CTAs start;
+// because it follows the wait, a kernel never overlaps the one two places
+// before it.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ unsigned long long global_ns() {
   unsigned long long t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
