@@ -1305,6 +1305,464 @@ __global__ void __launch_bounds__(kThreads, 2)
 
 }  // namespace pf
 
+// ---------------------------------------------------------------- persistent two-tile forward
+// d_v = 128 (d = 64 or 128) over the whole key range, without a window: the
+// two-tile CTA above (P over S, O 128 columns per tile), made persistent. A
+// CTA of the two-tile form spends several microseconds outside its key loop
+// (tensor-memory allocation, the first Q and K/V loads with an empty ring,
+// the last P.V, the O write-back) and a grid of a few waves leaves the last
+// one part-empty; both weigh most on short rows (a ragged N = 1000 has 8 key
+// tiles per pair, a causal pair near the diagonal a handful). Here one CTA
+// per SM walks a snake-dealt share of the (pair of query tiles, batch-head)
+// items, heaviest first, keeping the barriers, the K/V ring and the tensor
+// memory across them: the K/V copies run on across item boundaries, the next
+// item's Q is loaded as soon as the current item's last QK^T has completed,
+// and its first QK^T is issued right behind the current item's last P.V, so
+// it computes during the write-back. O is staged for whole-line stores in a
+// block of its own, since the Q buffer holds the next item's Q by then.
+//
+// CTA (320 threads): warps 0-7 softmax (warpgroup t = query tile t; thread =
+// row = TMEM lane), warp 8 MMA issue and TMEM allocation, warp 9 TMA producer.
+// Tensor memory (512 columns): S/P of tile t [128 t, 128 t + 128), O of tile
+// t [256 + 128 t, 384 + 128 t).
+namespace pq {
+
+constexpr int kThreads = 320;
+constexpr int kMmaWarp = 8;
+constexpr int kLoadWarp = 9;
+constexpr int kDV = 128;
+constexpr int kChunkBytes = kBlockM * 64 * 2;  // 16 KiB: 128 rows x 64 bf16, one 128-byte-swizzled chunk
+constexpr int kOStageBytes = 2 * 4 * 4096;      // 4 KiB per softmax warp
+
+template <int D>
+struct Cfg {
+  static constexpr int kChunks = D / 64;
+  static constexpr int kTileBytes = kChunks * kChunkBytes;  // Q or K tile
+  static constexpr int kVTileBytes = 2 * kChunkBytes;       // V tile
+  static constexpr int kStages = D == 64 ? 3 : 2;
+  static constexpr int kQOff = 0;  // tiles 0 and 1
+  static constexpr int kKOff = kQOff + 2 * kTileBytes;
+  static constexpr int kVOff = kKOff + kStages * kTileBytes;
+  static constexpr int kOStageOff = kVOff + kStages * kVTileBytes;
+  static constexpr int kBarOff = kOStageOff + kOStageBytes;
+  static constexpr int kBarQFull = 0;
+  static constexpr int kBarQFree = 1;  // every QK^T of the item has completed
+  static constexpr int kBarKFull = 2;
+  static constexpr int kBarKEmpty = kBarKFull + kStages;
+  static constexpr int kBarVFull = kBarKEmpty + kStages;
+  static constexpr int kBarVEmpty = kBarVFull + kStages;
+  static constexpr int kBarSFull = kBarVEmpty + kStages;  // one per tile
+  static constexpr int kBarPFull = kBarSFull + 2;         // one per tile (4 warps)
+  static constexpr int kBarOFinal = kBarPFull + 2;        // one per tile
+  static constexpr int kBarDrain = kBarOFinal + 2;
+  static constexpr int kNumBars = kBarDrain + 1;
+  static constexpr int kMiscOff = kBarOff + kNumBars * 8;
+  static constexpr int kSmemBytes = kMiscOff + 16 + 1024;  // + slack to align the base
+  static_assert(kSmemBytes <= 232448, "persistent two-tile forward exceeds shared memory");
+  static_assert(kOStageOff % 1024 == 0, "staging blocks need 1 KiB alignment");
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr uint32_t kColO = 256;
+};
+
+// Item x of the heaviest-first list (x / BH counts query-tile pairs from the
+// last, x % BH is the batch-head): its first row and each tile's key tiles
+// (the keys [0, 128 n_t) reach tile t; 0: the tile is past Nq).
+struct Pair {
+  int bh, row0;
+  int n[2];
+};
+__device__ __forceinline__ Pair pair_geom(const FwdArgs& a, int x) {
+  Pair p;
+  p.bh = x % a.BH;
+  p.row0 = (a.num_pairs - 1 - x / a.BH) * 2 * kBlockM;
+  const int n_kv = (a.Nk + kBlockN - 1) / kBlockN;
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    const int r0 = p.row0 + t * kBlockM;
+    int hi = n_kv;
+    if (a.causal) hi = min(hi, (min(r0 + kBlockM, a.Nq) - 1 + a.kv_off) / kBlockN + 1);
+    p.n[t] = (r0 >= a.Nq || hi <= 0) ? 0 : hi;
+  }
+  return p;
+}
+
+// The k-th item of this CTA: round k deals items k*G .. k*G+G-1 to the CTAs,
+// in reverse order on odd rounds, so the per-CTA totals stay balanced.
+__device__ __forceinline__ bool item_of(int k, int num_items, int* x) {
+  const int G = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
+  const int v = k * G + ((k & 1) ? (G - 1 - c) : c);
+  *x = v;
+  return v < num_items;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    fa_fwd_persist2(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV, const FwdArgs args) {
+  using C = Cfg<D>;
+  constexpr int kS = C::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_u32 = smem_u32(smem_raw);
+  const uint32_t base = (raw_u32 + 1023u) & ~1023u;
+  uint8_t* base_ptr = smem_raw + (base - raw_u32);
+  auto bar = [&](int i) -> uint32_t { return base + C::kBarOff + 8u * i; };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base_ptr + C::kMiscOff);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(base_ptr + C::kMiscOff + 4);
+  const int num_items = args.num_pairs * args.BH;
+  const int Nq = args.Nq, Nk = args.Nk;
+  const int warp = warp_id();
+  const int lane = lane_id();
+  // producer: Q loads and K/V copies started (K of stream step g is copy 2 g, its V 2 g + 1)
+  int q_loaded = 0, kv_issued = 0;
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(C::kBarQFull), 1);
+    mbar_init(bar(C::kBarQFree), 1);
+    for (int s = 0; s < kS; ++s) {
+      mbar_init(bar(C::kBarKFull + s), 1);
+      mbar_init(bar(C::kBarKEmpty + s), 1);
+      mbar_init(bar(C::kBarVFull + s), 1);
+      mbar_init(bar(C::kBarVEmpty + s), 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(bar(C::kBarSFull + t), 1);
+      mbar_init(bar(C::kBarPFull + t), 4);  // one arrival per softmax warp
+      mbar_init(bar(C::kBarOFinal + t), 1);
+    }
+    mbar_init(bar(C::kBarDrain), 1);
+    *abort_flag = 0;
+    mbar_fence_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  grid_dep_wait();
+  grid_dep_launch();
+
+  // Every role walks the same items, skipping those without work; g counts
+  // stream steps (one K/V tile each) over all of them and drives the K/V
+  // ring, q counts the items with work (one Q load each).
+  if (warp == kLoadWarp) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_map(&tmQ);
+      tma_prefetch_map(&tmK);
+      tma_prefetch_map(&tmV);
+      bool ok = true;
+      int g = 0, q = 0;
+      for (int k = 0; ok; ++k) {
+        int x;
+        if (!item_of(k, num_items, &x)) break;
+        const Pair it = pair_geom(args, x);
+        const int ns = max(it.n[0], it.n[1]);
+        if (ns == 0) continue;
+        for (int jj = 0; jj < ns && ok; ++jj, ++g) {
+          const int st = g % kS;
+          const uint32_t ph = ((g / kS) + 1) & 1;
+          const int key0 = jj * kBlockN;
+          if (g >= kS) ok = mbar_wait(bar(C::kBarKEmpty + st), ph, abort_flag);
+          if (!ok) break;
+          mbar_arrive_expect_tx(bar(C::kBarKFull + st), C::kTileBytes);
+          for (int c = 0; c < C::kChunks; ++c)
+            tma_load_3d(base + C::kKOff + st * C::kTileBytes + c * kChunkBytes, &tmK,
+                        bar(C::kBarKFull + st), c * 64, key0, it.bh);
+          kv_issued = 2 * g + 1;
+          if (jj == 0) {
+            // this item's Q tiles, once every QK^T of the item before has completed
+            if (q > 0) ok = mbar_wait(bar(C::kBarQFree), (q - 1) & 1, abort_flag);
+            if (!ok) break;
+            mbar_arrive_expect_tx(bar(C::kBarQFull), (it.n[0] > 0 ? C::kTileBytes : 0) +
+                                                         (it.n[1] > 0 ? C::kTileBytes : 0));
+            for (int t = 0; t < 2; ++t) {
+              if (it.n[t] == 0) continue;
+              for (int c = 0; c < C::kChunks; ++c)
+                tma_load_3d(base + C::kQOff + t * C::kTileBytes + c * kChunkBytes, &tmQ, bar(C::kBarQFull),
+                            c * 64, it.row0 + t * kBlockM, it.bh);
+            }
+            q_loaded = ++q;
+          }
+#ifdef FA_TEST_SKIP_ARRIVE
+          // Test-only build (never in libfa.so): the first item's last V tile is
+          // never loaded and nothing more is, so the MMA thread's bounded wait
+          // for it runs out and the CTA winds down through the abort path.
+          if (jj == ns - 1) {
+            ok = false;
+            break;
+          }
+#endif
+          if (g >= kS) ok = mbar_wait(bar(C::kBarVEmpty + st), ph, abort_flag);
+          if (!ok) break;
+          mbar_arrive_expect_tx(bar(C::kBarVFull + st), C::kVTileBytes);
+          for (int c = 0; c < 2; ++c)
+            tma_load_3d(base + C::kVOff + st * C::kVTileBytes + c * kChunkBytes, &tmV,
+                        bar(C::kBarVFull + st), c * 64, key0, it.bh);
+          kv_issued = 2 * g + 2;
+        }
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------ MMA issue
+    // the whole warp runs the issue loop (one elected lane issues)
+    constexpr uint32_t kIdS = idesc_bf16_f32(kBlockM, kBlockN, false, false);
+    constexpr uint32_t kIdO = idesc_bf16_f32(kBlockM, kDV, false, true);
+    // descriptors built once, advanced by byte offsets / 16
+    const uint64_t dQ0 = sdesc_sw128(base + C::kQOff, 16, 1024);
+    const uint64_t dK0 = sdesc_sw128(base + C::kKOff, 16, 1024);
+    const uint64_t dV0 = sdesc_sw128(base + C::kVOff, kChunkBytes, 1024);
+    bool ok = true;
+    int k_ready = -1;  // stream steps whose K tile is known to have landed
+    auto ensure_k = [&](int gs) {
+      if (ok && gs > k_ready) {
+        ok = mbar_wait_w(bar(C::kBarKFull + gs % kS), (gs / kS) & 1, abort_flag);
+        tc_fence_after();
+        k_ready = gs;
+      }
+    };
+    // S_t = Q_t K^T for stream step gs, into tile t's S/P columns
+    auto issue_s = [&](int t, int gs) {
+      const uint64_t qd = dQ0 + static_cast<uint64_t>((t * C::kTileBytes) >> 4);
+      const uint64_t kd = dK0 + static_cast<uint64_t>(((gs % kS) * C::kTileBytes) >> 4);
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint64_t off = static_cast<uint64_t>(((kk >> 2) * kChunkBytes + (kk & 3) * 32) >> 4);
+        mma_ss_w(tmem + t * 128, qd + off, kd + off, kIdS, kk > 0 ? 1u : 0u);
+      }
+      mma_commit_w(bar(C::kBarSFull + t));
+    };
+    // O_t (+)= P_t V for stream step gs; P_t over S_t (bf16 pairs in its first 64 columns)
+    auto issue_pv = [&](int t, int gs, bool first) {
+      const uint64_t vd = dV0 + static_cast<uint64_t>(((gs % kS) * C::kVTileBytes) >> 4);
+#pragma unroll
+      for (int kk = 0; kk < kBlockN / 16; ++kk)
+        mma_ts_w(tmem + C::kColO + t * kDV, tmem + t * 128 + kk * 8, vd + 128 * kk, kIdO,
+                 (!first || kk > 0) ? 1u : 0u);
+    };
+    int g = 0, q = 0;
+    int ut[2] = {0, 0};  // S tiles of tile t over all items (its S/P barrier phases)
+    for (int k = 0; ok; ++k) {
+      int x;
+      if (!item_of(k, num_items, &x)) break;
+      const Pair it = pair_geom(args, x);
+      const int ns = max(it.n[0], it.n[1]);
+      if (ns == 0) continue;
+      // the item's first QK^T: issued behind the previous item's last P.V
+      // (in order on the tensor core, so that P.V has read P before S lands
+      // in the same columns)
+      ok = mbar_wait_w(bar(C::kBarQFull), q & 1, abort_flag);
+      ensure_k(g);
+      if (!ok) break;
+      tc_fence_after();
+#pragma unroll
+      for (int t = 0; t < 2; ++t)
+        if (it.n[t] > 0) issue_s(t, g);
+      mma_commit_w(bar(C::kBarKEmpty + g % kS));
+      if (ns == 1) mma_commit_w(bar(C::kBarQFree));
+      for (int jj = 0; jj < ns && ok; ++jj) {
+        const int gs = g + jj;
+        ok = mbar_wait_w(bar(C::kBarVFull + gs % kS), (gs / kS) & 1, abort_flag);
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          if (!ok || jj >= it.n[t]) continue;
+          ok = mbar_wait_w(bar(C::kBarPFull + t), ut[t] & 1, abort_flag);
+          if (!ok) break;
+          tc_fence_after();
+          issue_pv(t, gs, jj == 0);
+          ++ut[t];
+          if (jj + 1 < it.n[t]) {
+            ensure_k(gs + 1);
+            if (!ok) break;
+            issue_s(t, gs + 1);
+          } else {
+            mma_commit_w(bar(C::kBarOFinal + t));
+          }
+        }
+        if (!ok) break;
+        // every QK^T of the item has been issued: its Q buffer is free once they complete
+        if (jj == ns - 2) mma_commit_w(bar(C::kBarQFree));
+        mma_commit_w(bar(C::kBarVEmpty + gs % kS));
+        if (jj + 1 < ns) mma_commit_w(bar(C::kBarKEmpty + (gs + 1) % kS));
+      }
+      g += ns;
+      ++q;
+    }
+    // Let every MMA this warp issued finish before TMEM is released.
+    mma_commit_w(bar(C::kBarDrain));
+    mbar_wait_w(bar(C::kBarDrain), 0, nullptr);
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int t = warp / 4;  // query tile
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + lane_base + t * 128;
+    const uint32_t tO = tmem + lane_base + C::kColO + t * kDV;
+    const float sl2 = args.scale_log2;
+    const float2 sl2x2 = make_float2(sl2, sl2);
+    // this warp's staging block: 32 rows x 64 columns of O, 128-byte rows
+    uint8_t* stage_blk = base_ptr + C::kOStageOff + (warp & 7) * 4096;
+    uint8_t* stage_row = stage_blk + lane * 128;
+    bool ok = true;
+    int ut = 0, qt = 0;  // S tiles and items of this query tile so far
+    for (int k = 0; ok; ++k) {
+      int x;
+      if (!item_of(k, num_items, &x)) break;
+      const Pair it = pair_geom(args, x);
+      const int n_mine = it.n[t];
+      if (n_mine == 0) continue;
+      const int bh = it.bh;
+      const int tile_row0 = it.row0 + t * kBlockM;
+      const int row = tile_row0 + (threadIdx.x & 127);
+      // keys visible to this row: key <= pos (pos = row + kv_off) when causal
+      const int key_hi = args.causal ? min(Nk, row + args.kv_off + 1) : Nk;  // exclusive
+      float m_ref = -INFINITY;  // log2-domain reference maximum
+      float l = 0.f;
+      for (int u = 0; u < n_mine; ++u, ++ut) {
+        const int key0 = u * kBlockN;
+        ok = mbar_wait(bar(C::kBarSFull + t), ut & 1, abort_flag);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t sr[4][32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, sr[c]);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld_wait(sr[c]);
+        float xs[128];
+#pragma unroll
+        for (int c = 0; c < 128; ++c) xs[c] = __uint_as_float(sr[c >> 5][c & 31]);
+        // only the causal boundary tiles and the ragged last tile need a mask
+        if ((args.causal && key0 + kBlockN - 1 > tile_row0 + args.kv_off) || key0 + kBlockN > Nk) {
+          const int lim = key_hi - key0;
+#pragma unroll
+          for (int c = 0; c < 128; ++c)
+            if (c >= lim) xs[c] = -INFINITY;
+        }
+        const float m_tile = max3(fmaxf(max32(xs), max32(xs + 32)), max32(xs + 64), max32(xs + 96)) * sl2;
+        const bool need = m_tile > m_ref + kRescaleThreshold;
+        const float m_old = m_ref;
+        if (need) m_ref = m_tile;
+        const float alpha = need ? ex2(m_old - m_ref) : 1.0f;
+        const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
+        // p = exp2(s * scale * log2(e) - m_ref), packed two at a time; P
+        // columns [32 h, 32 h + 32) hold scores [64 h, 64 h + 64), over S
+        const float2 negm = make_float2(-m_use, -m_use);
+        float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+        uint32_t pk[32];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const int e = 64 * h + 2 * c;
+            const float2 a = __ffma2_rn(make_float2(xs[e], xs[e + 1]), sl2x2, negm);
+            const float2 pr = make_float2(ex2(a.x), ex2(a.y));
+            if (c & 1) acc1 = __fadd2_rn(acc1, pr);
+            else acc0 = __fadd2_rn(acc0, pr);
+            pk[c] = pack_bf16(pr.x, pr.y);
+          }
+          tmem_st32(tS + 32 * h, pk);
+        }
+        l = alpha * l + ((acc0.x + acc0.y) + (acc1.x + acc1.y));
+        // Rescale the accumulator when this warp's maximum moved. O is
+        // settled: this S was committed after the tile's previous P.V.
+        if (u > 0 && __any_sync(0xffffffffu, need)) {
+#pragma unroll
+          for (int c = 0; c < kDV / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld32(tO + c * 32, o);
+            tmem_ld_wait(o);
+            const float2 al2 = make_float2(alpha, alpha);
+#pragma unroll
+            for (int e = 0; e < 32; e += 2) {
+              const float2 v = __fmul2_rn(make_float2(__uint_as_float(o[e]), __uint_as_float(o[e + 1])), al2);
+              o[e] = __float_as_uint(v.x);
+              o[e + 1] = __float_as_uint(v.y);
+            }
+            tmem_st32(tO + c * 32, o);
+          }
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive_warp(bar(C::kBarPFull + t));
+      }
+      if (!ok) break;
+      // write-back once the item's last P.V for this tile has completed; the
+      // tile's next P.V (next item) waits for this warpgroup's next P, so O is
+      // read out before it is overwritten
+      ok = mbar_wait(bar(C::kBarOFinal + t), qt & 1, abort_flag);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      const float inv_l = l > 0.f ? 1.0f / l : 0.f;
+      const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
+      const float lse_row = l > 0.f ? (m_use + log2f(l)) * kLn2 : -INFINITY;
+      const float2 il2 = make_float2(inv_l, inv_l);
+      // each warp swizzles its 32 rows, 64 columns at a time, into its staging
+      // block and writes them back as four whole lines per instruction
+      __nv_bfloat16* obase = args.o + static_cast<size_t>(bh) * Nq * kDV;
+      const int wrow0 = row - lane;  // first row of this warp
+#pragma unroll
+      for (int h = 0; h < kDV / 64; ++h) {
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tO + h * 64 + c * 32, o);
+          tmem_ld_wait(o);
+          uint32_t pko[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const float2 v = __fmul2_rn(make_float2(__uint_as_float(o[2 * e]), __uint_as_float(o[2 * e + 1])), il2);
+            pko[e] = pack_bf16(v.x, v.y);
+          }
+          // 16-byte chunks 4c..4c+3 of row `lane`, chunk v in slot v ^ (lane & 7)
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            *reinterpret_cast<uint4*>(stage_row + (((4 * c + e) ^ (lane & 7)) * 16)) =
+                make_uint4(pko[4 * e], pko[4 * e + 1], pko[4 * e + 2], pko[4 * e + 3]);
+        }
+        __syncwarp();
+        // instruction j: lanes 8r'..8r'+7 write the eight chunks of row 4j + r'
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int r = 4 * j + (lane >> 3), v = lane & 7;
+          const uint4 val = *reinterpret_cast<const uint4*>(stage_blk + r * 128 + ((v ^ (r & 7)) * 16));
+          if (wrow0 + r < Nq)
+            *reinterpret_cast<uint4*>(obase + static_cast<size_t>(wrow0 + r) * kDV + h * 64 + v * 8) = val;
+        }
+        __syncwarp();  // the block is read back before it is written again
+      }
+      if (row < Nq) args.lse[static_cast<size_t>(bh) * Nq + row] = lse_row;
+      ++qt;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kLoadWarp && lane == 0 && *abort_flag) {
+    // Every role has stopped, so the flag is final: let every copy this thread
+    // started land before the CTA exits (only the last Q load and the last
+    // 2 x stages K/V copies can still be pending: each Q load waits for the
+    // item before to have been consumed, and each ring slot for its last use).
+    if (q_loaded > 0) mbar_wait(bar(C::kBarQFull), (q_loaded - 1) & 1, nullptr);
+    for (int c = kv_issued - 1; c >= 0 && c >= kv_issued - 2 * kS; --c) {
+      const int gg = c >> 1, st = gg % kS;
+      mbar_wait(bar(((c & 1) ? C::kBarVFull : C::kBarKFull) + st), (gg / kS) & 1, nullptr);
+    }
+  }
+  if (warp == kMmaWarp) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+  if (threadIdx.x == 0 && *abort_flag) atomicExch(args.status, kStatusTimeout);
+}
+
+}  // namespace pq
+
 // The persistent one-tile forward (d = d_v = 64, whole key range): at most two
 // CTAs per SM, each walking its share of the query tiles.
 template <bool kDrop>
@@ -1341,6 +1799,46 @@ int launch_fwd_persist(const FwdProblem& p, void* o, float* lse, cudaStream_t st
   const long long grid = items < 2LL * sms ? items : 2LL * sms;
   const cudaError_t e = launch_overlapped(kern, dim3(static_cast<unsigned>(grid)), dim3(pf::kThreads),
                                           pf::kSmemBytes, stream, mq, mk, mv, mo, a);
+  return cudaGetLastError() == cudaSuccess && e == cudaSuccess ? 0 : -3;
+}
+
+// The persistent two-tile forward (d_v = 128, whole key range, no window): one
+// CTA per SM walks its share of the query-tile pairs.
+template <int D>
+int launch_fwd_persist2(const FwdProblem& p, void* o, float* lse, cudaStream_t stream) {
+  using C = pq::Cfg<D>;
+  const int BH = p.B * p.H;
+  CUtensorMap mq, mk, mv;
+  if (!make_map_bhnd(&mq, p.q, BH, p.Nq, D) || !make_map_bhnd(&mk, p.k, BH, p.Nk, D) ||
+      !make_map_bhnd(&mv, p.v, BH, p.Nk, pq::kDV))
+    return -3;
+  int* status = device_status_word();
+  const int sms = device_sm_count();
+  if (!status || sms <= 0) return -3;
+  auto kern = pq::fa_fwd_persist2<D>;
+  // attribute slots 17 and 18 (the other kernels use 0-16)
+  if (!ensure_smem_attr(reinterpret_cast<const void*>(kern), C::kSmemBytes, D == 128 ? 17 : 18)) return -3;
+  FwdArgs a{};
+  a.o = static_cast<__nv_bfloat16*>(o);
+  a.lse = lse;
+  a.status = status;
+  a.Nq = p.Nq;
+  a.Nk = p.Nk;
+  a.kv_off = p.Nk - p.Nq;
+  a.window = 0;
+  a.BH = BH;
+  a.causal = p.causal ? 1 : 0;
+  a.num_pairs = (p.Nq + 2 * kBlockM - 1) / (2 * kBlockM);
+  a.split_tiles = (p.Nk + kBlockN - 1) / kBlockN;
+  a.split_mode = 0;
+  const float sl2 = p.scale * 1.4426950408889634f;
+  a.scale_log2 = sl2 > 1e-30f ? sl2 : 1e-30f;
+  a.drop = p.drop;
+  const long long items = static_cast<long long>(a.num_pairs) * BH;
+  if (items > 0x7fffffffLL) return -1;
+  const long long grid = items < sms ? items : sms;
+  const cudaError_t e = launch_overlapped(kern, dim3(static_cast<unsigned>(grid)), dim3(pq::kThreads),
+                                          C::kSmemBytes, stream, mq, mk, mv, a);
   return cudaGetLastError() == cudaSuccess && e == cudaSuccess ? 0 : -3;
 }
 
@@ -1452,11 +1950,21 @@ int launch_fwd_general(const FwdProblem& p, void* o, float* lse, float* part_o, 
       return launch_fwd_persist<false>(p, o, lse, stream);
     return launch_fwd_d<64, 64, 2>(p, o, lse, part_o, part_lse, n_splits, stream);
   }
-  if (p.d == 128 && p.dv == 128) return launch_fwd_d<128, 128, 2>(p, o, lse, part_o, part_lse, n_splits, stream);
+  // d_v = 128 over the whole key range without a window (and no query
+  // before the first key when causal): two query tiles at a time, one
+  // persistent CTA per SM
+  const bool persist2 = part_o == nullptr && p.window == 0 && (!p.causal || p.Nk >= p.Nq);
+  if (p.d == 128 && p.dv == 128) {
+    if (persist2) return launch_fwd_persist2<128>(p, o, lse, stream);
+    return launch_fwd_d<128, 128, 2>(p, o, lse, part_o, part_lse, n_splits, stream);
+  }
   // d = d_v = 256: one query tile per CTA (S 128 + O 256 tensor-memory columns)
   if (p.d == 256 && p.dv == 256) return launch_fwd_d<256, 256, 1>(p, o, lse, part_o, part_lse, n_splits, stream);
   if (p.d == 128 && p.dv == 64) return launch_fwd_d<128, 64, 2>(p, o, lse, part_o, part_lse, n_splits, stream);
-  if (p.d == 64 && p.dv == 128) return launch_fwd_d<64, 128, 2>(p, o, lse, part_o, part_lse, n_splits, stream);
+  if (p.d == 64 && p.dv == 128) {
+    if (persist2) return launch_fwd_persist2<64>(p, o, lse, stream);
+    return launch_fwd_d<64, 128, 2>(p, o, lse, part_o, part_lse, n_splits, stream);
+  }
   return -2;
 }
 
