@@ -1306,13 +1306,14 @@ __global__ void __launch_bounds__(kThreads, 2)
 }  // namespace pf
 
 // ---------------------------------------------------------------- persistent two-tile forward
-// d_v = 128 (d = 64 or 128) over the whole key range, without a window: the
-// two-tile CTA above (P over S, O 128 columns per tile), made persistent. A
-// CTA of the two-tile form spends several microseconds outside its key loop
-// (tensor-memory allocation, the first Q and K/V loads with an empty ring,
-// the last P.V, the O write-back) and a grid of a few waves leaves the last
-// one part-empty; both weigh most on short rows (a ragged N = 1000 has 8 key
-// tiles per pair, a causal pair near the diagonal a handful). Here one CTA
+// d_v = 128 (d = 64 or 128) over the whole key range, with or without a
+// window: the two-tile CTA above (P over S, O 128 columns per tile), made
+// persistent. A CTA of the two-tile form spends several microseconds outside
+// its key loop (tensor-memory allocation, the first Q and K/V loads with an
+// empty ring, the last P.V, the O write-back) and a grid of a few waves
+// leaves the last one part-empty; both weigh most on short rows (a ragged
+// N = 1000 has 8 key tiles per pair, a causal pair near the diagonal or a
+// window of 1024 keys a handful). Here one CTA
 // per SM walks a snake-dealt share of the (pair of query tiles, batch-head)
 // items, heaviest first, keeping the barriers, the K/V ring and the tensor
 // memory across them: the K/V copies run on across item boundaries, the next
@@ -1365,24 +1366,40 @@ struct Cfg {
 };
 
 // Item x of the heaviest-first list (x / BH counts query-tile pairs from the
-// last, x % BH is the batch-head): its first row and each tile's key tiles
-// (the keys [0, 128 n_t) reach tile t; 0: the tile is past Nq).
+// last, x % BH is the batch-head): its first row and the key tiles of each
+// tile, [lo_t, lo_t + n_t) (the causal limit of its last row, the window's
+// start for its first row; n_t = 0: the tile is past Nq). The item streams
+// the union of the two ranges, key tiles [j0, j0 + ns); tile t takes part in
+// stream steps [a_t, a_t + n_t), a_t = lo_t - j0.
 struct Pair {
   int bh, row0;
-  int n[2];
+  int n[2], a[2];
+  int j0, ns;
 };
 __device__ __forceinline__ Pair pair_geom(const FwdArgs& a, int x) {
   Pair p;
   p.bh = x % a.BH;
   p.row0 = (a.num_pairs - 1 - x / a.BH) * 2 * kBlockM;
   const int n_kv = (a.Nk + kBlockN - 1) / kBlockN;
+  int lo[2];
 #pragma unroll
   for (int t = 0; t < 2; ++t) {
     const int r0 = p.row0 + t * kBlockM;
-    int hi = n_kv;
+    int l = 0, hi = n_kv;
     if (a.causal) hi = min(hi, (min(r0 + kBlockM, a.Nq) - 1 + a.kv_off) / kBlockN + 1);
-    p.n[t] = (r0 >= a.Nq || hi <= 0) ? 0 : hi;
+    if (a.window) {
+      const int first_key = r0 + a.kv_off - a.window + 1;
+      if (first_key > 0) l = first_key / kBlockN;
+    }
+    lo[t] = l;
+    p.n[t] = (r0 >= a.Nq || hi <= l) ? 0 : hi - l;
   }
+  // tile 1 starts no earlier than tile 0 and ends no earlier, when both have keys
+  p.j0 = p.n[0] > 0 ? lo[0] : lo[1];
+  const int end = max(p.n[0] > 0 ? lo[0] + p.n[0] : 0, p.n[1] > 0 ? lo[1] + p.n[1] : 0);
+  p.ns = p.n[0] + p.n[1] > 0 ? end - p.j0 : 0;
+#pragma unroll
+  for (int t = 0; t < 2; ++t) p.a[t] = lo[t] - p.j0;
   return p;
 }
 
@@ -1459,12 +1476,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         int x;
         if (!item_of(k, num_items, &x)) break;
         const Pair it = pair_geom(args, x);
-        const int ns = max(it.n[0], it.n[1]);
+        const int ns = it.ns;
         if (ns == 0) continue;
         for (int jj = 0; jj < ns && ok; ++jj, ++g) {
           const int st = g % kS;
           const uint32_t ph = ((g / kS) + 1) & 1;
-          const int key0 = jj * kBlockN;
+          const int key0 = (it.j0 + jj) * kBlockN;
           if (g >= kS) ok = mbar_wait(bar(C::kBarKEmpty + st), ph, abort_flag);
           if (!ok) break;
           mbar_arrive_expect_tx(bar(C::kBarKFull + st), C::kTileBytes);
@@ -1548,7 +1565,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int x;
       if (!item_of(k, num_items, &x)) break;
       const Pair it = pair_geom(args, x);
-      const int ns = max(it.n[0], it.n[1]);
+      const int ns = it.ns;
       if (ns == 0) continue;
       // the item's first QK^T: issued behind the previous item's last P.V
       // (in order on the tensor core, so that P.V has read P before S lands
@@ -1559,7 +1576,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
 #pragma unroll
       for (int t = 0; t < 2; ++t)
-        if (it.n[t] > 0) issue_s(t, g);
+        if (it.n[t] > 0 && it.a[t] == 0) issue_s(t, g);
       mma_commit_w(bar(C::kBarKEmpty + g % kS));
       if (ns == 1) mma_commit_w(bar(C::kBarQFree));
       for (int jj = 0; jj < ns && ok; ++jj) {
@@ -1569,19 +1586,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
-          if (!ok || jj >= it.n[t]) continue;
+          const int u = jj - it.a[t];  // tile-local step
+          if (!ok || u < 0 || u >= it.n[t]) continue;
           ok = mbar_wait_w(bar(C::kBarPFull + t), ut[t] & 1, abort_flag);
           if (!ok) break;
           tc_fence_after();
-          issue_pv(t, gs, jj == 0);
+          issue_pv(t, gs, u == 0);
           ++ut[t];
-          if (jj + 1 < it.n[t]) {
+          if (u + 1 < it.n[t]) {
             ensure_k(gs + 1);
             if (!ok) break;
             issue_s(t, gs + 1);
           } else {
             mma_commit_w(bar(C::kBarOFinal + t));
           }
+        }
+        if (!ok) break;
+        // a tile whose range starts at the next step (a window's later start)
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          if (!ok || it.n[t] == 0 || it.a[t] != jj + 1) continue;
+          ensure_k(gs + 1);
+          if (!ok) break;
+          issue_s(t, gs + 1);
         }
         if (!ok) break;
         // every QK^T of the item has been issued: its Q buffer is free once they complete
@@ -1617,12 +1644,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int bh = it.bh;
       const int tile_row0 = it.row0 + t * kBlockM;
       const int row = tile_row0 + (threadIdx.x & 127);
-      // keys visible to this row: key <= pos (pos = row + kv_off) when causal
-      const int key_hi = args.causal ? min(Nk, row + args.kv_off + 1) : Nk;  // exclusive
+      // keys visible to this row: pos - window < key <= pos (pos = row + kv_off)
+      const int pos = row + args.kv_off;
+      const int key_hi = args.causal ? min(Nk, pos + 1) : Nk;          // exclusive
+      const int key_lo = args.window ? pos - args.window + 1 : -(1 << 30);
+      const int key_tile0 = it.j0 + it.a[t];  // this tile's first key tile
       float m_ref = -INFINITY;  // log2-domain reference maximum
       float l = 0.f;
       for (int u = 0; u < n_mine; ++u, ++ut) {
-        const int key0 = u * kBlockN;
+        const int key0 = (key_tile0 + u) * kBlockN;
         ok = mbar_wait(bar(C::kBarSFull + t), ut & 1, abort_flag);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
@@ -1635,12 +1665,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         float xs[128];
 #pragma unroll
         for (int c = 0; c < 128; ++c) xs[c] = __uint_as_float(sr[c >> 5][c & 31]);
-        // only the causal boundary tiles and the ragged last tile need a mask
-        if ((args.causal && key0 + kBlockN - 1 > tile_row0 + args.kv_off) || key0 + kBlockN > Nk) {
-          const int lim = key_hi - key0;
+        if (args.window == 0) {
+          // only the causal boundary tiles and the ragged last tile need a mask
+          if ((args.causal && key0 + kBlockN - 1 > tile_row0 + args.kv_off) || key0 + kBlockN > Nk) {
+            const int lim = key_hi - key0;
 #pragma unroll
-          for (int c = 0; c < 128; ++c)
-            if (c >= lim) xs[c] = -INFINITY;
+            for (int c = 0; c < 128; ++c)
+              if (c >= lim) xs[c] = -INFINITY;
+          }
+        } else {
+          const int lim_hi = key_hi - key0, lim_lo = key_lo - key0;
+          if (lim_hi < kBlockN || lim_lo > 0) {
+#pragma unroll
+            for (int c = 0; c < 128; ++c)
+              if (c >= lim_hi || c < lim_lo) xs[c] = -INFINITY;
+          }
         }
         const float m_tile = max3(fmaxf(max32(xs), max32(xs + 32)), max32(xs + 64), max32(xs + 96)) * sl2;
         const bool need = m_tile > m_ref + kRescaleThreshold;
@@ -1802,7 +1841,7 @@ int launch_fwd_persist(const FwdProblem& p, void* o, float* lse, cudaStream_t st
   return cudaGetLastError() == cudaSuccess && e == cudaSuccess ? 0 : -3;
 }
 
-// The persistent two-tile forward (d_v = 128, whole key range, no window): one
+// The persistent two-tile forward (d_v = 128, whole key range): one
 // CTA per SM walks its share of the query-tile pairs.
 template <int D>
 int launch_fwd_persist2(const FwdProblem& p, void* o, float* lse, cudaStream_t stream) {
@@ -1825,7 +1864,7 @@ int launch_fwd_persist2(const FwdProblem& p, void* o, float* lse, cudaStream_t s
   a.Nq = p.Nq;
   a.Nk = p.Nk;
   a.kv_off = p.Nk - p.Nq;
-  a.window = 0;
+  a.window = p.window;
   a.BH = BH;
   a.causal = p.causal ? 1 : 0;
   a.num_pairs = (p.Nq + 2 * kBlockM - 1) / (2 * kBlockM);
@@ -1950,10 +1989,9 @@ int launch_fwd_general(const FwdProblem& p, void* o, float* lse, float* part_o, 
       return launch_fwd_persist<false>(p, o, lse, stream);
     return launch_fwd_d<64, 64, 2>(p, o, lse, part_o, part_lse, n_splits, stream);
   }
-  // d_v = 128 over the whole key range without a window (and no query
-  // before the first key when causal): two query tiles at a time, one
-  // persistent CTA per SM
-  const bool persist2 = part_o == nullptr && p.window == 0 && (!p.causal || p.Nk >= p.Nq);
+  // d_v = 128 over the whole key range (and no query before the first key
+  // when causal): two query tiles at a time, one persistent CTA per SM
+  const bool persist2 = part_o == nullptr && (!p.causal || p.Nk >= p.Nq);
   if (p.d == 128 && p.dv == 128) {
     if (persist2) return launch_fwd_persist2<128>(p, o, lse, stream);
     return launch_fwd_d<128, 128, 2>(p, o, lse, part_o, part_lse, n_splits, stream);
