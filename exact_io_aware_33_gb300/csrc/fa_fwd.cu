@@ -1331,15 +1331,21 @@ namespace pq {
 constexpr int kThreads = 320;
 constexpr int kMmaWarp = 8;
 constexpr int kLoadWarp = 9;
-constexpr int kDV = 128;
 constexpr int kChunkBytes = kBlockM * 64 * 2;  // 16 KiB: 128 rows x 64 bf16, one 128-byte-swizzled chunk
 constexpr int kOStageBytes = 2 * 4 * 4096;      // 4 KiB per softmax warp
 
-template <int D>
+// DV = 128: S/P of tile t in [128 t, 128 t + 128) (P over S), O of tile t in
+// [256 + 128 t, 384 + 128 t). DV = 64: S of tile t in [128 t, 128 t + 128), O
+// in [256 + 64 t, 320 + 64 t), P in [384 + 64 t, 448 + 64 t): with P in
+// columns of its own the softmax releases S as soon as it has loaded it, and
+// the tile's next QK^T computes while it forms P.
+template <int D, int DV>
 struct Cfg {
   static constexpr int kChunks = D / 64;
-  static constexpr int kTileBytes = kChunks * kChunkBytes;  // Q or K tile
-  static constexpr int kVTileBytes = 2 * kChunkBytes;       // V tile
+  static constexpr int kChunksV = DV / 64;
+  static constexpr int kTileBytes = kChunks * kChunkBytes;    // Q or K tile
+  static constexpr int kVTileBytes = kChunksV * kChunkBytes;  // V tile
+  static constexpr bool kSepP = DV == 64;
   static constexpr int kStages = D == 64 ? 3 : 2;
   static constexpr int kQOff = 0;  // tiles 0 and 1
   static constexpr int kKOff = kQOff + 2 * kTileBytes;
@@ -1354,8 +1360,10 @@ struct Cfg {
   static constexpr int kBarVEmpty = kBarVFull + kStages;
   static constexpr int kBarSFull = kBarVEmpty + kStages;  // one per tile
   static constexpr int kBarPFull = kBarSFull + 2;         // one per tile (4 warps)
-  static constexpr int kBarOFinal = kBarPFull + 2;        // one per tile
-  static constexpr int kBarDrain = kBarOFinal + 2;
+  static constexpr int kBarOFinal = kBarPFull + 2;        // one per tile (P over S)
+  static constexpr int kBarSFree = kBarOFinal + 2;        // one per tile (4 warps; separate P)
+  static constexpr int kBarPVDone = kBarSFree + 2;        // one per tile (separate P)
+  static constexpr int kBarDrain = kBarPVDone + 2;
   static constexpr int kNumBars = kBarDrain + 1;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kSmemBytes = kMiscOff + 16 + 1024;  // + slack to align the base
@@ -1363,6 +1371,8 @@ struct Cfg {
   static_assert(kOStageOff % 1024 == 0, "staging blocks need 1 KiB alignment");
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColO = 256;
+  static constexpr uint32_t kColP = kColO + 2 * DV;  // separate P only
+  static_assert(!kSepP || kColP + 128 <= kTmemCols, "two-tile forward exceeds tensor memory");
 };
 
 // Item x of the heaviest-first list (x / BH counts query-tile pairs from the
@@ -1412,11 +1422,11 @@ __device__ __forceinline__ bool item_of(int k, int num_items, int* x) {
   return v < num_items;
 }
 
-template <int D>
+template <int D, int DV>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_persist2(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const FwdArgs args) {
-  using C = Cfg<D>;
+  using C = Cfg<D, DV>;
   constexpr int kS = C::kStages;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_u32 = smem_u32(smem_raw);
@@ -1445,6 +1455,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(C::kBarSFull + t), 1);
       mbar_init(bar(C::kBarPFull + t), 4);  // one arrival per softmax warp
       mbar_init(bar(C::kBarOFinal + t), 1);
+      mbar_init(bar(C::kBarSFree + t), 4);
+      mbar_init(bar(C::kBarPVDone + t), 1);
     }
     mbar_init(bar(C::kBarDrain), 1);
     *abort_flag = 0;
@@ -1515,7 +1527,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (g >= kS) ok = mbar_wait(bar(C::kBarVEmpty + st), ph, abort_flag);
           if (!ok) break;
           mbar_arrive_expect_tx(bar(C::kBarVFull + st), C::kVTileBytes);
-          for (int c = 0; c < 2; ++c)
+          for (int c = 0; c < C::kChunksV; ++c)
             tma_load_3d(base + C::kVOff + st * C::kVTileBytes + c * kChunkBytes, &tmV,
                         bar(C::kBarVFull + st), c * 64, key0, it.bh);
           kv_issued = 2 * g + 2;
@@ -1526,7 +1538,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ MMA issue
     // the whole warp runs the issue loop (one elected lane issues)
     constexpr uint32_t kIdS = idesc_bf16_f32(kBlockM, kBlockN, false, false);
-    constexpr uint32_t kIdO = idesc_bf16_f32(kBlockM, kDV, false, true);
+    constexpr uint32_t kIdO = idesc_bf16_f32(kBlockM, DV, false, true);
     // descriptors built once, advanced by byte offsets / 16
     const uint64_t dQ0 = sdesc_sw128(base + C::kQOff, 16, 1024);
     const uint64_t dK0 = sdesc_sw128(base + C::kKOff, 16, 1024);
@@ -1551,73 +1563,135 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       mma_commit_w(bar(C::kBarSFull + t));
     };
-    // O_t (+)= P_t V for stream step gs; P_t over S_t (bf16 pairs in its first 64 columns)
+    // O_t (+)= P_t V for stream step gs; P_t (bf16 pairs, 64 columns) over
+    // S_t or in its own columns
     auto issue_pv = [&](int t, int gs, bool first) {
       const uint64_t vd = dV0 + static_cast<uint64_t>(((gs % kS) * C::kVTileBytes) >> 4);
+      const uint32_t pcol = C::kSepP ? C::kColP + t * 64 : t * 128;
 #pragma unroll
       for (int kk = 0; kk < kBlockN / 16; ++kk)
-        mma_ts_w(tmem + C::kColO + t * kDV, tmem + t * 128 + kk * 8, vd + 128 * kk, kIdO,
+        mma_ts_w(tmem + C::kColO + t * DV, tmem + pcol + kk * 8, vd + 128 * kk, kIdO,
                  (!first || kk > 0) ? 1u : 0u);
     };
     int g = 0, q = 0;
     int ut[2] = {0, 0};  // S tiles of tile t over all items (its S/P barrier phases)
-    for (int k = 0; ok; ++k) {
-      int x;
-      if (!item_of(k, num_items, &x)) break;
-      const Pair it = pair_geom(args, x);
-      const int ns = it.ns;
-      if (ns == 0) continue;
-      // the item's first QK^T: issued behind the previous item's last P.V
-      // (in order on the tensor core, so that P.V has read P before S lands
-      // in the same columns)
-      ok = mbar_wait_w(bar(C::kBarQFull), q & 1, abort_flag);
-      ensure_k(g);
-      if (!ok) break;
-      tc_fence_after();
+    if constexpr (C::kSepP) {
+      int s_iss[2] = {0, 0};  // S tiles issued per tile
+      // S_t for stream step gs once the tile's previous S is in the softmax's registers
+      auto next_s = [&](int t, int gs) {
+        if (s_iss[t] > 0) ok = mbar_wait_w(bar(C::kBarSFree + t), (s_iss[t] - 1) & 1, abort_flag);
+        ensure_k(gs);
+        if (!ok) return;
+        tc_fence_after();
+        issue_s(t, gs);
+        ++s_iss[t];
+      };
+      for (int k = 0; ok; ++k) {
+        int x;
+        if (!item_of(k, num_items, &x)) break;
+        const Pair it = pair_geom(args, x);
+        const int ns = it.ns;
+        if (ns == 0) continue;
+        ok = mbar_wait_w(bar(C::kBarQFull), q & 1, abort_flag);
 #pragma unroll
-      for (int t = 0; t < 2; ++t)
-        if (it.n[t] > 0 && it.a[t] == 0) issue_s(t, g);
-      mma_commit_w(bar(C::kBarKEmpty + g % kS));
-      if (ns == 1) mma_commit_w(bar(C::kBarQFree));
-      for (int jj = 0; jj < ns && ok; ++jj) {
-        const int gs = g + jj;
-        ok = mbar_wait_w(bar(C::kBarVFull + gs % kS), (gs / kS) & 1, abort_flag);
+        for (int t = 0; t < 2; ++t)
+          if (ok && it.n[t] > 0 && it.a[t] == 0) next_s(t, g);
+        if (!ok) break;
+        mma_commit_w(bar(C::kBarKEmpty + g % kS));
+        if (ns == 1) mma_commit_w(bar(C::kBarQFree));
+        for (int jj = 0; jj < ns && ok; ++jj) {
+          const int gs = g + jj;
+          // the next step's QK^T first, so that it computes while the softmax forms P
+          if (jj + 1 < ns) {
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+              const int u1 = jj + 1 - it.a[t];
+              if (ok && u1 >= 0 && u1 < it.n[t]) next_s(t, gs + 1);
+            }
+            if (!ok) break;
+            // every QK^T of the item has been issued: its Q buffer is free once they complete
+            if (jj == ns - 2) mma_commit_w(bar(C::kBarQFree));
+            mma_commit_w(bar(C::kBarKEmpty + (gs + 1) % kS));
+          }
+          ok = mbar_wait_w(bar(C::kBarVFull + gs % kS), (gs / kS) & 1, abort_flag);
+          if (!ok) break;
+          tc_fence_after();
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            const int u = jj - it.a[t];
+            if (!ok || u < 0 || u >= it.n[t]) continue;
+            ok = mbar_wait_w(bar(C::kBarPFull + t), ut[t] & 1, abort_flag);
+            if (!ok) break;
+            tc_fence_after();
+            issue_pv(t, gs, u == 0);
+            mma_commit_w(bar(C::kBarPVDone + t));
+            ++ut[t];
+          }
+          if (!ok) break;
+          mma_commit_w(bar(C::kBarVEmpty + gs % kS));
+        }
+        g += ns;
+        ++q;
+      }
+    } else {
+      for (int k = 0; ok; ++k) {
+        int x;
+        if (!item_of(k, num_items, &x)) break;
+        const Pair it = pair_geom(args, x);
+        const int ns = it.ns;
+        if (ns == 0) continue;
+        // the item's first QK^T: issued behind the previous item's last P.V
+        // (in order on the tensor core, so that P.V has read P before S lands
+        // in the same columns)
+        ok = mbar_wait_w(bar(C::kBarQFull), q & 1, abort_flag);
+        ensure_k(g);
         if (!ok) break;
         tc_fence_after();
 #pragma unroll
-        for (int t = 0; t < 2; ++t) {
-          const int u = jj - it.a[t];  // tile-local step
-          if (!ok || u < 0 || u >= it.n[t]) continue;
-          ok = mbar_wait_w(bar(C::kBarPFull + t), ut[t] & 1, abort_flag);
+        for (int t = 0; t < 2; ++t)
+          if (it.n[t] > 0 && it.a[t] == 0) issue_s(t, g);
+        mma_commit_w(bar(C::kBarKEmpty + g % kS));
+        if (ns == 1) mma_commit_w(bar(C::kBarQFree));
+        for (int jj = 0; jj < ns && ok; ++jj) {
+          const int gs = g + jj;
+          ok = mbar_wait_w(bar(C::kBarVFull + gs % kS), (gs / kS) & 1, abort_flag);
           if (!ok) break;
           tc_fence_after();
-          issue_pv(t, gs, u == 0);
-          ++ut[t];
-          if (u + 1 < it.n[t]) {
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            const int u = jj - it.a[t];  // tile-local step
+            if (!ok || u < 0 || u >= it.n[t]) continue;
+            ok = mbar_wait_w(bar(C::kBarPFull + t), ut[t] & 1, abort_flag);
+            if (!ok) break;
+            tc_fence_after();
+            issue_pv(t, gs, u == 0);
+            ++ut[t];
+            if (u + 1 < it.n[t]) {
+              ensure_k(gs + 1);
+              if (!ok) break;
+              issue_s(t, gs + 1);
+            } else {
+              mma_commit_w(bar(C::kBarOFinal + t));
+            }
+          }
+          if (!ok) break;
+          // a tile whose range starts at the next step (a window's later start)
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            if (!ok || it.n[t] == 0 || it.a[t] != jj + 1) continue;
             ensure_k(gs + 1);
             if (!ok) break;
             issue_s(t, gs + 1);
-          } else {
-            mma_commit_w(bar(C::kBarOFinal + t));
           }
-        }
-        if (!ok) break;
-        // a tile whose range starts at the next step (a window's later start)
-#pragma unroll
-        for (int t = 0; t < 2; ++t) {
-          if (!ok || it.n[t] == 0 || it.a[t] != jj + 1) continue;
-          ensure_k(gs + 1);
           if (!ok) break;
-          issue_s(t, gs + 1);
+          // every QK^T of the item has been issued: its Q buffer is free once they complete
+          if (jj == ns - 2) mma_commit_w(bar(C::kBarQFree));
+          mma_commit_w(bar(C::kBarVEmpty + gs % kS));
+          if (jj + 1 < ns) mma_commit_w(bar(C::kBarKEmpty + (gs + 1) % kS));
         }
-        if (!ok) break;
-        // every QK^T of the item has been issued: its Q buffer is free once they complete
-        if (jj == ns - 2) mma_commit_w(bar(C::kBarQFree));
-        mma_commit_w(bar(C::kBarVEmpty + gs % kS));
-        if (jj + 1 < ns) mma_commit_w(bar(C::kBarKEmpty + (gs + 1) % kS));
+        g += ns;
+        ++q;
       }
-      g += ns;
-      ++q;
     }
     // Let every MMA this warp issued finish before TMEM is released.
     mma_commit_w(bar(C::kBarDrain));
@@ -1627,7 +1701,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int t = warp / 4;  // query tile
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + lane_base + t * 128;
-    const uint32_t tO = tmem + lane_base + C::kColO + t * kDV;
+    const uint32_t tO = tmem + lane_base + C::kColO + t * DV;
+    const uint32_t tP = tmem + lane_base + C::kColP + t * 64;  // separate P only
     const float sl2 = args.scale_log2;
     const float2 sl2x2 = make_float2(sl2, sl2);
     // this warp's staging block: 32 rows x 64 columns of O, 128-byte rows
@@ -1662,6 +1737,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, sr[c]);
 #pragma unroll
         for (int c = 0; c < 4; ++c) tmem_ld_wait(sr[c]);
+        if constexpr (C::kSepP) {  // S is in registers: the tile's next QK^T may overwrite it
+          tc_fence_before();
+          mbar_arrive_warp(bar(C::kBarSFree + t));
+        }
         float xs[128];
 #pragma unroll
         for (int c = 0; c < 128; ++c) xs[c] = __uint_as_float(sr[c >> 5][c & 31]);
@@ -1688,7 +1767,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float alpha = need ? ex2(m_old - m_ref) : 1.0f;
         const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
         // p = exp2(s * scale * log2(e) - m_ref), packed two at a time; P
-        // columns [32 h, 32 h + 32) hold scores [64 h, 64 h + 64), over S
+        // columns [32 h, 32 h + 32) hold scores [64 h, 64 h + 64), over S or
+        // in P's own columns once the tile's previous P.V has read them
         const float2 negm = make_float2(-m_use, -m_use);
         float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
         uint32_t pk[32];
@@ -1703,14 +1783,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             else acc0 = __fadd2_rn(acc0, pr);
             pk[c] = pack_bf16(pr.x, pr.y);
           }
-          tmem_st32(tS + 32 * h, pk);
+          if constexpr (C::kSepP) {
+            if (h == 0 && ut > 0) {
+              ok = mbar_wait(bar(C::kBarPVDone + t), (ut - 1) & 1, abort_flag);
+              ok = __all_sync(0xffffffffu, ok);
+              if (!ok) break;
+              tc_fence_after();
+            }
+            tmem_st32(tP + 32 * h, pk);
+          } else {
+            tmem_st32(tS + 32 * h, pk);
+          }
         }
+        if (!ok) break;
         l = alpha * l + ((acc0.x + acc0.y) + (acc1.x + acc1.y));
         // Rescale the accumulator when this warp's maximum moved. O is
-        // settled: this S was committed after the tile's previous P.V.
+        // settled: this S was committed after the tile's previous P.V (P over
+        // S), or that P.V's completion was waited for above (separate P).
         if (u > 0 && __any_sync(0xffffffffu, need)) {
 #pragma unroll
-          for (int c = 0; c < kDV / 32; ++c) {
+          for (int c = 0; c < DV / 32; ++c) {
             uint32_t o[32];
             tmem_ld32(tO + c * 32, o);
             tmem_ld_wait(o);
@@ -1732,7 +1824,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       // write-back once the item's last P.V for this tile has completed; the
       // tile's next P.V (next item) waits for this warpgroup's next P, so O is
       // read out before it is overwritten
-      ok = mbar_wait(bar(C::kBarOFinal + t), qt & 1, abort_flag);
+      if constexpr (C::kSepP)
+        ok = mbar_wait(bar(C::kBarPVDone + t), (ut - 1) & 1, abort_flag);
+      else
+        ok = mbar_wait(bar(C::kBarOFinal + t), qt & 1, abort_flag);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
@@ -1742,10 +1837,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float2 il2 = make_float2(inv_l, inv_l);
       // each warp swizzles its 32 rows, 64 columns at a time, into its staging
       // block and writes them back as four whole lines per instruction
-      __nv_bfloat16* obase = args.o + static_cast<size_t>(bh) * Nq * kDV;
+      __nv_bfloat16* obase = args.o + static_cast<size_t>(bh) * Nq * DV;
       const int wrow0 = row - lane;  // first row of this warp
 #pragma unroll
-      for (int h = 0; h < kDV / 64; ++h) {
+      for (int h = 0; h < DV / 64; ++h) {
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           uint32_t o[32];
@@ -1770,7 +1865,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int r = 4 * j + (lane >> 3), v = lane & 7;
           const uint4 val = *reinterpret_cast<const uint4*>(stage_blk + r * 128 + ((v ^ (r & 7)) * 16));
           if (wrow0 + r < Nq)
-            *reinterpret_cast<uint4*>(obase + static_cast<size_t>(wrow0 + r) * kDV + h * 64 + v * 8) = val;
+            *reinterpret_cast<uint4*>(obase + static_cast<size_t>(wrow0 + r) * DV + h * 64 + v * 8) = val;
         }
         __syncwarp();  // the block is read back before it is written again
       }
@@ -1841,22 +1936,23 @@ int launch_fwd_persist(const FwdProblem& p, void* o, float* lse, cudaStream_t st
   return cudaGetLastError() == cudaSuccess && e == cudaSuccess ? 0 : -3;
 }
 
-// The persistent two-tile forward (d_v = 128, whole key range): one
+// The persistent two-tile forward (whole key range): one
 // CTA per SM walks its share of the query-tile pairs.
-template <int D>
+template <int D, int DV>
 int launch_fwd_persist2(const FwdProblem& p, void* o, float* lse, cudaStream_t stream) {
-  using C = pq::Cfg<D>;
+  using C = pq::Cfg<D, DV>;
   const int BH = p.B * p.H;
   CUtensorMap mq, mk, mv;
   if (!make_map_bhnd(&mq, p.q, BH, p.Nq, D) || !make_map_bhnd(&mk, p.k, BH, p.Nk, D) ||
-      !make_map_bhnd(&mv, p.v, BH, p.Nk, pq::kDV))
+      !make_map_bhnd(&mv, p.v, BH, p.Nk, DV))
     return -3;
   int* status = device_status_word();
   const int sms = device_sm_count();
   if (!status || sms <= 0) return -3;
-  auto kern = pq::fa_fwd_persist2<D>;
-  // attribute slots 17 and 18 (the other kernels use 0-16)
-  if (!ensure_smem_attr(reinterpret_cast<const void*>(kern), C::kSmemBytes, D == 128 ? 17 : 18)) return -3;
+  auto kern = pq::fa_fwd_persist2<D, DV>;
+  // attribute slots 17-19 (the other kernels use 0-16)
+  constexpr int kSlot = DV == 64 ? 19 : (D == 128 ? 17 : 18);
+  if (!ensure_smem_attr(reinterpret_cast<const void*>(kern), C::kSmemBytes, kSlot)) return -3;
   FwdArgs a{};
   a.o = static_cast<__nv_bfloat16*>(o);
   a.lse = lse;
@@ -1989,18 +2085,21 @@ int launch_fwd_general(const FwdProblem& p, void* o, float* lse, float* part_o, 
       return launch_fwd_persist<false>(p, o, lse, stream);
     return launch_fwd_d<64, 64, 2>(p, o, lse, part_o, part_lse, n_splits, stream);
   }
-  // d_v = 128 over the whole key range (and no query before the first key
-  // when causal): two query tiles at a time, one persistent CTA per SM
+  // d or d_v = 128 over the whole key range (and no query before the first
+  // key when causal): two query tiles at a time, one persistent CTA per SM
   const bool persist2 = part_o == nullptr && (!p.causal || p.Nk >= p.Nq);
   if (p.d == 128 && p.dv == 128) {
-    if (persist2) return launch_fwd_persist2<128>(p, o, lse, stream);
+    if (persist2) return launch_fwd_persist2<128, 128>(p, o, lse, stream);
     return launch_fwd_d<128, 128, 2>(p, o, lse, part_o, part_lse, n_splits, stream);
   }
   // d = d_v = 256: one query tile per CTA (S 128 + O 256 tensor-memory columns)
   if (p.d == 256 && p.dv == 256) return launch_fwd_d<256, 256, 1>(p, o, lse, part_o, part_lse, n_splits, stream);
-  if (p.d == 128 && p.dv == 64) return launch_fwd_d<128, 64, 2>(p, o, lse, part_o, part_lse, n_splits, stream);
+  if (p.d == 128 && p.dv == 64) {
+    if (persist2) return launch_fwd_persist2<128, 64>(p, o, lse, stream);
+    return launch_fwd_d<128, 64, 2>(p, o, lse, part_o, part_lse, n_splits, stream);
+  }
   if (p.d == 64 && p.dv == 128) {
-    if (persist2) return launch_fwd_persist2<64>(p, o, lse, stream);
+    if (persist2) return launch_fwd_persist2<64, 128>(p, o, lse, stream);
     return launch_fwd_d<64, 128, 2>(p, o, lse, part_o, part_lse, n_splits, stream);
   }
   return -2;
