@@ -205,8 +205,10 @@ __global__ void __launch_bounds__(256) fa_bwd_post(const float* __restrict__ acc
 //   warp  13   TMA producer; warps 14-15 idle
 // TMEM columns: S^T/P^T [0,128), dP^T and dQ [128,256), dK [256,384),
 // dV [384,512).
-// Every wait sleeps in hardware (mbar_wait_sleep): with these longer steps,
-// polling warps take more issue slots than a later wake-up costs.
+// Every wait polls (the issuing warps converged, one verdict per warp): a
+// wait that sleeps in hardware wakes later than a poll notices the phase,
+// and on this kernel's chain of hand-offs per step that cost more than the
+// issue slots polling takes.
 namespace wide {
 
 constexpr int kHalf = 64;  // query columns per P/dS warpgroup
@@ -333,7 +335,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int it = 0; it < n_steps; ++it) {
         const int s = it % C::kStages;
         if (it >= C::kStages)
-          ok = mbar_wait_sleep(bar(C::kBarQEmpty + s), ((it / C::kStages) + 1) & 1, abort_flag);
+          ok = mbar_wait(bar(C::kBarQEmpty + s), ((it / C::kStages) + 1) & 1, abort_flag);
         if (!ok) break;
 #ifdef FA_TEST_SKIP_ARRIVE
         // Test-only build (never in libfa.so): the item's last query step is
@@ -364,11 +366,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t kIdK = idesc_bf16_f32(kBlk, D, false, true);      // dK
       constexpr uint32_t kIdQ = idesc_bf16_f32(kBlk, D, true, true);       // dQ
       const uint32_t kb = base + C::kKOff, vb = base + C::kVOff, dsb = base + C::kDSOff;
-      bool ok = mbar_wait_sleep_w(bar(C::kBarKV), 0, abort_flag);
+      bool ok = mbar_wait_w(bar(C::kBarKV), 0, abort_flag);
       tc_fence_after();
       for (int it = 0; it < n_steps && ok; ++it) {
         const int s = it % C::kStages;
-        ok = mbar_wait_sleep_w(bar(C::kBarQFull + s), (it / C::kStages) & 1, abort_flag);
+        ok = mbar_wait_w(bar(C::kBarQFull + s), (it / C::kStages) & 1, abort_flag);
         if (!ok) break;
         tc_fence_after();
         const uint32_t qb = base + C::kStageOff + s * C::kStageBytes;
@@ -384,7 +386,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                    sdesc_sw128(qb + off + h * 8192, 16, 1024), kIdT, kk > 0 ? 1u : 0u);
           }
           if (C::kDqAliasDp && h == 0 && it > 0) {  // dQ of the last step shares dP's columns
-            ok = mbar_wait_sleep_w(bar(C::kBarDQEmpty), (it - 1) & 1, abort_flag);
+            ok = mbar_wait_w(bar(C::kBarDQEmpty), (it - 1) & 1, abort_flag);
             if (!ok) break;
             tc_fence_after();
           }
@@ -399,14 +401,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          ok = mbar_wait_sleep_w(bar(C::kBarDSFull + h), it & 1, abort_flag);
+          ok = mbar_wait_w(bar(C::kBarDSFull + h), it & 1, abort_flag);
           if (!ok) break;
           tc_fence_after();
           if (h == 1) {
             // dQ as soon as both dS halves are written: its read-out gates the
             // next step (dQ shares the dP^T columns at d = 128)
             if (!C::kDqAliasDp && it > 0) {
-              ok = mbar_wait_sleep_w(bar(C::kBarDQEmpty), (it - 1) & 1, abort_flag);
+              ok = mbar_wait_w(bar(C::kBarDQEmpty), (it - 1) & 1, abort_flag);
               if (!ok) break;
               tc_fence_after();
             }
@@ -472,8 +474,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       // the stage's vectors arrive with its Q/dO tiles; S^T, dP^T with the MMA commit
-      ok = mbar_wait_sleep(bar(C::kBarQFull + it % C::kStages), (it / C::kStages) & 1, abort_flag);
-      if (ok) ok = mbar_wait_sleep(bar(C::kBarSFull + w), it & 1, abort_flag);
+      ok = mbar_wait(bar(C::kBarQFull + it % C::kStages), (it / C::kStages) & 1, abort_flag);
+      if (ok) ok = mbar_wait(bar(C::kBarSFull + w), it & 1, abort_flag);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
@@ -542,7 +544,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float scale = args.scale;
     bool ok = true;
     for (int it = 0; it < n_steps; ++it) {
-      ok = mbar_wait_sleep(bar(C::kBarDQFull), it & 1, abort_flag);
+      ok = mbar_wait(bar(C::kBarDQFull), it & 1, abort_flag);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
@@ -567,7 +569,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     if (ok) {
-      ok = mbar_wait_sleep(bar(C::kBarDKDV), 0, abort_flag);
+      ok = mbar_wait(bar(C::kBarDKDV), 0, abort_flag);
       ok = __all_sync(0xffffffffu, ok);
     }
     if (ok) {
