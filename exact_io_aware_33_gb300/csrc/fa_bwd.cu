@@ -240,8 +240,8 @@ struct BwdCfg {
   static constexpr int kBarSFull = kBarQEmpty + kStages;    // one per query half
   static constexpr int kBarDSFull = kBarSFull + 2;           // one per query half
   static constexpr int kBarDQFull = kBarDSFull + 2;
-  static constexpr int kBarDQEmpty = kBarDQFull + 1;
-  static constexpr int kBarDKDV = kBarDQEmpty + 1;
+  static constexpr int kBarDQEmpty = kBarDQFull + 1;  // two: dQ columns [0, d/2), [d/2, d) read out
+  static constexpr int kBarDKDV = kBarDQEmpty + 2;
   static constexpr int kBarDrain = kBarDKDV + 1;
   static constexpr int kNumBars = kBarDrain + 1;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
@@ -303,6 +303,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(bar(C::kBarDQFull), 1);
     mbar_init(bar(C::kBarDQEmpty), 4);
+    mbar_init(bar(C::kBarDQEmpty + 1), 4);
     mbar_init(bar(C::kBarDKDV), 1);
     mbar_init(bar(C::kBarDrain), 1);
     *abort_flag = 0;
@@ -385,8 +386,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_ss_w(tmem + C::kColS + kHalf * h, sdesc_sw128(kb + off, 16, 1024),
                    sdesc_sw128(qb + off + h * 8192, 16, 1024), kIdT, kk > 0 ? 1u : 0u);
           }
-          if (C::kDqAliasDp && h == 0 && it > 0) {  // dQ of the last step shares dP's columns
-            ok = mbar_wait_w(bar(C::kBarDQEmpty), (it - 1) & 1, abort_flag);
+          if (C::kDqAliasDp && it > 0) {  // dQ of the last step shares dP's columns, half by half
+            ok = mbar_wait_w(bar(C::kBarDQEmpty + h), (it - 1) & 1, abort_flag);
             if (!ok) break;
             tc_fence_after();
           }
@@ -408,7 +409,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // dQ as soon as both dS halves are written: its read-out gates the
             // next step (dQ shares the dP^T columns at d = 128)
             if (!C::kDqAliasDp && it > 0) {
-              ok = mbar_wait_w(bar(C::kBarDQEmpty), (it - 1) & 1, abort_flag);
+              ok = mbar_wait_w(bar(C::kBarDQEmpty + 1), (it - 1) & 1, abort_flag);
               if (!ok) break;
               tc_fence_after();
             }
@@ -554,9 +555,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t g[32];
         tmem_ld32(tmem + lane_base + C::kColDQ + c * 32, g);
         tmem_ld_wait(g);
-        if (c == D / 32 - 1) {  // dQ has left tensor memory: its columns are free
+        if (c == D / 64 - 1 || c == D / 32 - 1) {  // half of dQ has left tensor memory
           tc_fence_before();
-          mbar_arrive_warp(bar(C::kBarDQEmpty));
+          mbar_arrive_warp(bar(C::kBarDQEmpty + (c == D / 32 - 1 ? 1 : 0)));
         }
         if (q < N) {
 #pragma unroll
