@@ -115,3 +115,41 @@ def test_backward_wait_runs_out_and_the_context_survives(timeout_lib, d):
     for t, ref in zip(got, refs):
         gg = t.float().cpu().double().numpy()
         assert np.abs(gg - ref).max() / np.abs(ref).max() <= 5e-2
+
+
+@pytest.mark.parametrize("d,dv,window", [(128, 64, 0), (64, 128, 0), (128, 128, 200)])
+def test_forward_ex_wait_runs_out_and_the_context_survives(timeout_lib, d, dv, window):
+    # The persistent two-tile forward's other forms: P in columns of its own
+    # (d_v = 64), d = 64 with d_v = 128, and a window (tiles starting at
+    # different key tiles); causal, N = 512.
+    from oracle import general
+    B, H, N, scale = 1, 2, 512, 1.0 / math.sqrt(d)
+    gen = torch.Generator().manual_seed(3300 + d + dv + window)
+    x = {"q": torch.randn(B, H, N, d, generator=gen).to(torch.bfloat16),
+         "k": torch.randn(B, H, N, d, generator=gen).to(torch.bfloat16),
+         "v": torch.randn(B, H, N, dv, generator=gen).to(torch.bfloat16)}
+    g = {n: t.cuda() for n, t in x.items()}
+    o = torch.empty(B, H, N, dv, dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty(B, H, N, dtype=torch.float32, device="cuda")
+    torch.cuda.synchronize()
+    assert fa.fa_get_last_device_status() == fa.FA_OK
+
+    t0 = time.perf_counter()
+    rc = timeout_lib.fa_fwd_ex(_p(g["q"]), _p(g["k"]), _p(g["v"]), _p(o), _p(lse), B, H, N, N, d, dv, 1,
+                               window, scale, ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert rc == fa.FA_OK
+    status = timeout_lib.fa_get_last_device_status()
+    elapsed = time.perf_counter() - t0
+    assert status == fa.FA_ERR_TIMEOUT
+    assert elapsed < 10.0, f"the wind-down took {elapsed:.2f} s"
+    assert timeout_lib.fa_get_last_device_status() == fa.FA_OK
+    assert fa.fa_get_last_device_status() == fa.FA_OK
+
+    # the product library's forward in the same process, against the oracle
+    o2, lse2 = fa.fa_fwd_ex(g["q"], g["k"], g["v"], causal=True, window=window, scale=scale)
+    torch.cuda.synchronize()
+    assert fa.fa_get_last_device_status() == fa.FA_OK
+    o_ref, lse_ref = general.forward(x["q"], x["k"], x["v"], True, scale, window)
+    err = np.abs(o2.float().cpu().double().numpy() - o_ref)
+    assert err.max() <= 2e-2 and err.mean() <= 2e-3
+    assert np.abs(lse2.cpu().double().numpy() - lse_ref).max() <= 1e-3
