@@ -96,8 +96,9 @@ def test_workload_full_size(idx):
     assert bool((of <= vmax + slack).all()) and bool((of >= vmin - slack).all())
 
 
-def test_scale_zero_is_uniform_average():
-    x = si.make_small(1, 2, 300, 64, seed=5, with_grad=False)
+@pytest.mark.parametrize("d", [64, 128])
+def test_scale_zero_is_uniform_average(d):
+    x = si.make_small(1, 2, 300, d, seed=5, with_grad=False)
     for causal in (False, True):
         o, lse = _run(x, causal, 0.0)
         o_ref, lse_ref = dense.forward(x["q"], x["k"], x["v"], causal, 0.0)
@@ -113,16 +114,18 @@ def test_large_scores_move_the_maximum():
         _compare(o, lse, o_ref, lse_ref)
 
 
-def test_deterministic():
-    x = si.make_small(2, 3, 777, 64, seed=11, with_grad=False)
+@pytest.mark.parametrize("d", [64, 128])
+def test_deterministic(d):
+    x = si.make_small(2, 3, 777, d, seed=11, with_grad=False)
     o1, l1 = _run(x, True, 0.125)
     o2, l2 = _run(x, True, 0.125)
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
 
 
-def test_rows_beyond_n_untouched():
+@pytest.mark.parametrize("d", [64, 128])
+def test_rows_beyond_n_untouched(d):
     # outputs live in a larger buffer; the bytes after the problem stay as set
-    B, H, N, d = 1, 1, 200, 64
+    B, H, N = 1, 1, 200
     x = si.make_small(B, H, N, d, seed=13, with_grad=False)
     g = _gpu(x)
     big = torch.full((B * H * N * d + 4096,), float("nan"), dtype=torch.bfloat16, device="cuda")
