@@ -2085,8 +2085,9 @@ int launch_fwd_general(const FwdProblem& p, void* o, float* lse, float* part_o, 
       return launch_fwd_persist<false>(p, o, lse, stream);
     return launch_fwd_d<64, 64, 2>(p, o, lse, part_o, part_lse, n_splits, stream);
   }
-  // d or d_v = 128 over the whole key range (and no query before the first
-  // key when causal): two query tiles at a time, one persistent CTA per SM
+  // d or d_v = 128 over the whole key range: two query tiles at a time, one
+  // persistent CTA per SM (the argument checks leave no causal query before
+  // the first key, which the persistent form relies on)
   const bool persist2 = part_o == nullptr && (!p.causal || p.Nk >= p.Nq);
   if (p.d == 128 && p.dv == 128) {
     if (persist2) return launch_fwd_persist2<128, 128>(p, o, lse, stream);
